@@ -1,0 +1,196 @@
+/*
+ * irm_oracle.c -- reference oracle for delta-rotated MLA KV reconstruction.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, the smoke check and the benchmark's CPU
+ * baseline may load this library.  The product path never calls it, and it shares no
+ * code, header, table or constant with the CUDA path.
+ *
+ * Plain fp64 loops; OpenMP only over independent query rows.  No blocking, fusion or
+ * reordering beyond the definitions below, so each step can be read against the pages.
+ *
+ * Pages cited (the web pages describing the method):
+ *   [walkthrough] "Irminsul论文详解：面向Agentic LLM Serving的MLA原生位置无关缓存"
+ *                 (gentlecold.top), sections numbered as on the page;
+ *   [summary]     "Irminsul: MLA-Native Position-Independent Caching for Agentic LLM
+ *                 Serving" (gist.science, French and Korean technical summary), sections
+ *                 numbered as on the page.
+ *
+ * What is computed:
+ *   - a KV row is [cKV (512, position-free) | k_r (64, RoPE slice)]     [walkthrough §4],
+ *                                                                        [summary §2.1]
+ *   - a reused chunk at target position p_tgt, cached at p_src, has
+ *     delta = p_tgt - p_src and k_r,rot = R(delta) k_r,base, because
+ *     R(delta) R(p_src) = R(p_tgt); cKV is reused untouched            [walkthrough §4, §15],
+ *                                                                        [summary §2.2]
+ *   - the assembly loop appends, per segment, either freshly prefilled rows or the
+ *     cached rows with rotated k_r; positions below 32 are always fresh [walkthrough §5, §7]
+ *   - absorbed MLA attention: scores use [cKV | k_r] against [q_lat | q_rope], the output
+ *     is the softmax-weighted sum of cKV (W_UV applied outside)          [walkthrough §4]
+ * Readings where the pages are silent (each is also listed in the design notes):
+ *   - RoPE convention: NeoX half split, pair j couples dims (j, j+32), frequency
+ *     theta_j = 10000^(-2j/64), j = 0..31; R(p) turns pair j by angle +p*theta_j.
+ *   - a fresh row (reused = 0) has delta = 0 and is passed through unchanged.
+ *   - softmax scale is a caller argument (1/sqrt(192) for the configurations used here).
+ *   - query i of n_q sits at position ctx - n_q + i and sees keys t <= that position.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef int64_t i64;
+
+#define D_LAT 512
+#define D_ROPE 64
+#define D_ROW 576
+#define N_PAIRS 32
+#define CARVE_OUT 32
+
+/* bf16 bit pattern -> fp64, exact: the bf16 value is the top half of an IEEE float. */
+static double bf16_to_f64(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* RoPE frequencies, NeoX half split: theta_j = 10000^(-2j/64).  (reading, see header) */
+void oracle_rope_theta(double *theta) {
+  for (int j = 0; j < N_PAIRS; ++j) theta[j] = pow(10000.0, -2.0 * (double)j / (double)D_ROPE);
+}
+
+/* R(angle_scale) applied to one 64-d row: pair j = (x_j, x_{j+32}) is turned by
+ * angle_scale * theta_j.  Used both for R(delta) [walkthrough §4] and for R(p). */
+static void rotate_row(const double *k, i64 steps, const double *theta, double *out) {
+  for (int j = 0; j < N_PAIRS; ++j) {
+    double ang = (double)steps * theta[j];
+    double c = cos(ang), s = sin(ang);
+    double x = k[j], y = k[j + N_PAIRS];
+    out[j] = x * c - y * s;
+    out[j + N_PAIRS] = x * s + y * c;
+  }
+}
+
+/* out[r] = R(steps[r]) k[r] for n rows of 64 values. */
+void oracle_rotate(const double *k, i64 n, const i64 *steps, double *out) {
+  double theta[N_PAIRS];
+  oracle_rope_theta(theta);
+  for (i64 r = 0; r < n; ++r) rotate_row(k + r * D_ROPE, steps[r], theta, out + r * D_ROPE);
+}
+
+/*
+ * Assembly plan [walkthrough §5 pseudo-code, §4 delta rule].
+ * Chunk table of all requests, concatenated; request b owns chunks [indptr[b], indptr[b+1])
+ * listed in target order.  For target row t of chunk c:
+ *   src_row = pool_offset_c + (t - p_tgt_c)
+ *   delta   = reused_c ? p_tgt_c - p_src_c : 0
+ *   pos_src = t - delta
+ * Rows are written request after request (row offset of request b = sum of earlier ctx).
+ * Returns 0, or -1 if a request's chunks do not tile [0, ctx) in order, or -2 if a reused
+ * chunk covers a position below 32 (the carve-out is always prefilled [walkthrough §7]).
+ */
+int oracle_plan(i64 B, const i64 *indptr, const i64 *pool_offset, const i64 *len,
+                const i64 *p_src, const i64 *p_tgt, const uint8_t *reused, i64 *ctx_out,
+                i64 *src_row, i64 *delta, i64 *pos_src) {
+  i64 row = 0;
+  for (i64 b = 0; b < B; ++b) {
+    i64 expect = 0;
+    for (i64 c = indptr[b]; c < indptr[b + 1]; ++c) {
+      if (p_tgt[c] != expect || len[c] <= 0) return -1;
+      if (reused[c] && p_tgt[c] < CARVE_OUT) return -2;
+      for (i64 i = 0; i < len[c]; ++i) {
+        i64 t = p_tgt[c] + i;
+        i64 d = reused[c] ? p_tgt[c] - p_src[c] : 0;
+        src_row[row] = pool_offset[c] + i;
+        delta[row] = d;
+        pos_src[row] = t - d;
+        ++row;
+      }
+      expect += len[c];
+    }
+    ctx_out[b] = expect;
+  }
+  return 0;
+}
+
+/*
+ * Assembled KV rows in fp64: out[r] = [cKV(src_row[r]) | R(delta[r]) k_r(src_row[r])].
+ * kv_rows is the bf16 row store [n_rows, 576]; cKV is only widened, never modified.
+ */
+void oracle_assemble(const uint16_t *kv_rows, i64 n, const i64 *src_row, const i64 *delta,
+                     double *out) {
+  double theta[N_PAIRS];
+  oracle_rope_theta(theta);
+#pragma omp parallel for schedule(static)
+  for (i64 r = 0; r < n; ++r) {
+    const uint16_t *src = kv_rows + src_row[r] * D_ROW;
+    double *dst = out + r * D_ROW;
+    double kr[D_ROPE];
+    for (int d = 0; d < D_LAT; ++d) dst[d] = bf16_to_f64(src[d]);
+    for (int d = 0; d < D_ROPE; ++d) kr[d] = bf16_to_f64(src[D_LAT + d]);
+    if (delta[r] == 0) {
+      for (int d = 0; d < D_ROPE; ++d) dst[D_LAT + d] = kr[d];
+    } else {
+      rotate_row(kr, delta[r], theta, dst + D_LAT);
+    }
+  }
+}
+
+/*
+ * Absorbed MLA attention for R query rows [walkthrough §4].
+ *   q[r]    = [q_lat | q_rope] of row r, fp64 [576]
+ *   K       = assembled rows of one request, fp64 [ctx, 576]
+ *   visible = number of keys row r sees (keys 0..visible-1)
+ *   s_t = scale * (q_lat . cKV_t + q_rope . k_r,t)
+ *   O   = sum_t exp(s_t - m) cKV_t / sum_t exp(s_t - m),  m = max_t s_t
+ *   lse = m + ln sum_t exp(s_t - m)
+ */
+void oracle_attn(const double *q, const i64 *visible, i64 R, const double *K, i64 ctx,
+                 double scale, double *O, double *lse) {
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (i64 r = 0; r < R; ++r) {
+      const double *qr = q + r * D_ROW;
+      i64 n = visible[r];
+      double m = -INFINITY;
+      for (i64 t = 0; t < n; ++t) {
+        const double *kt = K + t * D_ROW;
+        double acc = 0.0;
+        for (int d = 0; d < D_ROW; ++d) acc += qr[d] * kt[d];
+        s[t] = acc * scale;
+        if (s[t] > m) m = s[t];
+      }
+      double *o = O + r * D_LAT;
+      for (int d = 0; d < D_LAT; ++d) o[d] = 0.0;
+      double l = 0.0;
+      for (i64 t = 0; t < n; ++t) {
+        double p = exp(s[t] - m);
+        l += p;
+        const double *kt = K + t * D_ROW;
+        for (int d = 0; d < D_LAT; ++d) o[d] += p * kt[d];
+      }
+      for (int d = 0; d < D_LAT; ++d) o[d] /= l;
+      lse[r] = m + log(l);
+    }
+    free(s);
+  }
+}
+
+/* Widen bf16 bit patterns to fp64 (n values). */
+void oracle_widen(const uint16_t *src, i64 n, double *dst) {
+  for (i64 i = 0; i < n; ++i) dst[i] = bf16_to_f64(src[i]);
+}
+
+/* Number of threads OpenMP would use (reported with timings). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
