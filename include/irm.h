@@ -1,0 +1,183 @@
+/*
+ * irm.h -- C ABI of the GB300 (sm_103a) reuse-time MLA KV reconstruction library.
+ *
+ * The method (Irminsul, position-independent caching for MLA models): a request's KV is
+ * rebuilt from a content-addressed chunk pool.  Every KV row is [cKV (512 bf16,
+ * position-free) | k_r (64 bf16, RoPE slice)].  A chunk cached at source position p_src
+ * and reused at target position p_tgt keeps its cKV rows untouched and has its k_r rows
+ * rotated in closed form by R(delta), delta = p_tgt - p_src, because
+ * R(delta) R(p_src) = R(p_tgt).  Positions 0..31 are always freshly prefilled.
+ *   Passages: "Irminsul论文详解：面向Agentic LLM Serving的MLA原生位置无关缓存"
+ *   (gentlecold.top) §4 (row split, delta rule), §5 (assembly loop), §7 (carve-out),
+ *   §15 (worked example); "Irminsul: MLA-Native Position-Independent Caching for Agentic
+ *   LLM Serving" (gist.science technical summary) §2.1-2.2.
+ *
+ * Conventions fixed here where the pages are silent:
+ *   - RoPE is the NeoX half split: pair j couples k_r[j] and k_r[j+32] and turns by
+ *     angle delta * theta_j, theta_j = 10000^(-2j/64), j = 0..31.  Rotation math is fp32,
+ *     the rotated k_r is rounded to bf16 (round to nearest even) once.
+ *   - A fresh chunk (reused = 0) has delta = 0; its p_src is ignored.
+ *   - Query i of n_q sits at position ctx - n_q + i and sees keys t <= that position.
+ *
+ * Memory and streams.  All pointers named *_dev / device are device memory owned by the
+ * caller; pointers named *_host are host memory owned by the caller.  The library keeps
+ * no allocation of its own and performs no host<->device copy: a chunk table is passed
+ * twice, as the host copy (validated and used for launch geometry) and as a byte-identical
+ * device copy (read by the kernels).  Every call is asynchronous on `stream`.  Kernels
+ * re-check each source row against n_rows and record (never fault on) a violation.
+ *
+ * Errors.  Calls return an irm_status.  No exception crosses the ABI and nothing aborts.
+ * Host-side checks happen before any launch.  Device-side problems (a source row out of
+ * range because the device table differs from the host table, or a pipeline wait that
+ * exceeded its 2 s limit) set bits in the status word at the start of the workspace; read
+ * and clear it with irm_device_status().
+ *
+ * Workspace.  Each call takes a caller-owned device workspace of at least the size its
+ * *_workspace_size function reports (>= IRM_WORKSPACE_HEADER bytes).  Its first
+ * IRM_WORKSPACE_HEADER bytes hold the device status word: zero them once before first use.
+ */
+#ifndef IRM_H_
+#define IRM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t; /* identical to the CUDA runtime's typedef */
+
+#define IRM_D_LAT 512        /* cKV width */
+#define IRM_D_ROPE 64        /* k_r width */
+#define IRM_D_ROW 576        /* KV row width, elements (1152 bytes in bf16) */
+#define IRM_PAGE_ROWS 64     /* rows per page of the paged KV layout */
+#define IRM_CARVE_OUT 32     /* positions 0..31 are always fresh */
+#define IRM_MAX_HEADS 128
+#define IRM_WORKSPACE_HEADER 256
+
+typedef enum irm_status {
+  IRM_OK = 0,
+  IRM_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size or count */
+  IRM_ERR_CHUNK_TABLE = -2,    /* chunks do not tile [0, ctx) in order, len <= 0, rows out of range */
+  IRM_ERR_CARVEOUT = -3,       /* a reused chunk covers a position < 32 */
+  IRM_ERR_UNSUPPORTED = -4,    /* shape outside what the kernels implement */
+  IRM_ERR_CUDA = -5,           /* a CUDA runtime call failed (see irm_last_error) */
+  IRM_ERR_DEVICE_TIMEOUT = -6, /* a device pipeline wait ran out (from irm_device_status) */
+  IRM_ERR_DEVICE_BOUNDS = -7,  /* a kernel met a source row outside the row store */
+  IRM_ERR_WORKSPACE = -8       /* workspace missing or smaller than required */
+} irm_status;
+
+/* One chunk of a request's table, listed in target order [walkthrough §5].
+ * Rows pool_offset .. pool_offset+len-1 of the row store become target positions
+ * p_tgt .. p_tgt+len-1.  24 bytes, naturally aligned. */
+typedef struct irm_chunk {
+  int64_t pool_offset; /* first row of the chunk in the row store */
+  int32_t len;         /* rows, > 0 */
+  int32_t p_src;       /* position the cached k_r rows were encoded at (reused chunks) */
+  int32_t p_tgt;       /* target position of the first row; chunks tile [0, ctx) in order */
+  uint8_t reused;      /* 1: cached chunk, k_r rotated by p_tgt - p_src; 0: fresh */
+  uint8_t pad[3];
+} irm_chunk;
+
+/* Text for a status code (static storage). */
+const char* irm_status_string(int status);
+
+/* Detail of the last error raised on the calling thread ("" if none). */
+const char* irm_last_error(void);
+
+/* Library build identifier: "irm <version> sm_103a". */
+const char* irm_version(void);
+
+/*
+ * Host-only validation of a batch of chunk tables (no GPU needed).
+ *   chunks_host  [indptr_host[B]] records; request b owns [indptr_host[b], indptr_host[b+1])
+ *   indptr_host  [B+1], indptr_host[0] == 0, non-decreasing
+ *   n_rows       rows in the row store (every source row must lie in [0, n_rows))
+ *   ctx_out      [B] or NULL: receives each request's context length
+ * Returns IRM_OK, IRM_ERR_CHUNK_TABLE, IRM_ERR_CARVEOUT or IRM_ERR_INVALID_ARG.
+ */
+irm_status irm_validate_chunks(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                               int64_t n_rows, int64_t* ctx_out);
+
+/*
+ * Reads and clears the device status word of a workspace (synchronizes `stream`).
+ * Returns IRM_OK, IRM_ERR_DEVICE_TIMEOUT, IRM_ERR_DEVICE_BOUNDS or IRM_ERR_CUDA.
+ */
+irm_status irm_device_status(void* workspace, cudaStream_t stream);
+
+/*
+ * Rotate+gather into a paged KV layout, and/or the per-row assembly plan.
+ * [walkthrough §5 assembly loop: reused chunks contribute (cKV, R(delta) k_r,base)]
+ *
+ * For target row t of request b, with c its chunk:
+ *   src_row = pool_offset_c + (t - p_tgt_c); delta = reused_c ? p_tgt_c - p_src_c : 0
+ *   paged_out[page_table[b*max_pages + t/64]*64 + t%64] = [cKV(src_row) | R(delta) k_r(src_row)]
+ * cKV bytes are copied unchanged; rows with delta = 0 are copied bit for bit.
+ *
+ *   chunks_host, indptr_host, B   host chunk tables (validated)
+ *   chunks_dev, indptr_dev        device copies of the same bytes
+ *   kv_rows      device bf16 [n_rows, 576], 16-byte aligned
+ *   paged_out    device bf16 [n_pages, 64, 576] or NULL (plan only); rows of a page that
+ *                no target row maps to are left untouched
+ *   page_table   device int32 [B, max_pages] (required when paged_out != NULL); every
+ *                entry used must lie in [0, n_pages) -- the kernel skips a row whose page
+ *                is out of range and records IRM_ERR_DEVICE_BOUNDS
+ *   out_src_row, out_delta, out_pos_src   device int32 [sum ctx] or NULL; rows are listed
+ *                request after request (pos_src = t - delta)
+ * Workspace: irm_assemble_kv_workspace_size bytes.
+ */
+irm_status irm_assemble_kv_workspace_size(int B, size_t* bytes);
+irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                           const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                           const void* kv_rows, int64_t n_rows, void* paged_out,
+                           int64_t n_pages, const int32_t* page_table, int max_pages,
+                           int32_t* out_src_row,
+                           int32_t* out_delta, int32_t* out_pos_src, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Fused delta-rotate + absorbed MLA decode attention (one query token per request).
+ * [walkthrough §4: scores over [cKV | k_r], output P.cKV; the rotation is applied on the
+ *  HBM -> shared memory load path, so rotated keys are never written back]
+ *
+ *   q_lat   device bf16 [B, H, 512]   absorbed query (W_UK folded in)
+ *   q_rope  device bf16 [B, H, 64]    RoPE query slice, already encoded at position ctx-1
+ *   H       1..128 heads
+ *   kv_rows device bf16 [n_rows, 576]
+ *   softmax_scale  scale applied to q.k (1/sqrt(192) for DeepSeek-V2/V3 shapes)
+ *   out     device bf16 [B, H, 512]:  O = softmax(s) . cKV, s_t = scale * (q_lat.cKV_t +
+ *           q_rope.R(delta_t) k_r,t)
+ *   lse     device fp32 [B, H] or NULL: natural-log sum of exp(s_t)
+ * Workspace: irm_mla_attn_decode_workspace_size bytes (holds split-KV partials).
+ */
+irm_status irm_mla_attn_decode_workspace_size(const irm_chunk* chunks_host,
+                                              const int32_t* indptr_host, int B, int H,
+                                              size_t* bytes);
+irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int H,
+                               const irm_chunk* chunks_host, const int32_t* indptr_host,
+                               const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                               const void* kv_rows, int64_t n_rows, float softmax_scale,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/*
+ * Fused delta-rotate + absorbed MLA prefill attention (n_q causal query tokens per request,
+ * the last n_q positions of each request's assembled context).
+ *   q_lat [B, n_q, H, 512], q_rope [B, n_q, H, 64], out [B, n_q, H, 512] bf16,
+ *   lse [B, n_q, H] fp32 or NULL; 1 <= n_q <= ctx_b for every request.
+ * Workspace: irm_mla_attn_prefill_workspace_size bytes.
+ */
+irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes);
+irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, int n_q, int H,
+                                const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IRM_H_ */

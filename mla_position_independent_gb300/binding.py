@@ -1,0 +1,214 @@
+"""Thin ctypes binding over libirm.so (include/irm.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  If libirm.so is missing the first
+call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+from .synth import CHUNK_DTYPE
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libirm.so")
+_lib = None
+
+WORKSPACE_HEADER = 256
+DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
+
+EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_chunks",
+           "irm_device_status", "irm_assemble_kv_workspace_size", "irm_assemble_kv",
+           "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
+           "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill"]
+
+
+class IrmError(RuntimeError):
+    def __init__(self, status: int, text: str, detail: str):
+        super().__init__(f"irm status {status} ({text}): {detail}")
+        self.status = status
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built: run __graft_entry__.build() "
+                               "(the CUDA library is required; there is no fallback)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        L.irm_status_string.restype = ctypes.c_char_p
+        L.irm_status_string.argtypes = [I]
+        L.irm_last_error.restype = ctypes.c_char_p
+        L.irm_version.restype = ctypes.c_char_p
+        L.irm_validate_chunks.argtypes = [P, P, I, I64, P]
+        L.irm_device_status.argtypes = [P, P]
+        L.irm_assemble_kv_workspace_size.argtypes = [I, P]
+        L.irm_assemble_kv.argtypes = [P, P, I, P, P, P, I64, P, I64, P, I, P, P, P, P, SZ, P]
+        L.irm_mla_attn_decode_workspace_size.argtypes = [P, P, I, I, P]
+        L.irm_mla_attn_decode.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float, P, P, P,
+                                          SZ, P]
+        L.irm_mla_attn_prefill_workspace_size.argtypes = [I, I, I, P]
+        L.irm_mla_attn_prefill.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
+                                           P, P, SZ, P]
+        for name in EXPORTS:
+            if name not in ("irm_status_string", "irm_last_error", "irm_version"):
+                getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def _check(st: int):
+    if st != 0:
+        L = lib()
+        raise IrmError(st, L.irm_status_string(st).decode(), L.irm_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on the GPU")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+class ChunkTable:
+    """A batch of chunk tables kept twice, as the library wants it: the host copy (validated,
+    used for launch geometry) and a byte-identical device copy (read by the kernels)."""
+
+    def __init__(self, chunks: np.ndarray, indptr: np.ndarray, device="cuda"):
+        self.chunks_host = np.ascontiguousarray(chunks, dtype=CHUNK_DTYPE)
+        self.indptr_host = np.ascontiguousarray(indptr, dtype=np.int32)
+        self.B = int(self.indptr_host.shape[0] - 1)
+        self.chunks_dev = torch.from_numpy(self.chunks_host.view(np.uint8).copy()).to(device)
+        self.indptr_dev = torch.from_numpy(self.indptr_host.copy()).to(device)
+
+    def validate(self, n_rows: int) -> np.ndarray:
+        ctx = np.zeros(self.B, np.int64)
+        _check(lib().irm_validate_chunks(_ptr(self.chunks_host), _ptr(self.indptr_host), self.B,
+                                         int(n_rows), _ptr(ctx)))
+        return ctx
+
+
+def validate_chunks(chunks: np.ndarray, indptr: np.ndarray, n_rows: int) -> np.ndarray:
+    """Host-only validation (no GPU needed).  Returns each request's context length."""
+    chunks = np.ascontiguousarray(chunks, dtype=CHUNK_DTYPE)
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    B = int(indptr.shape[0] - 1)
+    ctx = np.zeros(max(B, 1), np.int64)
+    _check(lib().irm_validate_chunks(_ptr(chunks), _ptr(indptr), B, int(n_rows), _ptr(ctx)))
+    return ctx[:B]
+
+
+def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-initialised workspace (the first 256 bytes hold the device status word)."""
+    return torch.zeros(max(int(nbytes), WORKSPACE_HEADER), dtype=torch.uint8, device=device)
+
+
+def device_status(workspace: torch.Tensor, stream=None):
+    """Raises IrmError if a kernel recorded a timeout or an out-of-range row (and clears it)."""
+    _check(lib().irm_device_status(_ptr(workspace), _stream(stream)))
+
+
+def assemble_kv_workspace_size(B: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().irm_assemble_kv_workspace_size(int(B), ctypes.byref(n)))
+    return n.value
+
+
+def irm_assemble_kv(table: ChunkTable, kv_rows: torch.Tensor, paged_out=None, page_table=None,
+                    out_src_row=None, out_delta=None, out_pos_src=None, workspace=None,
+                    stream=None):
+    _need(kv_rows, torch.bfloat16, "kv_rows", 2)
+    n_pages, max_pages = 0, 0
+    if paged_out is not None:
+        _need(paged_out, torch.bfloat16, "paged_out", 3)
+        _need(page_table, torch.int32, "page_table", 2)
+        n_pages, max_pages = int(paged_out.shape[0]), int(page_table.shape[1])
+    for t, n in ((out_src_row, "out_src_row"), (out_delta, "out_delta"), (out_pos_src, "out_pos_src")):
+        if t is not None:
+            _need(t, torch.int32, n, 1)
+    if workspace is None:
+        workspace = new_workspace(assemble_kv_workspace_size(table.B), kv_rows.device)
+    _check(lib().irm_assemble_kv(
+        _ptr(table.chunks_host), _ptr(table.indptr_host), table.B, _ptr(table.chunks_dev),
+        _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]), _ptr(paged_out), n_pages,
+        _ptr(page_table), max_pages, _ptr(out_src_row), _ptr(out_delta), _ptr(out_pos_src),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def decode_workspace_size(table: ChunkTable, H: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().irm_mla_attn_decode_workspace_size(_ptr(table.chunks_host),
+                                                    _ptr(table.indptr_host), table.B, int(H),
+                                                    ctypes.byref(n)))
+    return n.value
+
+
+def prefill_workspace_size(B: int, n_q: int, H: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().irm_mla_attn_prefill_workspace_size(int(B), int(n_q), int(H), ctypes.byref(n)))
+    return n.value
+
+
+def irm_mla_attn_decode(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,
+                        out=None, lse=None, workspace=None, stream=None):
+    """q_lat [B, H, 512] / q_rope [B, H, 64] bf16 (a [B, 1, H, *] view is accepted)."""
+    B, H = int(q_lat.shape[0]), int(q_lat.shape[-2])
+    _need(q_lat, torch.bfloat16, "q_lat")
+    _need(q_rope, torch.bfloat16, "q_rope")
+    _need(kv_rows, torch.bfloat16, "kv_rows", 2)
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_lat.device)
+    _need(out, torch.bfloat16, "out")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(table, H), q_lat.device)
+    _check(lib().irm_mla_attn_decode(
+        _ptr(q_lat), _ptr(q_rope), B, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
+        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, lse, workspace
+
+
+def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,
+                         out=None, lse=None, workspace=None, stream=None):
+    """q_lat [B, n_q, H, 512] / q_rope [B, n_q, H, 64] bf16, causal over the last n_q rows."""
+    B, n_q, H = (int(x) for x in q_lat.shape[:3])
+    _need(q_lat, torch.bfloat16, "q_lat", 4)
+    _need(q_rope, torch.bfloat16, "q_rope", 4)
+    _need(kv_rows, torch.bfloat16, "kv_rows", 2)
+    if out is None:
+        out = torch.empty((B, n_q, H, 512), dtype=torch.bfloat16, device=q_lat.device)
+    _need(out, torch.bfloat16, "out")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    if workspace is None:
+        workspace = new_workspace(prefill_workspace_size(B, n_q, H), q_lat.device)
+    _check(lib().irm_mla_attn_prefill(
+        _ptr(q_lat), _ptr(q_rope), B, n_q, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
+        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, lse, workspace

@@ -1,0 +1,363 @@
+// C ABI of the library: host-side validation of chunk tables, launch geometry, launches.
+// No allocation, no host<->device copy on any compute path (see include/irm.h).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/irm.h"
+#include "irm_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+irm_status fail(irm_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+irm_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(IRM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// RoPE phase increments F[j] = theta_j / (2 pi) * 2^64 with theta_j = 10000^(-2j/64),
+// computed once in fp64 on the host; the device turns (delta * F[j]) mod 2^64 into an angle.
+const irm::RopePhaseHost& rope_phase() {
+  static const irm::RopePhaseHost tab = [] {
+    irm::RopePhaseHost t{};
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int j = 0; j < 32; ++j) {
+      const double theta = std::pow(10000.0, -2.0 * j / 64.0);
+      t.F[j] = (uint64_t)std::ldexp(theta / two_pi, 64);
+    }
+    return t;
+  }();
+  return tab;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n > 0 ? n : 148;
+}
+
+struct TableInfo {
+  std::vector<int64_t> ctx;
+  int64_t n_chunks = 0;
+  int64_t max_ctx = 0;
+  int64_t min_ctx = 0;
+};
+
+// Chunk-table rules [walkthrough §5 assembly loop, §7 carve-out]: per request the chunks
+// tile [0, ctx) in target order with len > 0; source rows lie in the row store; a reused
+// chunk never covers a position below 32; delta and positions fit in int32.
+irm_status validate(const irm_chunk* chunks, const int32_t* indptr, int B, int64_t n_rows,
+                    TableInfo* info) {
+  if (B <= 0) return fail(IRM_ERR_INVALID_ARG, "B must be positive (got %d)", B);
+  if (chunks == nullptr || indptr == nullptr)
+    return fail(IRM_ERR_INVALID_ARG, "null chunk table pointer");
+  if (indptr[0] != 0) return fail(IRM_ERR_CHUNK_TABLE, "indptr[0] must be 0");
+  if (n_rows < 0 || n_rows >= (int64_t(1) << 31))
+    return fail(IRM_ERR_INVALID_ARG, "n_rows %lld outside [0, 2^31)", (long long)n_rows);
+  info->ctx.assign(B, 0);
+  for (int b = 0; b < B; ++b) {
+    const int32_t c0 = indptr[b], c1 = indptr[b + 1];
+    if (c1 <= c0) return fail(IRM_ERR_CHUNK_TABLE, "request %d has no chunks", b);
+    int64_t expect = 0;
+    for (int32_t c = c0; c < c1; ++c) {
+      const irm_chunk& ch = chunks[c];
+      if (ch.len <= 0) return fail(IRM_ERR_CHUNK_TABLE, "chunk %d: len %d <= 0", c, ch.len);
+      if ((int64_t)ch.p_tgt != expect)
+        return fail(IRM_ERR_CHUNK_TABLE, "chunk %d: p_tgt %d, expected %lld (chunks must tile the context in order)",
+                    c, ch.p_tgt, (long long)expect);
+      if (ch.pool_offset < 0 || ch.pool_offset + ch.len > n_rows)
+        return fail(IRM_ERR_CHUNK_TABLE, "chunk %d: rows [%lld, %lld) outside the row store of %lld rows", c,
+                    (long long)ch.pool_offset, (long long)(ch.pool_offset + ch.len), (long long)n_rows);
+      if (ch.reused > 1) return fail(IRM_ERR_CHUNK_TABLE, "chunk %d: reused must be 0 or 1", c);
+      if (ch.reused && ch.p_tgt < IRM_CARVE_OUT)
+        return fail(IRM_ERR_CARVEOUT, "chunk %d: reused chunk covers position %d < %d (first-chunk carve-out)",
+                    c, ch.p_tgt, IRM_CARVE_OUT);
+      if (ch.reused) {
+        const int64_t d = (int64_t)ch.p_tgt - (int64_t)ch.p_src;
+        if (d > INT32_MAX || d < INT32_MIN) return fail(IRM_ERR_CHUNK_TABLE, "chunk %d: delta overflows int32", c);
+      }
+      expect += ch.len;
+      if (expect > INT32_MAX) return fail(IRM_ERR_CHUNK_TABLE, "request %d: context exceeds int32", b);
+    }
+    info->ctx[b] = expect;
+  }
+  info->n_chunks = indptr[B];
+  info->max_ctx = info->min_ctx = info->ctx[0];
+  for (int b = 1; b < B; ++b) {
+    info->max_ctx = std::max(info->max_ctx, info->ctx[b]);
+    info->min_ctx = std::min(info->min_ctx, info->ctx[b]);
+  }
+  return IRM_OK;
+}
+
+constexpr int kBM = 128;
+constexpr int kBN = 64;
+
+// Decode split-KV factor: the attention runs one 2-CTA cluster per (request, split); pick
+// the split count that minimises waves x (tiles per split + fixed cost).
+int choose_splits(int B, int64_t max_ctx, int sms) {
+  const int pairs = std::max(1, sms / 2);
+  const int64_t tiles = (max_ctx + kBN - 1) / kBN;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int S = 1; S <= 64 && S <= tiles; ++S) {
+    const int64_t units = (int64_t)B * S;
+    const int64_t waves = (units + pairs - 1) / pairs;
+    const double cost = (double)waves * ((double)((tiles + S - 1) / S) + 3.0) + (S > 1 ? 1.0 : 0.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t partial_bytes(int B, int units) {
+  const size_t o = (size_t)B * units * kBM * IRM_D_LAT * sizeof(float);
+  const size_t l = (size_t)B * units * kBM * sizeof(float);
+  return align_up(o, 256) + align_up(l, 256);
+}
+
+struct AttnPlan {
+  int qpt, n_qtiles, S;
+  size_t ws_bytes;
+};
+
+irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p) {
+  if (H < 1 || H > IRM_MAX_HEADS) return fail(IRM_ERR_UNSUPPORTED, "H=%d outside [1, %d]", H, IRM_MAX_HEADS);
+  if (n_q < 1) return fail(IRM_ERR_INVALID_ARG, "n_q must be >= 1");
+  if (n_q > info.min_ctx)
+    return fail(IRM_ERR_INVALID_ARG, "n_q=%d exceeds the shortest context (%lld)", n_q, (long long)info.min_ctx);
+  p->qpt = kBM / H;
+  p->n_qtiles = (n_q + p->qpt - 1) / p->qpt;
+  if (p->n_qtiles > 32767) return fail(IRM_ERR_UNSUPPORTED, "too many query tiles (%d)", p->n_qtiles);
+  if (B > 65535) return fail(IRM_ERR_UNSUPPORTED, "B=%d exceeds 65535", B);
+  p->S = decode ? choose_splits(B, info.max_ctx, num_sms()) : 1;
+  p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles * p->S) : 0);
+  return IRM_OK;
+}
+
+irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H,
+                    const irm_chunk* chunks_host, const int32_t* indptr_host,
+                    const irm_chunk* chunks_dev, const int32_t* indptr_dev, const void* kv_rows,
+                    int64_t n_rows, float softmax_scale, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream, bool decode) {
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
+  if (st != IRM_OK) return st;
+  AttnPlan pl;
+  if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
+  if (!q_lat || !q_rope || !kv_rows || !out || !chunks_dev || !indptr_dev)
+    return fail(IRM_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_rows, 16) || !aligned(out, 16))
+    return fail(IRM_ERR_INVALID_ARG, "q_lat, q_rope, kv_rows and out must be 16-byte aligned");
+  if (!aligned(chunks_dev, 8) || !aligned(indptr_dev, 4) || (lse && !aligned(lse, 4)))
+    return fail(IRM_ERR_INVALID_ARG, "misaligned chunk table or lse pointer");
+  if (!std::isfinite(softmax_scale)) return fail(IRM_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.ws_bytes)
+    return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
+                pl.ws_bytes, workspace_bytes);
+  irm::AttnArgs a{};
+  a.q_lat = q_lat;
+  a.q_rope = q_rope;
+  a.kv = kv_rows;
+  a.chunks = chunks_dev;
+  a.indptr = indptr_dev;
+  a.n_rows = n_rows;
+  a.n_chunks = info.n_chunks;
+  a.B = B;
+  a.n_q = n_q;
+  a.H = H;
+  a.qpt = pl.qpt;
+  a.n_qtiles = pl.n_qtiles;
+  a.S = pl.S;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.out = out;
+  a.lse = lse;
+  a.status = static_cast<int*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
+  if (pl.S > 1) {
+    a.opart = reinterpret_cast<float*>(ws);
+    a.lsepart = reinterpret_cast<float*>(
+        ws + align_up((size_t)B * pl.n_qtiles * pl.S * kBM * IRM_D_LAT * sizeof(float), 256));
+  }
+  std::memcpy(a.phase.F, rope_phase().F, sizeof a.phase.F);
+  cudaError_t e = irm::launch_mla_attn(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mla attention launch");
+  if (pl.S > 1) {
+    e = irm::launch_combine(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV combine launch");
+  }
+  return IRM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* irm_status_string(int status) {
+  switch (status) {
+    case IRM_OK: return "ok";
+    case IRM_ERR_INVALID_ARG: return "invalid argument";
+    case IRM_ERR_CHUNK_TABLE: return "invalid chunk table";
+    case IRM_ERR_CARVEOUT: return "reused chunk inside the first-chunk carve-out";
+    case IRM_ERR_UNSUPPORTED: return "unsupported shape";
+    case IRM_ERR_CUDA: return "CUDA error";
+    case IRM_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case IRM_ERR_DEVICE_BOUNDS: return "device saw a source row or page outside its buffer";
+    case IRM_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* irm_last_error(void) { return g_last_error.c_str(); }
+
+const char* irm_version(void) { return "irm 0.1 sm_103a"; }
+
+irm_status irm_validate_chunks(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                               int64_t n_rows, int64_t* ctx_out) {
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
+  if (st == IRM_OK && ctx_out != nullptr)
+    for (int b = 0; b < B; ++b) ctx_out[b] = info.ctx[b];
+  return st;
+}
+
+irm_status irm_device_status(void* workspace, cudaStream_t stream) {
+  if (workspace == nullptr) return fail(IRM_ERR_INVALID_ARG, "null workspace");
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (word != 0) {
+    e = cudaMemsetAsync(workspace, 0, sizeof word, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  }
+  if (word & 1) return fail(IRM_ERR_DEVICE_TIMEOUT, "a device pipeline wait exceeded its limit");
+  if (word & 2) return fail(IRM_ERR_DEVICE_BOUNDS, "a kernel met a source row or page outside its buffer");
+  return IRM_OK;
+}
+
+irm_status irm_assemble_kv_workspace_size(int B, size_t* bytes) {
+  if (B <= 0 || bytes == nullptr) return fail(IRM_ERR_INVALID_ARG, "B must be positive and bytes non-null");
+  *bytes = IRM_WORKSPACE_HEADER + align_up((size_t)(B + 1) * sizeof(int64_t), 256);
+  return IRM_OK;
+}
+
+irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                           const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                           const void* kv_rows, int64_t n_rows, void* paged_out, int64_t n_pages,
+                           const int32_t* page_table, int max_pages, int32_t* out_src_row,
+                           int32_t* out_delta, int32_t* out_pos_src, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
+  if (st != IRM_OK) return st;
+  const bool plan_out = out_src_row || out_delta || out_pos_src;
+  if (plan_out && !(out_src_row && out_delta && out_pos_src))
+    return fail(IRM_ERR_INVALID_ARG, "out_src_row, out_delta and out_pos_src go together");
+  if (!chunks_dev || !indptr_dev) return fail(IRM_ERR_INVALID_ARG, "null device chunk table");
+  if (paged_out) {
+    if (!kv_rows || !page_table) return fail(IRM_ERR_INVALID_ARG, "paged output needs kv_rows and page_table");
+    if (!aligned(kv_rows, 16) || !aligned(paged_out, 16))
+      return fail(IRM_ERR_INVALID_ARG, "kv_rows and paged_out must be 16-byte aligned");
+    if (n_pages <= 0 || max_pages <= 0) return fail(IRM_ERR_INVALID_ARG, "n_pages and max_pages must be positive");
+    if ((info.max_ctx + IRM_PAGE_ROWS - 1) / IRM_PAGE_ROWS > max_pages)
+      return fail(IRM_ERR_INVALID_ARG, "a context of %lld rows needs more than max_pages=%d pages",
+                  (long long)info.max_ctx, max_pages);
+  }
+  size_t need = 0;
+  irm_assemble_kv_workspace_size(B, &need);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+  irm::GatherArgs g{};
+  g.chunks = chunks_dev;
+  g.indptr = indptr_dev;
+  g.B = B;
+  g.n_chunks = info.n_chunks;
+  g.kv = kv_rows;
+  g.n_rows = n_rows;
+  g.paged_out = paged_out;
+  g.n_pages = n_pages;
+  g.page_table = page_table;
+  g.max_pages = max_pages;
+  g.status = static_cast<int*>(workspace);
+  g.out_src = out_src_row;
+  g.out_delta = out_delta;
+  g.out_pos_src = out_pos_src;
+  std::memcpy(g.phase.F, rope_phase().F, sizeof g.phase.F);
+  if (plan_out) {
+    int64_t* row_start = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER);
+    g.row_start = row_start;
+    cudaError_t e = irm::launch_row_start(chunks_dev, indptr_dev, B, row_start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "row-start launch");
+  }
+  if (!paged_out && !plan_out) return IRM_OK;
+  cudaError_t e = irm::launch_rotate_gather(g, num_sms(), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rotate+gather launch");
+  return IRM_OK;
+}
+
+irm_status irm_mla_attn_decode_workspace_size(const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                              int B, int H, size_t* bytes) {
+  if (bytes == nullptr) return fail(IRM_ERR_INVALID_ARG, "bytes is null");
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, INT32_MAX, &info);
+  if (st != IRM_OK) return st;
+  AttnPlan pl;
+  if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
+  *bytes = pl.ws_bytes;
+  return IRM_OK;
+}
+
+irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int H,
+                               const irm_chunk* chunks_host, const int32_t* indptr_host,
+                               const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                               const void* kv_rows, int64_t n_rows, float softmax_scale, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+                  n_rows, softmax_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes) {
+  if (bytes == nullptr || B <= 0 || n_q <= 0 || H <= 0 || H > IRM_MAX_HEADS)
+    return fail(IRM_ERR_INVALID_ARG, "bad arguments");
+  *bytes = IRM_WORKSPACE_HEADER;
+  return IRM_OK;
+}
+
+irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, int n_q, int H,
+                                const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                const void* kv_rows, int64_t n_rows, float softmax_scale, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+                  n_rows, softmax_scale, out, lse, workspace, workspace_bytes, stream, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Internal launch interfaces between the C ABI (irm_host.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/irm.h"
+
+namespace irm {
+
+struct RopePhaseHost {
+  uint64_t F[32];
+};
+
+struct GatherArgs {
+  const irm_chunk* chunks;
+  const int32_t* indptr;
+  int B;
+  int64_t n_chunks;
+  const void* kv;
+  int64_t n_rows;
+  void* paged_out;
+  int64_t n_pages;
+  const int32_t* page_table;
+  int max_pages;
+  const int64_t* row_start;  // [B+1], required when out_src != nullptr
+  int32_t* out_src;
+  int32_t* out_delta;
+  int32_t* out_pos_src;
+  int* status;
+  struct {
+    uint64_t F[32];
+  } phase;
+};
+
+// Fused attention (decode and prefill share one kernel).
+struct AttnArgs {
+  const void* q_lat;    // bf16 [B, n_q, H, 512]
+  const void* q_rope;   // bf16 [B, n_q, H, 64]
+  const void* kv;       // bf16 [n_rows, 576]
+  const irm_chunk* chunks;
+  const int32_t* indptr;
+  int64_t n_rows;
+  int64_t n_chunks;
+  int B, n_q, H;
+  int qpt;        // queries per 128-row tile = 128 / H
+  int n_qtiles;   // ceil(n_q / qpt)
+  int S;          // KV splits per query tile
+  float scale_log2;
+  void* out;      // bf16 [B, n_q, H, 512] (S == 1)
+  float* lse;     // fp32 [B, n_q, H] or nullptr (S == 1)
+  float* opart;   // fp32 [B, n_qtiles*S, 128, 512] (S > 1)
+  float* lsepart; // fp32 [B, n_qtiles*S, 128] (S > 1)
+  int* status;
+  struct {
+    uint64_t F[32];
+  } phase;
+};
+
+cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int B,
+                             int64_t* row_start, cudaStream_t stream);
+cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
+size_t attn_smem_bytes();
+
+}  // namespace irm

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, on the same seeded
+inputs.  Indices and positions are compared bit for bit; bf16 outputs within relative L2
+5e-3 and max-abs 2e-2; rotated k_r within relative L2 4.7e-3 (the pages' bf16 figure)."""
+import numpy as np
+import pytest
+import torch
+
+from mla_position_independent_gb300 import synth
+import mla_position_independent_gb300 as irm
+from helpers import (SCALE, TOL_KR_REL_L2, assert_close, encode_rope_rows, rel_l2, to_device,
+                     widen_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    irm.lib()
+
+
+# ----------------------------------------------------------------------------- assembly
+
+def _assemble_and_check(case, oracle_mod, check_plan=True):
+    case = to_device(case)
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    n_rows = case.kv_rows.shape[0]
+    total = int(case.chunks["len"].astype(np.int64).sum())
+    paged = torch.zeros((case.n_pages, 64, 576), dtype=torch.bfloat16, device="cuda")
+    pt = torch.from_numpy(case.page_table).cuda()
+    outs = [torch.full((total,), -7, dtype=torch.int32, device="cuda") for _ in range(3)]
+    ws = irm.irm_assemble_kv(table, case.kv_rows, paged, pt, *outs)
+    irm.device_status(ws)
+    kv_bits = synth.bits(case.kv_rows)
+    if check_plan:
+        pl = oracle_mod.plan(case.chunks, case.indptr)
+        assert np.array_equal(outs[0].cpu().numpy(), pl["src_row"])
+        assert np.array_equal(outs[1].cpu().numpy(), pl["delta"])
+        assert np.array_equal(outs[2].cpu().numpy(), pl["pos_src"])
+    slot, ref = oracle_mod.rotate_gather(kv_bits, case.chunks, case.indptr, case.page_table)
+    got_bits = synth.bits(paged.view(-1, 576))[slot]
+    # cKV: byte-identical; rows with delta == 0: byte-identical k_r
+    src_bits = kv_bits[oracle_mod.plan(case.chunks, case.indptr)["src_row"]]
+    assert np.array_equal(got_bits[:, :512], src_bits[:, :512])
+    pl = oracle_mod.plan(case.chunks, case.indptr)
+    zero = pl["delta"] == 0
+    assert np.array_equal(got_bits[zero, 512:], src_bits[zero, 512:])
+    if (~zero).any():
+        got = oracle_mod.widen(got_bits[~zero, 512:])
+        r = rel_l2(got, ref[~zero, 512:])
+        assert r <= TOL_KR_REL_L2, f"rotated k_r rel L2 {r:.3e}"
+        return r
+    return 0.0
+
+
+def test_assemble_tiny(oracle_mod):
+    case = encode_rope_rows(synth.tiny_case(0), oracle_mod)
+    case.page_table = np.random.default_rng(3).permutation(8).astype(np.int32)[None]
+    case.n_pages = 8
+    _assemble_and_check(case, oracle_mod)
+
+
+@pytest.mark.parametrize("lens", [[32, 1, 31, 32, 33, 63, 64, 65, 512], [40], [32, 7], [32, 100, 3]])
+@pytest.mark.parametrize("deltas", [(0, 1, -1), (65536, -65536, 12345)])
+def test_assemble_edge_cases(oracle_mod, lens, deltas):
+    rng = np.random.default_rng(sum(lens))
+    n_rows = 2048
+    reqs, p = [[]], 0
+    for k, n in enumerate(lens):
+        reused = p >= 32
+        d = deltas[k % len(deltas)] if reused else 0
+        off = int(rng.integers(0, n_rows - n))
+        reqs[0].append((off, n, p - d, reused))
+        p += n
+    case = synth.custom_case(reqs, n_rows=n_rows, n_q=0, pages=True)
+    _assemble_and_check(case, oracle_mod)
+
+
+def test_assemble_multi_request(oracle_mod):
+    case = synth.custom_case([[(0, 32, 0, 0), (500, 70, 9, 1), (100, 1, 50, 1)],
+                              [(900, 5, 0, 0)], [(1000, 32, 0, 0), (32, 129, -4000, 1)]],
+                             n_rows=1200, n_q=0, pages=True)
+    _assemble_and_check(case, oracle_mod)
+
+
+def test_rotate_gather_64k_rows_full(oracle_mod):
+    case = synth.rotate_gather_case(1 << 16, seed=0, device="cuda")
+    r = _assemble_and_check(case, oracle_mod)
+    assert r < 2.5e-3
+
+
+@pytest.mark.parametrize("n_rows", [1 << 20, 1 << 22])
+def test_rotate_gather_full_size_sampled(oracle_mod, n_rows):
+    """The configured sizes, checked on sampled target rows plus every chunk's endpoints."""
+    case = synth.rotate_gather_case(n_rows, seed=0, device="cuda")
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    paged = torch.empty((case.n_pages, 64, 576), dtype=torch.bfloat16, device="cuda")
+    pt = torch.from_numpy(case.page_table).cuda()
+    ws = irm.irm_assemble_kv(table, case.kv_rows, paged, pt)
+    irm.device_status(ws)
+    rng = np.random.default_rng(1)
+    ends = np.concatenate([case.chunks["p_tgt"], case.chunks["p_tgt"] + case.chunks["len"] - 1])
+    t = np.unique(np.concatenate([rng.integers(0, n_rows, 20000), ends[:20000]]))
+    rows = np.stack([np.zeros_like(t), t], 1)
+    # only the rows the oracle needs are copied to the host
+    pl = oracle_mod.plan(case.chunks, case.indptr)
+    src = pl["src_row"][t]
+    kv_sub = synth.bits(case.kv_rows[torch.from_numpy(src).cuda()])
+    ref = oracle_mod.assemble(kv_sub, np.arange(len(t)), pl["delta"][t])
+    slot = case.page_table[0, t // 64].astype(np.int64) * 64 + t % 64
+    got = synth.bits(paged.view(-1, 576)[torch.from_numpy(slot).cuda()])
+    assert np.array_equal(got[:, :512], kv_sub[:, :512])
+    nz = pl["delta"][t] != 0
+    assert np.array_equal(got[~nz, 512:], kv_sub[~nz, 512:])
+    assert rel_l2(oracle_mod.widen(got[nz, 512:]), ref[nz, 512:]) <= TOL_KR_REL_L2
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _attn_gpu(case, prefill):
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    B, n_q, H = case.q_lat.shape[:3]
+    if prefill:
+        lse = torch.empty((B, n_q, H), dtype=torch.float32, device="cuda")
+        out, lse, ws = irm.irm_mla_attn_prefill(case.q_lat, case.q_rope, table, case.kv_rows,
+                                                SCALE, lse=lse)
+    else:
+        lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        out, lse, ws = irm.irm_mla_attn_decode(case.q_lat[:, 0], case.q_rope[:, 0], table,
+                                               case.kv_rows, SCALE, lse=lse)
+        out, lse = out[:, None], lse[:, None]
+    irm.device_status(ws)
+    return out, lse
+
+
+def _check_attn(case, oracle_mod, prefill, select=None, what=""):
+    out, lse = _attn_gpu(case, prefill)
+    kv = synth.bits(case.kv_rows)
+    ql, qr = synth.bits(case.q_lat), synth.bits(case.q_rope)
+    O, L = oracle_mod.mla_attention(ql, qr, case.chunks, case.indptr, kv, SCALE, select=select)
+    got = widen_bf16(out)
+    gl = lse.cpu().numpy().astype(np.float64)
+    if select is not None:
+        s = np.asarray(select)
+        got, gl = got[s[:, 0], s[:, 1], s[:, 2]], gl[s[:, 0], s[:, 1], s[:, 2]]
+    r, m = assert_close(got, O, what or case.name)
+    assert np.max(np.abs(gl - L)) < 2e-2, f"lse max abs {np.max(np.abs(gl - L)):.3e}"
+    return r, m
+
+
+@pytest.mark.parametrize("q_std", [synth.Q_STD, 1.0])
+def test_prefill_tiny(oracle_mod, q_std):
+    case = to_device(encode_rope_rows(synth.tiny_case(0, q_std=q_std), oracle_mod))
+    _check_attn(case, oracle_mod, prefill=True)
+
+
+@pytest.mark.parametrize("q_std", [synth.Q_STD, 1.0])
+def test_decode_v2lite_full(oracle_mod, q_std):
+    case = to_device(synth.v2lite_decode(0, q_std=q_std))
+    _check_attn(case, oracle_mod, prefill=False)
+
+
+def test_decode_v3_sampled(oracle_mod):
+    case = synth.v3_decode(0, device="cuda")
+    rng = np.random.default_rng(5)
+    bs = rng.choice(64, 3, replace=False)
+    sel = np.array([[b, 0, h] for b in bs for h in rng.choice(128, 12, replace=False)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel)
+
+
+def test_decode_v3_sharp_sampled(oracle_mod):
+    case = synth.v3_decode(0, q_std=1.0, device="cuda")
+    sel = np.array([[b, 0, h] for b in (0, 63) for h in (0, 77, 127)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel)
+
+
+def test_prefill_chunked_sampled(oracle_mod):
+    case = synth.chunked_prefill(0, device="cuda")
+    sel = np.array([[b, i, h] for b in (0, 3) for i in (0, 1, 1000, 2047) for h in (0, 64, 127)])
+    _check_attn(case, oracle_mod, prefill=True, select=sel)
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+@pytest.mark.parametrize("lens", [[40], [32, 1, 31, 33, 63, 64, 65], [32, 17], [32, 200, 128, 3]])
+def test_attention_edge_cases(oracle_mod, H, lens):
+    rng = np.random.default_rng(H + len(lens))
+    n_rows = 2048
+    reqs = []
+    for b in range(2):
+        p, req = 0, []
+        for k, n in enumerate(lens):
+            reused = p >= 32 and k % 2 == 1
+            d = [1, -1, 65536, -65536, 0, 777][k % 6] if reused else 0
+            req.append((int(rng.integers(0, n_rows - n)), n, p - d, reused))
+            p += n
+        reqs.append(req)
+    ctx = sum(lens)
+    for n_q in sorted({1, min(5, ctx), min(ctx, 70)}):
+        case = to_device(synth.custom_case(reqs, n_rows=n_rows, n_q=n_q, H=H, q_std=1.0,
+                                           seed=n_q))
+        _check_attn(case, oracle_mod, prefill=True, what=f"H={H} lens={lens} n_q={n_q}")
+        if n_q == 1:
+            _check_attn(case, oracle_mod, prefill=False, what=f"decode H={H} lens={lens}")
+
+
+def test_device_table_mismatch_is_recorded_not_faulted(oracle_mod):
+    """A device chunk table whose rows leave the row store (the host copy is valid) is caught
+    by the kernels' bounds check: rows are zero filled and the status word is set."""
+    case = to_device(synth.custom_case([[(0, 32, 0, 0), (40, 64, 5, 1)]], n_rows=200, n_q=1, H=16))
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    bad = case.chunks.copy()
+    bad["pool_offset"][1] = 10_000_000
+    table.chunks_dev.copy_(torch.from_numpy(bad.view(np.uint8).copy()).cuda())
+    out, _, ws = irm.irm_mla_attn_decode(case.q_lat[:, 0], case.q_rope[:, 0], table, case.kv_rows)
+    with pytest.raises(irm.IrmError) as e:
+        irm.device_status(ws)
+    assert e.value.status == -7
+    irm.device_status(ws)  # cleared
