@@ -12,13 +12,19 @@
 //     CTA 1 owns cKV[256:512) and k_r (and therefore the rotation).  Each CTA loads only
 //     its own columns of every KV row, so each row is read from memory exactly once.
 //   - Each CTA computes its partial scores S_r = Q_r K_r^T (tcgen05, M=128, N=64) into
-//     TMEM and ships them to the peer with st.async; both add the two partials in the
-//     same way and run the identical online softmax, so P is bit-identical in both.
+//     TMEM and ships them to the peer with st.async; both add the two partials and run
+//     the identical online softmax, so P is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
-//   - Warp roles: warps 0-3 softmax (thread = TMEM lane = query row), warps 4-7 load
-//     tiles with cp.async (row gather following the chunk table) and rotate k_r, warp 8
-//     allocates TMEM and issues the UMMAs.
+//   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-5 gather KV rows with
+//     cp.async following the chunk table (completion tracked by an mbarrier, so they run
+//     ahead across stages); 6 allocates TMEM and issues the UMMAs in readiness order;
+//     7 publishes landed tiles, rotating k_r by R(delta) first.
+//   - Only the first Mv rows (valid query rows rounded up to 8) of Q, P and the score
+//     exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
+//     whatever follows in shared memory.  Those rows only ever produce rows of S / O that
+//     are never read, and the space saved becomes extra KV pipeline stages (decode with
+//     16 heads runs 5 stages; 128-row tiles run 2).
 // Every pipeline wait is bounded (2 s) and reports a timeout in the status word.
 #include <cuda_runtime.h>
 #include <climits>
@@ -33,52 +39,69 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 64;   // KV rows per tile
 constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kMaxSlabs = 5;                      // 64-column slabs per CTA (4 or 5)
-constexpr uint32_t kSlabQ = kBM * 128;            // bytes of one Q slab
-constexpr uint32_t kSlabKV = kBN * 128;           // bytes of one KV slab
-constexpr uint32_t kStage = kMaxSlabs * kSlabKV;  // one KV pipeline stage
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kMaxSlabs * kSlabQ;
-constexpr uint32_t kOffP = kOffKV + 2 * kStage;
-constexpr uint32_t kOffX = kOffP + kBM * 128;
-constexpr uint32_t kOffMisc = kOffX + kBM * kBN * 4;
-constexpr uint32_t kOffMapSrc = kOffMisc + 32 * 8;
-constexpr uint32_t kOffMapDelta = kOffMapSrc + 2 * kBN * 4;
-constexpr uint32_t kOffPhase = kOffMapDelta + 2 * kBN * 4;
+constexpr int kLoaderWarps = 2;
+constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 6
+constexpr int kPubWarp = kMmaWarp + 1;                   // 7
+constexpr int kThreads = (kPubWarp + 1) * 32;            // 256: 2 warps per SM sub-partition
+constexpr int kLoaderThreads = kLoaderWarps * 32;
+constexpr int kMaxStages = 6;
+constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
+constexpr uint32_t kStage = 5 * kSlabKV; // one KV pipeline stage (up to 5 slabs)
+constexpr uint32_t kSmemLimit = 232448;
+
+// Fixed area at the start of shared memory.
+constexpr uint32_t kOffBars = 0;                                   // 64 mbarriers
+constexpr uint32_t kOffMapSrc = kOffBars + 64 * 8;                 // int32 [kMaxStages][64]
+constexpr uint32_t kOffMapDelta = kOffMapSrc + kMaxStages * kBN * 4;
+constexpr uint32_t kOffPhase = kOffMapDelta + kMaxStages * kBN * 4;  // uint64 [32]
 constexpr uint32_t kOffTmemPtr = kOffPhase + 32 * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kMiscBytes = 2048;
-constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + base alignment slack
-static_assert(kOffAbort + 4 <= kOffMisc + kMiscBytes, "misc area overflow");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kFixedBytes = 4096;
+static_assert(kOffAbort + 4 <= kFixedBytes, "fixed area overflow");
 
 enum : int {
-  BAR_KV_FULL = 0,   // [2] producers -> MMA (count 4: one arrive per producer warp)
-  BAR_KV_EMPTY = 2,  // [2] MMA commit after P.V of the stage
-  BAR_S_FULL = 4,    // [2] MMA commit after Q.K^T into S buffer
-  BAR_S_EMPTY = 6,   // [2] softmax warps read S (count 4)
-  BAR_P_FULL = 8,    // softmax wrote P (and rescaled O) (count 4)
-  BAR_PV_DONE = 9,   // MMA commit after P.V
-  BAR_X_FULL = 10,   // peer's partial scores landed (1 arrive + tx bytes)
-  BAR_X_EMPTY = 11,  // peer consumed our partial scores (remote arrive)
-  BAR_DRAIN = 12,    // all UMMAs done before TMEM is released
-  BAR_MAP = 13,      // [2] producer warp 0 published the tile's row map (count 1)
-  BAR_LANDED = 15,   // [2] every producer warp's copies of the tile landed (count 4)
-  BAR_X_READ = 17,   // every softmax warp read the peer's partial scores (count 4)
-  NUM_BARS = 18,
+  BAR_KV_FULL = 0,                      // [kMaxStages] publisher -> MMA (count 1)
+  BAR_KV_EMPTY = BAR_KV_FULL + kMaxStages,  // [kMaxStages] UMMA commit after P.V of the stage
+  BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every loader thread's copies landed
+  BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
+  BAR_S_FULL = BAR_MAP + kMaxStages,        // [2] UMMA commit after Q.K^T into S buffer
+  BAR_S_EMPTY = BAR_S_FULL + 2,             // [2] softmax warps read S (count 4)
+  BAR_P_FULL = BAR_S_EMPTY + 2,             // softmax wrote P (and rescaled O) (count 4)
+  BAR_PV_DONE = BAR_P_FULL + 1,             // UMMA commit after P.V
+  BAR_X_FULL = BAR_PV_DONE + 1,             // peer's partial scores landed (1 arrive + tx)
+  BAR_X_EMPTY = BAR_X_FULL + 1,             // peer consumed our partial scores (remote)
+  BAR_X_READ = BAR_X_EMPTY + 1,             // every softmax warp read the peer's scores
+  BAR_DRAIN = BAR_X_READ + 1,               // all UMMAs done before TMEM is released
+  NUM_BARS = BAR_DRAIN + 1,
 };
+static_assert(NUM_BARS <= 64, "barrier area");
 
-constexpr uint32_t kTmemO = 0;     // O half: 256 fp32 columns
-constexpr uint32_t kTmemS = 256;   // S double buffer: 2 x 64 columns
+constexpr uint32_t kTmemO = 0;    // O half: 256 fp32 columns
+constexpr uint32_t kTmemS = 256;  // S double buffer: 2 x 64 columns
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);    // A, B K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);   // B (cKV tile) MN-major
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);   // A, B K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);  // B (cKV tile) MN-major
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t FULL = 0xffffffffu;
+
+// Shared-memory layout for a given number of stored query rows (Mv, multiple of 8).
+struct Layout {
+  uint32_t q, p, x, kv, total;
+  int stages;
+};
+__host__ __device__ inline Layout make_layout(int Mv) {
+  Layout L;
+  L.q = kFixedBytes;                              // 5 slabs of Mv rows x 128 B
+  L.p = L.q + 5u * (uint32_t)Mv * 128u;            // Mv rows x 128 B
+  L.x = L.p + (uint32_t)Mv * 128u;                 // 16 float4 x Mv rows
+  L.kv = (L.x + (uint32_t)Mv * 256u + 1023u) & ~1023u;
+  const uint32_t avail = kSmemLimit - 1024u - L.kv;  // 1024: base alignment slack
+  int st = (int)(avail / kStage);
+  L.stages = st > kMaxStages ? kMaxStages : st;
+  L.total = L.kv + (uint32_t)L.stages * kStage + 1024u;
+  return L;
+}
 
 // Warp-uniform bounded wait: every lane polls (and so acquires) the barrier, and the
 // verdict is agreed with __all_sync so no lane leaves a loop its warp-mates stay in.
@@ -108,6 +131,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int nslab = rank == 0 ? 4 : 5;
   const int col0 = (int)rank * 256;
+  const int Mv = a.Mv;
+  const Layout L = make_layout(Mv);
+  const int NS = L.stages;
+  const uint32_t slabQ = (uint32_t)Mv * 128u;
 
   // ---- work unit: request b, query tile, KV split --------------------------------------
   const int b = blockIdx.y;
@@ -115,7 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int qtile = unit / a.S, split = unit % a.S;
   int c_begin = a.indptr[b], c_end = a.indptr[b + 1];
   int ctx = 0;
-  bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks;
+  const bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks;
   if (table_ok) {
     const irm_chunk last = a.chunks[c_end - 1];
     ctx = last.p_tgt + last.len;
@@ -131,7 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int ke = (int)((int64_t)(split + 1) * kv_tiles / a.S);
   const int ntiles = ke - kb;
 
-  auto bar = [&](int i) -> uint32_t { return sb + kOffMisc + 8u * (uint32_t)i; };
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBars + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
   int32_t* map_src = reinterpret_cast<int32_t*>(smem + kOffMapSrc);
   int32_t* map_delta = reinterpret_cast<int32_t*>(smem + kOffMapDelta);
@@ -139,24 +166,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     if (!table_ok) set_status(a.status, kDevErrBounds);
-    mbar_init(bar(BAR_KV_FULL), kProducerWarps);
-    mbar_init(bar(BAR_KV_FULL + 1), kProducerWarps);
-    mbar_init(bar(BAR_KV_EMPTY), 1);
-    mbar_init(bar(BAR_KV_EMPTY + 1), 1);
-    mbar_init(bar(BAR_S_FULL), 1);
-    mbar_init(bar(BAR_S_FULL + 1), 1);
-    mbar_init(bar(BAR_S_EMPTY), kSoftmaxWarps);
-    mbar_init(bar(BAR_S_EMPTY + 1), kSoftmaxWarps);
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(bar(BAR_KV_FULL + s), 1);
+      mbar_init(bar(BAR_KV_EMPTY + s), 1);
+      mbar_init(bar(BAR_LANDED + s), kLoaderThreads);
+      mbar_init(bar(BAR_MAP + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BAR_S_FULL + s), 1);
+      mbar_init(bar(BAR_S_EMPTY + s), kSoftmaxWarps);
+    }
     mbar_init(bar(BAR_P_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_PV_DONE), 1);
     mbar_init(bar(BAR_X_FULL), 1);
     mbar_init(bar(BAR_X_EMPTY), 1);
-    mbar_init(bar(BAR_DRAIN), 1);
-    mbar_init(bar(BAR_MAP), 1);
-    mbar_init(bar(BAR_MAP + 1), 1);
-    mbar_init(bar(BAR_LANDED), kProducerWarps);
-    mbar_init(bar(BAR_LANDED + 1), kProducerWarps);
     mbar_init(bar(BAR_X_READ), kSoftmaxWarps);
+    mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -173,31 +198,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
 
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-    // ======================= producers: gather, rotate, publish ========================
+    // ======================= loaders: row gather with cp.async =========================
     const int tp = tid - kSoftmaxWarps * 32;
     const int pw = warp - kSoftmaxWarps;
+    const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
+    const int rsub = tp >> 3;   // row within a group of kLoaderThreads / 8
     const __nv_bfloat16* ql = static_cast<const __nv_bfloat16*>(a.q_lat);
     const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
     const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
-    const int per_row = nslab * 8;  // 16-byte chunks per row owned by this CTA
 
-    // Q columns of this CTA, 128 rows (rows past the tile's valid rows are zero).
-    for (int idx = tp; idx < kBM * per_row; idx += 128) {
-      const int m = idx / per_row, rem = idx - m * per_row, slab = rem >> 3, chk = rem & 7;
-      const void* src = a.q_lat;
-      uint32_t nbytes = 0;
-      if (m < rows_valid && ntiles > 0) {
-        const int qi = q0 + m / a.H, h = m % a.H;
-        const int64_t row = ((int64_t)b * a.n_q + qi) * a.H + h;
-        src = (slab < 4) ? (const void*)(ql + row * kDLat + col0 + slab * 64 + chk * 8)
-                         : (const void*)(qr + row * kDRope + chk * 8);
-        nbytes = 16;
+    // Q columns of this CTA: Mv rows (rows past the tile's valid rows are zero filled).
+    if (ntiles > 0) {
+      for (int m = rsub; m < Mv; m += kLoaderThreads / 8) {
+        const bool valid = m < rows_valid;
+        int64_t row = 0;
+        if (valid) {
+          const int qi = q0 + m / a.H, h = m % a.H;
+          row = ((int64_t)b * a.n_q + qi) * a.H + h;
+        }
+        const uint32_t dst = sb + L.q + sw128_offset(m, chk);
+        for (int slab = 0; slab < nslab; ++slab) {
+          const void* src = a.q_lat;
+          if (valid)
+            src = (slab < 4) ? (const void*)(ql + row * kDLat + col0 + slab * 64 + chk * 8)
+                             : (const void*)(qr + row * kDRope + chk * 8);
+          cp_async_16(dst + slab * slabQ, src, valid ? 16u : 0u);
+        }
       }
-      cp_async_16(sb + kOffQ + slab * kSlabQ + sw128_offset(m, chk), src, nbytes);
     }
-    cp_async_commit();
 
-    // Producer warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
+    // Loader warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
     // per-tile row maps: source row (-1 = outside the context, zero filled) and delta.
     int win = c_begin;
     int w_start = INT_MAX, w_end = INT_MAX, w_delta = 0;
@@ -237,8 +267,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int src0 = -1, src1 = -1, d0 = 0, d1 = 0;
       bool need0 = t0 < ctx, need1 = t1 < ctx;
       for (int guard = 0; guard < kBN + 1; ++guard) {
-        const int nvalid = min(32, c_end - win);
         if (!__any_sync(FULL, need0 || need1)) break;
+        const int nvalid = min(32, c_end - win);
         if (nvalid <= 0) {  // the device table does not cover the context
           if (lane == 0) set_status(a.status, kDevErrBounds);
           break;
@@ -279,40 +309,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     bool ok = true;
+    int s = 0;
+    uint32_t ph = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      // stage s is free once the P.V of tile j-2 completed (that also means every producer
-      // finished reading the row map of tile j-2, which shares buffer s)
-      if (j >= 2 && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
+      // stage s is free once the P.V of tile j-NS completed; that also means the MMA used
+      // the row map of tile j-NS, and the publisher finished with it
+      if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
       if (pw == 0) {
         build_map((kb + j) * kBN, s);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
       }
       if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
-      const uint32_t stage = sb + kOffKV + (uint32_t)s * kStage;
-      for (int idx = tp; idx < kBN * per_row; idx += 128) {
-        const int row = idx / per_row, rem = idx - row * per_row, slab = rem >> 3, chk = rem & 7;
+      const uint32_t stage = sb + L.kv + (uint32_t)s * kStage;
+#pragma unroll 2
+      for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
+        const int row = rr + rsub;
         const int sr = map_src[s * kBN + row];
-        const void* src = a.kv;
-        uint32_t nbytes = 0;
-        if (sr >= 0) {
-          src = kvp + (int64_t)sr * kDRow + col0 + slab * 64 + chk * 8;
-          nbytes = 16;
-        }
-        cp_async_16(stage + slab * kSlabKV + sw128_offset(row, chk), src, nbytes);
+        const __nv_bfloat16* rowp = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + col0 + chk * 8;
+        const uint32_t dst = stage + sw128_offset(row, chk);
+        const uint32_t nb = sr >= 0 ? 16u : 0u;
+        for (int slab = 0; slab < nslab; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
       }
-      cp_async_commit();
-      cp_async_wait_all();
+      cp_async_arrive_noinc(bar(BAR_LANDED + s));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    cp_async_wait_all();
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.status, kDevErrTimeout);
+    }
+  } else if (warp == kPubWarp) {
+    // ======================= publisher: rotate k_r, hand tiles to the MMA ==============
+    bool ok = true;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
       if (rank == 1) {
-        // delta-rotation of k_r in shared memory (slab 4 holds k_r of the 64 rows), once
-        // every producer warp's copies of the tile have landed
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_LANDED + s));
-        if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
-        uint8_t* kr = smem + kOffKV + (uint32_t)s * kStage + 4 * kSlabKV;
-        for (int it = tp; it < kBN * 4; it += 128) {
+        // delta-rotation of k_r in shared memory (slab 4 of the stage holds k_r)
+        uint8_t* kr = smem + L.kv + (uint32_t)s * kStage + 4 * kSlabKV;
+        for (int it = lane; it < kBN * 4; it += 32) {
           const int row = it >> 2, pv = it & 3;
           const int d = map_delta[s * kBN + row];
           if (d != 0) {
@@ -328,54 +368,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // the tile's bytes (cp.async and rotated) -> async proxy before the UMMA reads them
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
-    cp_async_wait_all();
     if (!ok) {
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
     }
   } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer (one thread) ===================================
+    // ======================= MMA issuer (one thread), issues in readiness order ========
     if (lane == 0 && ntiles > 0) {
       const uint32_t tO = tmem + kTmemO;
+      int ns = 0, np = 0;            // next Q.K^T tile, next P.V tile
+      int ss = 0, sp = 0;            // their KV stages
+      uint32_t phs = 0;              // kv_full parity of stage ss
       bool ok = true;
-      auto issue_pv = [&](int jj) -> bool {
-        if (!mbar_wait(bar(BAR_P_FULL), jj & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t stage = sb + kOffKV + (uint32_t)(jj & 1) * kStage;
+      uint64_t t_idle = 0;
+      int spins = 0;
+      while (np < ntiles) {
+        bool progressed = false;
+        if (ns < ntiles && mbar_test_wait(bar(BAR_KV_FULL + ss), phs) &&
+            (ns < 2 || mbar_test_wait(bar(BAR_S_EMPTY + (ns & 1)), ((ns >> 1) - 1) & 1))) {
+          tc_fence_after();
+          fence_proxy_async_smem();
+          const uint32_t stage = sb + L.kv + (uint32_t)ss * kStage;
+          const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
+          for (int slab = 0; slab < nslab; ++slab) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sdesc_sw128(sb + kOffP + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
-          umma_bf16(tO, ad, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(sb + L.q + slab * slabQ + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
+              umma_bf16(tS, ad, bd, kIdescS, (slab | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(bar(BAR_S_FULL + (ns & 1)));
+          ++ns;
+          if (++ss == NS) {
+            ss = 0;
+            phs ^= 1u;
+          }
+          progressed = true;
         }
-        umma_commit(bar(BAR_KV_EMPTY + (jj & 1)));
-        umma_commit(bar(BAR_PV_DONE));
-        return true;
-      };
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j & 1;
-        ok = mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, abort_flag);
-        if (ok && j >= 2) ok = mbar_wait(bar(BAR_S_EMPTY + s), ((j >> 1) - 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t stage = sb + kOffKV + (uint32_t)s * kStage;
-        const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)s;
-        for (int slab = 0; slab < nslab; ++slab) {
+        if (np < ns && mbar_test_wait(bar(BAR_P_FULL), np & 1)) {
+          tc_fence_after();
+          const uint32_t stage = sb + L.kv + (uint32_t)sp * kStage;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sb + kOffQ + slab * kSlabQ + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
-            umma_bf16(tS, ad, bd, kIdescS, (slab | kk) ? 1u : 0u);
+            const uint64_t ad = sdesc_sw128(sb + L.p + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
+            umma_bf16(tO, ad, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(BAR_KV_EMPTY + sp));
+          umma_commit(bar(BAR_PV_DONE));
+          ++np;
+          if (++sp == NS) sp = 0;
+          progressed = true;
+        }
+        if (progressed) {
+          spins = 0;
+          t_idle = 0;
+        } else if (++spins >= 64) {
+          spins = 0;
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (*abort_flag || now - t_idle > kWaitLimitNs) {
+            ok = false;
+            break;
           }
         }
-        umma_commit(bar(BAR_S_FULL + s));
-        if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) ok = issue_pv(ntiles - 1);
       if (!ok) {
         *abort_flag = 1;
         set_status(a.status, kDevErrTimeout);
@@ -387,14 +454,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ======================= softmax + epilogue (thread = query row) ===================
     const int m = tid;
+    const bool warp_live = warp * 32 < Mv;       // this warp holds stored query rows
+    const bool row_live = m < Mv;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + kTmemO + lane_base;
     const int pos_m = (m < rows_valid) ? ctx - a.n_q + q0 + m / a.H : pos_last;
     float m_run = -INFINITY, l_run = 0.f;
-    const uint32_t rX = mapa_shared(sb + kOffX, peer);
+    // score exchange buffer, transposed ([16 float4][Mv rows]) so that consecutive rows
+    // are consecutive 16-byte words: conflict-free for both the peer's stores and our loads
+    const uint32_t rX = mapa_shared(sb + L.x, peer);
     const uint32_t rXfull = mapa_shared(bar(BAR_X_FULL), peer);
     const uint32_t rXempty = mapa_shared(bar(BAR_X_EMPTY), peer);
-    const float* X = reinterpret_cast<const float*>(smem + kOffX) + m * kBN;
+    const float4* X = reinterpret_cast<const float4*>(smem + L.x);
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int s = j & 1;
@@ -402,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float sv[kBN];
       if (!(ok = warp_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      {
+      if (warp_live) {
         uint32_t r[32];
         tmem_ld32(tmem + kTmemS + 64u * (uint32_t)s + lane_base, r);
         tmem_ld_wait();
@@ -417,21 +488,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY + s));
 
-      // exchange partial scores with the peer (each side owns half of the contraction)
+      // exchange partial scores with the peer (each side owns part of the contraction)
       if (j >= 1 && !(ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag))) break;
-      if (m == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), kBM * kBN * 4);
+      if (m == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 4u);
+      if (row_live) {
 #pragma unroll
-      for (int i = 0; i < kBN; i += 4)
-        st_async_v4(rX + (uint32_t)(m * kBN + i) * 4u, sv[i], sv[i + 1], sv[i + 2], sv[i + 3],
-                    rXfull);
+        for (int i = 0; i < kBN / 4; ++i)
+          st_async_v4(rX + (uint32_t)(i * Mv + m) * 16u, sv[4 * i], sv[4 * i + 1], sv[4 * i + 2],
+                      sv[4 * i + 3], rXfull);
+      }
       if (!(ok = warp_wait_cluster(bar(BAR_X_FULL), j & 1, abort_flag))) break;
+      if (row_live) {
 #pragma unroll
-      for (int i = 0; i < kBN; i += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(X + i);
-        sv[i] += v.x;
-        sv[i + 1] += v.y;
-        sv[i + 2] += v.z;
-        sv[i + 3] += v.w;
+        for (int i = 0; i < kBN / 4; ++i) {
+          const float4 v = X[i * Mv + m];
+          sv[4 * i] += v.x;
+          sv[4 * i + 1] += v.y;
+          sv[4 * i + 2] += v.z;
+          sv[4 * i + 3] += v.w;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_X_READ));
@@ -440,25 +515,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         else *abort_flag = 1;
       }
 
-      // online softmax in log2 units; causal mask t <= pos_m
+      bool want = false;
       float mx = -INFINITY;
+      if (row_live) {
+        // online softmax in log2 units; causal mask t <= pos_m
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) {
-        float x = sv[i] * a.scale_log2;
-        if (T + i > pos_m) x = -INFINITY;
-        sv[i] = x;
-        mx = fmaxf(mx, x);
+        for (int i = 0; i < kBN; ++i) {
+          float x = sv[i] * a.scale_log2;
+          if (T + i > pos_m) x = -INFINITY;
+          sv[i] = x;
+          mx = fmaxf(mx, x);
+        }
+        // The running max only moves when it grows by more than 2^8: P stays <= 256 and O
+        // is rescaled rarely (the final 1/l uses the same max, so the result is exact).
+        want = (m < rows_valid) && (mx > m_run + 8.f);
       }
-      // The running max only moves when it grows by more than 2^8: P stays <= 256 and
-      // O is rescaled rarely (the final 1/l uses the same max, so the result is exact).
-      const bool want = mx > m_run + 8.f;
-      float corr = 1.f;
-      if (want) corr = fast_exp2(m_run - mx);
+      const float corr = want ? fast_exp2(m_run - mx) : 1.f;
       bool pv_waited = false;
       if (j > 0 && __any_sync(FULL, want)) {
         if (!(ok = warp_wait(bar(BAR_PV_DONE), (j - 1) & 1, abort_flag))) break;
         pv_waited = true;
         tc_fence_after();
+#pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t r[32];
           tmem_ld32(tO + c, r);
@@ -473,25 +551,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_run *= corr;
         m_run = mx;
       }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
       uint32_t pk[kBN / 2];
+      if (row_live) {
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float lsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < kBN; i += 2) {
-        const __nv_bfloat162 h =
-            __floats2bfloat162_rn(fast_exp2(sv[i] - m_use), fast_exp2(sv[i + 1] - m_use));
-        const float2 hf = __bfloat1622float2(h);  // sum what the tensor core will multiply
-        lsum += hf.x + hf.y;
-        pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int i = 0; i < kBN; i += 2) {
+          const __nv_bfloat162 h =
+              __floats2bfloat162_rn(fast_exp2(sv[i] - m_use), fast_exp2(sv[i + 1] - m_use));
+          const float2 hf = __bfloat1622float2(h);  // sum what the tensor core will multiply
+          lsum += hf.x + hf.y;
+          pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        l_run += lsum;
       }
-      l_run += lsum;
       if (j > 0 && !pv_waited &&
           !(ok = warp_wait(bar(BAR_PV_DONE), (j - 1) & 1, abort_flag)))
         break;
+      if (row_live) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(smem + kOffP + sw128_offset(m, c)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(m, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -504,50 +586,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     // ---- epilogue: O / l for this CTA's 256 columns ------------------------------------
-    const bool have = ntiles > 0 && ok && l_run > 0.f;
-    const float inv_l = have ? 1.f / l_run : 0.f;
-    const float lse_v = have ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
-    const bool write_row = m < rows_valid;
-    const int qi = q0 + (write_row ? m / a.H : 0), hh = write_row ? m % a.H : 0;
-    const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
-    const int64_t prow = ((int64_t)b * a.n_qtiles * a.S + unit) * kBM + m;
-    for (int c = 0; c < 256; c += 32) {
-      uint32_t r[32];
-      if (ntiles > 0) {
-        tmem_ld32(tO + c, r);  // warp-collective: every lane executes it
-        tmem_ld_wait();
-      }
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[i]) * inv_l : 0.f;
-      if (!write_row) continue;
-      if (a.S == 1) {
-        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat +
-                                            col0 + c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-          w.x = *reinterpret_cast<uint32_t*>(&h0);
-          w.y = *reinterpret_cast<uint32_t*>(&h1);
-          w.z = *reinterpret_cast<uint32_t*>(&h2);
-          w.w = *reinterpret_cast<uint32_t*>(&h3);
-          o[q] = w;
+    if (warp_live) {
+      const bool have = ntiles > 0 && ok && l_run > 0.f;
+      const float inv_l = have ? 1.f / l_run : 0.f;
+      const float lse_v = have ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      const bool write_row = m < rows_valid;
+      const int qi = q0 + (write_row ? m / a.H : 0), hh = write_row ? m % a.H : 0;
+      const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
+      const int64_t prow = ((int64_t)b * a.n_qtiles * a.S + unit) * kBM + m;
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t r[32];
+        if (ntiles > 0) {
+          tmem_ld32(tO + c, r);  // warp-collective: every lane executes it
+          tmem_ld_wait();
         }
-      } else {
-        float4* o = reinterpret_cast<float4*>(a.opart + prow * kDLat + col0 + c);
+        float v[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[i]) * inv_l : 0.f;
+        if (!write_row) continue;
+        if (a.S == 1) {
+          uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat +
+                                              col0 + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+            w.x = *reinterpret_cast<uint32_t*>(&h0);
+            w.y = *reinterpret_cast<uint32_t*>(&h1);
+            w.z = *reinterpret_cast<uint32_t*>(&h2);
+            w.w = *reinterpret_cast<uint32_t*>(&h3);
+            o[q] = w;
+          }
+        } else {
+          float4* o = reinterpret_cast<float4*>(a.opart + prow * kDLat + col0 + c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
       }
-    }
-    if (write_row && rank == 0) {
-      if (a.S == 1) {
-        if (a.lse != nullptr) a.lse[orow] = lse_v;
-      } else {
-        a.lsepart[prow] = lse_v;
+      if (write_row && rank == 0) {
+        if (a.S == 1) {
+          if (a.lse != nullptr) a.lse[orow] = lse_v;
+        } else {
+          a.lsepart[prow] = lse_v;
+        }
       }
     }
   }
@@ -615,14 +699,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
 
 }  // namespace
 
-size_t attn_smem_bytes() { return kSmemBytes; }
+size_t attn_smem_bytes(int Mv) { return make_layout(Mv).total; }
 
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream) {
+  const Layout L = make_layout(a.Mv);
+  if (L.stages < 2) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+                                       (int)L.total);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.n_qtiles * a.S, a.B);
-  mla_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  mla_attn_kernel<<<grid, kThreads, L.total, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -193,6 +193,8 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   a.qpt = pl.qpt;
   a.n_qtiles = pl.n_qtiles;
   a.S = pl.S;
+  // query rows a tile really holds (decode: H); Q, P and the score exchange store only these
+  a.Mv = std::min(kBM, (std::min(pl.qpt, n_q) * H + 7) / 8 * 8);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = out;
   a.lse = lse;

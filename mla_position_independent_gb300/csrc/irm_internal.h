@@ -45,6 +45,7 @@ struct AttnArgs {
   int qpt;        // queries per 128-row tile = 128 / H
   int n_qtiles;   // ceil(n_q / qpt)
   int S;          // KV splits per query tile
+  int Mv;         // stored query rows per tile (valid rows rounded up to 8)
   float scale_log2;
   void* out;      // bf16 [B, n_q, H, 512] (S == 1)
   float* lse;     // fp32 [B, n_q, H] or nullptr (S == 1)
@@ -61,6 +62,6 @@ cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
-size_t attn_smem_bytes();
+size_t attn_smem_bytes(int Mv);
 
 }  // namespace irm
