@@ -222,10 +222,7 @@ class Workload:
                                 workspace=self.ws, stream=stream)
 
     def launches_per_step(self):
-        if self.kind == "decode":
-            hdr = self.irm.binding.WORKSPACE_HEADER
-            return 2 if self.ws.numel() > hdr else 1   # attention (+ split-KV merge)
-        return 1
+        return 1  # one fused kernel per call (the split-KV merge runs inside it)
 
     def check_status(self):
         self.irm.device_status(self.ws)
@@ -422,8 +419,7 @@ def main():
         unit = "GB/s"
     rf = roofline(wl, ms, pk)
     rf["peak_source"] = pk["src"]
-    rf["kernel"] = "mla_attn_kernel (+ split-KV merge)" if wl.kind == "decode" else (
-        "mla_attn_kernel" if wl.kind == "prefill" else "rotate_gather_kernel")
+    rf["kernel"] = "rotate_gather_kernel" if wl.kind == "gather" else "mla_attn_kernel"
     rf["traffic"] = traffic_for(args.workload)
     e2e = None
     if wl.kind == "decode":

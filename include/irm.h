@@ -34,7 +34,10 @@
  *
  * Workspace.  Each call takes a caller-owned device workspace of at least the size its
  * *_workspace_size function reports (>= IRM_WORKSPACE_HEADER bytes).  Its first
- * IRM_WORKSPACE_HEADER bytes hold the device status word: zero them once before first use.
+ * IRM_WORKSPACE_HEADER bytes hold the device status word.  Zero the whole workspace once
+ * before first use: decode keeps split-KV completion counters in it, which every call
+ * leaves at zero again.  After a call that reported a device error, zero it again.
+ * Calls that share one workspace must not overlap on the GPU.
  */
 #ifndef IRM_H_
 #define IRM_H_

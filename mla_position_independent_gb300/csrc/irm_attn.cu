@@ -16,10 +16,10 @@
 //     the identical online softmax, so P is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
-//   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-5 gather KV rows with
+//   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-7 gather KV rows with
 //     cp.async following the chunk table (completion tracked by an mbarrier, so they run
-//     ahead across stages); 6 allocates TMEM and issues the UMMAs in readiness order;
-//     7 publishes landed tiles, rotating k_r by R(delta) first.
+//     ahead across stages) and, one tile behind, rotate k_r by R(delta) and publish the tile;
+//     8 allocates TMEM and issues the UMMAs in readiness order.
 //   - Only the first Mv rows (valid query rows rounded up to 8) of Q, P and the score
 //     exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
 //     whatever follows in shared memory.  Those rows only ever produce rows of S / O that
@@ -39,10 +39,9 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 64;   // KV rows per tile
 constexpr int kSoftmaxWarps = 4;
-constexpr int kLoaderWarps = 2;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 6
-constexpr int kPubWarp = kMmaWarp + 1;                   // 7
-constexpr int kThreads = (kPubWarp + 1) * 32;            // 256: 2 warps per SM sub-partition
+constexpr int kLoaderWarps = 4;
+constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 8
+constexpr int kThreads = (kMmaWarp + 1) * 32;            // 288
 constexpr int kLoaderThreads = kLoaderWarps * 32;
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
@@ -60,7 +59,7 @@ constexpr uint32_t kFixedBytes = 4096;
 static_assert(kOffAbort + 4 <= kFixedBytes, "fixed area overflow");
 
 enum : int {
-  BAR_KV_FULL = 0,                      // [kMaxStages] publisher -> MMA (count 1)
+  BAR_KV_FULL = 0,                      // [kMaxStages] loaders published the tile (count 4)
   BAR_KV_EMPTY = BAR_KV_FULL + kMaxStages,  // [kMaxStages] UMMA commit after P.V of the stage
   BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every loader thread's copies landed
   BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
@@ -69,9 +68,8 @@ enum : int {
   BAR_P_FULL = BAR_S_EMPTY + 2,             // softmax wrote P (and rescaled O) (count 4)
   BAR_PV_DONE = BAR_P_FULL + 1,             // UMMA commit after P.V
   BAR_X_FULL = BAR_PV_DONE + 1,             // peer's partial scores landed (1 arrive + tx)
-  BAR_X_EMPTY = BAR_X_FULL + 1,             // peer consumed our partial scores (remote)
-  BAR_X_READ = BAR_X_EMPTY + 1,             // every softmax warp read the peer's scores
-  BAR_DRAIN = BAR_X_READ + 1,               // all UMMAs done before TMEM is released
+  BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 4 softmax warps consumed our scores (remote)
+  BAR_DRAIN = BAR_X_EMPTY + 1,              // all UMMAs done before TMEM is released
   NUM_BARS = BAR_DRAIN + 1,
 };
 static_assert(NUM_BARS <= 64, "barrier area");
@@ -124,6 +122,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_attn_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int last_sh;  // this CTA merges the split-KV partials of its query tile
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -164,10 +163,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int32_t* map_delta = reinterpret_cast<int32_t*>(smem + kOffMapDelta);
   uint64_t* phaseF = reinterpret_cast<uint64_t*>(smem + kOffPhase);
 
+
   if (tid == 0) {
+    last_sh = 0;
     if (!table_ok) set_status(a.status, kDevErrBounds);
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), 1);
+      mbar_init(bar(BAR_KV_FULL + s), kLoaderWarps);
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
       mbar_init(bar(BAR_LANDED + s), kLoaderThreads);
       mbar_init(bar(BAR_MAP + s), 1);
@@ -179,8 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_P_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_PV_DONE), 1);
     mbar_init(bar(BAR_X_FULL), 1);
-    mbar_init(bar(BAR_X_EMPTY), 1);
-    mbar_init(bar(BAR_X_READ), kSoftmaxWarps);
+    mbar_init(bar(BAR_X_EMPTY), kSoftmaxWarps);
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
@@ -263,43 +263,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       load_window();
     }
     auto build_map = [&](int T, int s) {
+      // rows T+lane and T+lane+32; the few window chunks overlapping the tile are found with
+      // one ballot and broadcast in turn (no per-row search)
       const int t0 = T + lane, t1 = T + lane + 32;
+      const int t_end = min(T + kBN, ctx);
       int src0 = -1, src1 = -1, d0 = 0, d1 = 0;
-      bool need0 = t0 < ctx, need1 = t1 < ctx;
-      for (int guard = 0; guard < kBN + 1; ++guard) {
-        if (!__any_sync(FULL, need0 || need1)) break;
+      for (int guard = 0; guard < kBN + 1 && T < t_end; ++guard) {
         const int nvalid = min(32, c_end - win);
         if (nvalid <= 0) {  // the device table does not cover the context
           if (lane == 0) set_status(a.status, kDevErrBounds);
           break;
         }
+        unsigned ov = __ballot_sync(FULL, lane < nvalid && w_start < t_end && w_end > T);
+        while (ov != 0u) {
+          const int k = __ffs(ov) - 1;
+          ov &= ov - 1u;
+          const int st = __shfl_sync(FULL, w_start, k), en = __shfl_sync(FULL, w_end, k);
+          const long long of = __shfl_sync(FULL, w_off, k);
+          const int dd = __shfl_sync(FULL, w_delta, k);
+          if (t0 >= st && t0 < en && t0 < t_end) {
+            const long long r = of + (t0 - st);
+            if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src0 = (int)r;
+            d0 = dd;
+          }
+          if (t1 >= st && t1 < en && t1 < t_end) {
+            const long long r = of + (t1 - st);
+            if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src1 = (int)r;
+            d1 = dd;
+          }
+        }
         const int last_end = __shfl_sync(FULL, w_end, nvalid - 1);
-        int k0 = 0, k1 = 0;
-#pragma unroll
-        for (int step = 16; step >= 1; step >>= 1) {
-          const int c0 = k0 + step, c1 = k1 + step;
-          const int s0 = __shfl_sync(FULL, w_start, c0 & 31);
-          const int s1 = __shfl_sync(FULL, w_start, c1 & 31);
-          if (c0 < nvalid && s0 <= t0) k0 = c0;
-          if (c1 < nvalid && s1 <= t1) k1 = c1;
-        }
-        const int st0 = __shfl_sync(FULL, w_start, k0), st1 = __shfl_sync(FULL, w_start, k1);
-        const long long of0 = __shfl_sync(FULL, w_off, k0), of1 = __shfl_sync(FULL, w_off, k1);
-        const int dd0 = __shfl_sync(FULL, w_delta, k0), dd1 = __shfl_sync(FULL, w_delta, k1);
-        if (need0 && t0 < last_end) {
-          const long long r = of0 + (t0 - st0);
-          if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src0 = (int)r;
-          d0 = dd0;
-          need0 = false;
-        }
-        if (need1 && t1 < last_end) {
-          const long long r = of1 + (t1 - st1);
-          if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src1 = (int)r;
-          d1 = dd1;
-          need1 = false;
-        }
-        if (!__any_sync(FULL, need0 || need1)) break;
-        win += nvalid;
+        if (last_end >= t_end) break;  // the window covers the rest of the tile
+        win += nvalid;                 // slide to the chunk holding row last_end
         load_window();
       }
       map_src[s * kBN + lane] = src0;
@@ -308,75 +303,119 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       map_delta[s * kBN + lane + 32] = d1;
     };
 
-    bool ok = true;
-    int s = 0;
-    uint32_t ph = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      // stage s is free once the P.V of tile j-NS completed; that also means the MMA used
-      // the row map of tile j-NS, and the publisher finished with it
-      if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
-      if (pw == 0) {
-        build_map((kb + j) * kBN, s);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
+    // Publish a landed tile: rank 1 rotates k_r by R(delta) in shared memory (loader warp pw
+    // owns rows 16pw..16pw+15), then every warp fences its writes for the async proxy and
+    // arrives on KV_FULL.  Rows form runs of equal delta (chunks): per run every lane
+    // computes the (cos, sin) of its two pairs once and the warp walks the run's rows two at a
+    // time, lane = (row parity h, pair-pair i) rotating pairs 2i, 2i+1 (k_r[2i], k_r[2i+1]
+    // with k_r[32+2i], k_r[33+2i]) through 32-bit shared-memory accesses.
+    auto publish = [&](int sp, uint32_t php) -> bool {
+      if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
+      __syncwarp();
+      if (rank == 1) {
+        uint8_t* kr = smem + L.kv + (uint32_t)sp * kStage + 4 * kSlabKV;
+        const int dA = map_delta[sp * kBN + lane], dB = map_delta[sp * kBN + lane + 32];
+        const int pA = __shfl_up_sync(FULL, dA, 1), pBu = __shfl_up_sync(FULL, dB, 1);
+        const int d31 = __shfl_sync(FULL, dA, 31);
+        const int pB = lane == 0 ? d31 : pBu;
+        const unsigned mA = __ballot_sync(FULL, lane == 0 || dA != pA);
+        const unsigned mB = __ballot_sync(FULL, dB != pB);
+        const int lo = 16 * pw, hi = lo + 16;
+        // runs overlapping [lo, hi): keep starts inside, plus the run containing lo
+        uint64_t all = (uint64_t)mA | ((uint64_t)mB << 32);
+        uint64_t rem = all & (((hi == 64) ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull));
+        rem |= 1ull << lo;  // the run containing row lo starts (for this warp) at lo
+        const int h = lane >> 4, i = lane & 15;
+        const uint32_t woff = (uint32_t)(i & 3) * 4u, xc = (uint32_t)(i >> 2), yc = 4u + (uint32_t)(i >> 2);
+        while (rem != 0) {
+          const int r0 = __ffsll((long long)rem) - 1;
+          rem &= rem - 1;
+          const int r1 = rem != 0 ? __ffsll((long long)rem) - 1 : hi;
+          const int d = map_delta[sp * kBN + r0];
+          if (d == 0) continue;
+          float c0, s0, c1, s1;
+          rope_cos_sin(d, phaseF[2 * i], c0, s0);
+          rope_cos_sin(d, phaseF[2 * i + 1], c1, s1);
+#pragma unroll 4
+          for (int r = r0 + h; r < r1; r += 2) {
+            uint8_t* rowp = kr + r * 128;
+            uint32_t* px = reinterpret_cast<uint32_t*>(rowp + ((xc ^ (uint32_t)(r & 7)) << 4) + woff);
+            uint32_t* py = reinterpret_cast<uint32_t*>(rowp + ((yc ^ (uint32_t)(r & 7)) << 4) + woff);
+            const uint32_t xw = *px, yw = *py;
+            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw));
+            const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw));
+            const __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(xf.x, c0, -yf.x * s0), fmaf(xf.y, c1, -yf.y * s1));
+            const __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(xf.x, s0, yf.x * c0), fmaf(xf.y, s1, yf.y * c1));
+            *px = *reinterpret_cast<const uint32_t*>(&xo);
+            *py = *reinterpret_cast<const uint32_t*>(&yo);
+          }
+        }
       }
-      if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
-      const uint32_t stage = sb + L.kv + (uint32_t)s * kStage;
+      // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads them
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + sp));
+      return true;
+    };
+
+    bool ok = true, pending = false;
+    int s = 0, sprev = 0;
+    uint32_t ph = 0, phprev = 0;
+    for (int j = 0; j <= ntiles; ++j) {
+      if (j < ntiles) {
+        if (pw == 0) {
+          // the map slot is free once tile j-NS was published; build the map now, while stage
+          // s may still be in use by the P.V of tile j-NS
+          if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
+          build_map((kb + j) * kBN, s);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
+        }
+        // stage s is free once the P.V of tile j-NS completed; while waiting for it, publish
+        // the previous tile as soon as its bytes have landed (with few stages the P.V of tile
+        // j-NS may itself be waiting for that tile's scores)
+        if (j >= NS) {
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            if (pending && __all_sync(FULL, mbar_test_wait(bar(BAR_LANDED + sprev), phprev))) {
+              if (!(ok = publish(sprev, phprev))) break;
+              pending = false;
+            }
+            if (__all_sync(FULL, mbar_test_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u))) break;
+            __nanosleep(32);
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          // every lane polled the phase above; one acquiring wait keeps the memory order
+          if (!(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
+        }
+        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
+        const uint32_t stage = sb + L.kv + (uint32_t)s * kStage;
 #pragma unroll 2
-      for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
-        const int row = rr + rsub;
-        const int sr = map_src[s * kBN + row];
-        const __nv_bfloat16* rowp = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + col0 + chk * 8;
-        const uint32_t dst = stage + sw128_offset(row, chk);
-        const uint32_t nb = sr >= 0 ? 16u : 0u;
-        for (int slab = 0; slab < nslab; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
+        for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
+          const int row = rr + rsub;
+          const int sr = map_src[s * kBN + row];
+          const __nv_bfloat16* rowp = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + col0 + chk * 8;
+          const uint32_t dst = stage + sw128_offset(row, chk);
+          const uint32_t nb = sr >= 0 ? 16u : 0u;
+          for (int slab = 0; slab < nslab; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
+        }
+        cp_async_arrive_noinc(bar(BAR_LANDED + s));
       }
-      cp_async_arrive_noinc(bar(BAR_LANDED + s));
+      // publish the previous tile while this one is in flight
+      if (pending && !(ok = publish(sprev, phprev))) break;
+      pending = j < ntiles;
+      sprev = s;
+      phprev = ph;
       if (++s == NS) {
         s = 0;
         ph ^= 1u;
       }
     }
     cp_async_wait_all();
-    if (!ok) {
-      *abort_flag = 1;
-      set_status(a.status, kDevErrTimeout);
-    }
-  } else if (warp == kPubWarp) {
-    // ======================= publisher: rotate k_r, hand tiles to the MMA ==============
-    bool ok = true;
-    int s = 0;
-    uint32_t ph = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
-      if (rank == 1) {
-        // delta-rotation of k_r in shared memory (slab 4 of the stage holds k_r)
-        uint8_t* kr = smem + L.kv + (uint32_t)s * kStage + 4 * kSlabKV;
-        for (int it = lane; it < kBN * 4; it += 32) {
-          const int row = it >> 2, pv = it & 3;
-          const int d = map_delta[s * kBN + row];
-          if (d != 0) {
-            uint4* px = reinterpret_cast<uint4*>(kr + sw128_offset(row, pv));
-            uint4* py = reinterpret_cast<uint4*>(kr + sw128_offset(row, pv + 4));
-            uint4 x = *px, y = *py;
-            float cc[8], ss[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[8 * pv + e], cc[e], ss[e]);
-            rotate_pairs8(x, y, cc, ss);
-            *px = x;
-            *py = y;
-          }
-        }
-      }
-      // the tile's bytes (cp.async and rotated) -> async proxy before the UMMA reads them
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));
-      if (++s == NS) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
     if (!ok) {
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
@@ -435,6 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           t_idle = 0;
         } else if (++spins >= 64) {
           spins = 0;
+          __nanosleep(64);
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) t_idle = now;
           if (*abort_flag || now - t_idle > kWaitLimitNs) {
@@ -459,6 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + kTmemO + lane_base;
     const int pos_m = (m < rows_valid) ? ctx - a.n_q + q0 + m / a.H : pos_last;
+    const int pos_first = ctx - a.n_q + q0;  // position of the tile's first query
     float m_run = -INFINITY, l_run = 0.f;
     // score exchange buffer, transposed ([16 float4][Mv rows]) so that consecutive rows
     // are consecutive 16-byte words: conflict-free for both the peer's stores and our loads
@@ -509,23 +550,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_X_READ));
-      if (m == 0) {  // all four warps read the peer's scores: it may send the next tile's
-        if (mbar_wait(bar(BAR_X_READ), j & 1, abort_flag)) mbar_arrive_remote(rXempty);
-        else *abort_flag = 1;
-      }
+      // this warp is done with the peer's scores (the values are in registers and used, so a
+      // relaxed arrive suffices; a release would stall on this lane's outstanding st.async)
+      if (lane == 0) mbar_arrive_remote_relaxed(rXempty);
 
       bool want = false;
       float mx = -INFINITY;
       if (row_live) {
-        // online softmax in log2 units; causal mask t <= pos_m
+        // causal mask t <= pos_m, only on tiles that reach past the tile's first query
+        if (T + kBN - 1 > pos_first) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          float x = sv[i] * a.scale_log2;
-          if (T + i > pos_m) x = -INFINITY;
-          sv[i] = x;
-          mx = fmaxf(mx, x);
+          for (int i = 0; i < kBN; ++i)
+            if (T + i > pos_m) sv[i] = -INFINITY;
         }
+        // row max as a tree (scale > 0, so max(s) * scale = max(s * scale))
+        float t32[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t32[i] = fmaxf(sv[i], sv[i + 32]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) t32[i] = fmaxf(t32[i], t32[i + w]);
+        mx = t32[0] * a.scale_log2;  // log2 units
         // The running max only moves when it grows by more than 2^8: P stays <= 256 and O
         // is rescaled rarely (the final 1/l uses the same max, so the result is exact).
         want = (m < rows_valid) && (mx > m_run + 8.f);
@@ -554,16 +600,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pk[kBN / 2];
       if (row_live) {
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float lsum = 0.f;
+        const float c = a.scale_log2;
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = 0.f;
 #pragma unroll
         for (int i = 0; i < kBN; i += 2) {
-          const __nv_bfloat162 h =
-              __floats2bfloat162_rn(fast_exp2(sv[i] - m_use), fast_exp2(sv[i + 1] - m_use));
-          const float2 hf = __bfloat1622float2(h);  // sum what the tensor core will multiply
-          lsum += hf.x + hf.y;
+          const float p0 = fast_exp2(fmaf(sv[i], c, -m_use));
+          const float p1 = fast_exp2(fmaf(sv[i + 1], c, -m_use));
+          part[(i >> 1) & 7] += p0 + p1;
+          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
           pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        l_run += lsum;
+        l_run += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       }
       if (j > 0 && !pv_waited &&
           !(ok = warp_wait(bar(BAR_PV_DONE), (j - 1) & 1, abort_flag)))
@@ -626,16 +675,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
-      if (write_row && rank == 0) {
+      if (write_row) {
         if (a.S == 1) {
-          if (a.lse != nullptr) a.lse[orow] = lse_v;
+          if (a.lse != nullptr && rank == 0) a.lse[orow] = lse_v;
         } else {
-          a.lsepart[prow] = lse_v;
+          a.lsepart[(int64_t)rank * a.B * a.n_qtiles * a.S * kBM + prow] = lse_v;
         }
       }
     }
+    if (a.S > 1) {
+      // Split-KV merge, fused: the last CTA (per rank) to finish a query tile merges the S
+      // partials of its 256 columns after teardown (threadfence-reduction pattern; the
+      // counter resets itself, so the workspace stays reusable).
+      __threadfence();
+      named_bar_sync(1, kSoftmaxWarps * 32);
+      if (m == 0) {
+        int* cnt = a.counters + ((int64_t)b * a.n_qtiles + qtile) * 2 + rank;
+        last_sh = (atomicAdd(cnt, 1) == a.S - 1) ? 1 : 0;
+      }
+    }
   }
-
   // ---- teardown ---------------------------------------------------------------------
   __syncthreads();
   cluster_arrive();  // the peer no longer sends to this CTA's shared memory
@@ -644,57 +703,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// LSE-weighted merge of the split-KV partials; one warp per (request, query, head) row.
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnArgs a) {
-  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)a.B * a.n_q * a.H;
-  if (gw >= total) return;
-  const int h = (int)(gw % a.H);
-  const int qi = (int)((gw / a.H) % a.n_q);
-  const int b = (int)(gw / ((int64_t)a.H * a.n_q));
-  const int qtile = qi / a.qpt;
-  const int m = (qi - qtile * a.qpt) * a.H + h;
-  const int64_t base = ((int64_t)b * a.n_qtiles * a.S + (int64_t)qtile * a.S) * kBM + m;
-  float mx = -INFINITY;
-  for (int s = 0; s < a.S; ++s) mx = fmaxf(mx, a.lsepart[base + (int64_t)s * kBM]);
-  float4 acc[4];
+  if (a.S > 1 && last_sh) {
+    // all threads: item = (query row, 16-byte group of this rank's 256 columns)
+    __threadfence();
+    const float* lse_r = a.lsepart + (int64_t)rank * a.B * a.n_qtiles * a.S * kBM;
+    const int64_t ubase = ((int64_t)b * a.n_qtiles + qtile) * a.S;  // first unit of the tile
+    for (int it = tid; it < rows_valid * 64; it += kThreads) {
+      const int mm = it >> 6, c4 = it & 63;
+      // online merge over the partials, 8 at a time with all their loads in flight
+      float mx = -INFINITY, wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sp0 = 0; sp0 < a.S; sp0 += 8) {
+        float l[8];
+        float4 v[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < a.S; ++s) {
-      const float l = a.lsepart[base + (int64_t)s * kBM];
-      if (l == -INFINITY) continue;
-      const float w = __expf(l - mx);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(a.opart + (base + (int64_t)s * kBM) * kDLat);
+        for (int k = 0; k < 8; ++k) {
+          const int sp = sp0 + k;
+          l[k] = -INFINITY;
+          v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (sp < a.S) {
+            l[k] = lse_r[(ubase + sp) * kBM + mm];
+            v[k] = reinterpret_cast<const float4*>(a.opart + ((ubase + sp) * kBM + mm) * kDLat + col0)[c4];
+          }
+        }
+        float cm = mx;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 v = src[k * 32 + lane];
-        acc[k].x += w * v.x;
-        acc[k].y += w * v.y;
-        acc[k].z += w * v.z;
-        acc[k].w += w * v.w;
+        for (int k = 0; k < 8; ++k) cm = fmaxf(cm, l[k]);
+        if (cm == -INFINITY) continue;
+        const float corr = (mx == -INFINITY) ? 0.f : __expf(mx - cm);
+        wsum *= corr;
+        acc.x *= corr;
+        acc.y *= corr;
+        acc.z *= corr;
+        acc.w *= corr;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float w = (l[k] == -INFINITY) ? 0.f : __expf(l[k] - cm);
+          wsum += w;
+          acc.x += w * v[k].x;
+          acc.y += w * v[k].y;
+          acc.z += w * v[k].z;
+          acc.w += w * v[k].w;
+        }
+        mx = cm;
       }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      const int qi = q0 + mm / a.H, hh = mm % a.H;
+      const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 w2;
+      w2.x = *reinterpret_cast<const uint32_t*>(&h0);
+      w2.y = *reinterpret_cast<const uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + col0 + c4 * 4) = w2;
+      if (c4 == 0 && rank == 0 && a.lse != nullptr)
+        a.lse[orow] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
     }
+    __syncthreads();
+    if (tid == 0) a.counters[((int64_t)b * a.n_qtiles + qtile) * 2 + rank] = 0;
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + h;
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + orow * kDLat;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int col = (k * 32 + lane) * 4;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
-    uint2 w;
-    w.x = *reinterpret_cast<uint32_t*>(&h0);
-    w.y = *reinterpret_cast<uint32_t*>(&h1);
-    *reinterpret_cast<uint2*>(o + col) = w;
-  }
-  if (lane == 0 && a.lse != nullptr) a.lse[orow] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -709,13 +776,6 @@ cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.n_qtiles * a.S, a.B);
   mla_attn_kernel<<<grid, kThreads, L.total, stream>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
-  const int64_t warps = (int64_t)a.B * a.n_q * a.H;
-  const int64_t blocks = (warps * 32 + 255) / 256;
-  combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -134,10 +134,16 @@ int choose_splits(int B, int64_t max_ctx, int sms) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t partial_bytes(int B, int units) {
-  const size_t o = (size_t)B * units * kBM * IRM_D_LAT * sizeof(float);
-  const size_t l = (size_t)B * units * kBM * sizeof(float);
-  return align_up(o, 256) + align_up(l, 256);
+// Split-KV scratch: fp32 partial O, per-rank partial LSE, finished-split counters.
+size_t partial_o_bytes(int B, int units) {
+  return align_up((size_t)B * units * kBM * IRM_D_LAT * sizeof(float), 256);
+}
+size_t partial_lse_bytes(int B, int units) {
+  return align_up((size_t)2 * B * units * kBM * sizeof(float), 256);
+}
+size_t counter_bytes(int B, int n_qtiles) { return align_up((size_t)B * n_qtiles * 2 * sizeof(int), 256); }
+size_t partial_bytes(int B, int n_qtiles, int S) {
+  return partial_o_bytes(B, n_qtiles * S) + partial_lse_bytes(B, n_qtiles * S) + counter_bytes(B, n_qtiles);
 }
 
 struct AttnPlan {
@@ -155,7 +161,7 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
   if (p->n_qtiles > 32767) return fail(IRM_ERR_UNSUPPORTED, "too many query tiles (%d)", p->n_qtiles);
   if (B > 65535) return fail(IRM_ERR_UNSUPPORTED, "B=%d exceeds 65535", B);
   p->S = decode ? choose_splits(B, info.max_ctx, num_sms()) : 1;
-  p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles * p->S) : 0);
+  p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
   return IRM_OK;
 }
 
@@ -201,17 +207,14 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   a.status = static_cast<int*>(workspace);
   uint8_t* ws = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
   if (pl.S > 1) {
+    const int units = pl.n_qtiles * pl.S;
     a.opart = reinterpret_cast<float*>(ws);
-    a.lsepart = reinterpret_cast<float*>(
-        ws + align_up((size_t)B * pl.n_qtiles * pl.S * kBM * IRM_D_LAT * sizeof(float), 256));
+    a.lsepart = reinterpret_cast<float*>(ws + partial_o_bytes(B, units));
+    a.counters = reinterpret_cast<int*>(ws + partial_o_bytes(B, units) + partial_lse_bytes(B, units));
   }
   std::memcpy(a.phase.F, rope_phase().F, sizeof a.phase.F);
   cudaError_t e = irm::launch_mla_attn(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "mla attention launch");
-  if (pl.S > 1) {
-    e = irm::launch_combine(a, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "split-KV combine launch");
-  }
   return IRM_OK;
 }
 

@@ -50,7 +50,8 @@ struct AttnArgs {
   void* out;      // bf16 [B, n_q, H, 512] (S == 1)
   float* lse;     // fp32 [B, n_q, H] or nullptr (S == 1)
   float* opart;   // fp32 [B, n_qtiles*S, 128, 512] (S > 1)
-  float* lsepart; // fp32 [B, n_qtiles*S, 128] (S > 1)
+  float* lsepart; // fp32 [2 ranks][B, n_qtiles*S, 128] (S > 1)
+  int* counters;  // int [B, n_qtiles, 2] finished-split counters, zero between calls (S > 1)
   int* status;
   struct {
     uint64_t F[32];
@@ -61,7 +62,6 @@ cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int
                              int64_t* row_start, cudaStream_t stream);
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
 size_t attn_smem_bytes(int Mv);
 
 }  // namespace irm
