@@ -165,6 +165,30 @@ irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int
                                cudaStream_t stream);
 
 /*
+ * Decode without any device allocation by the caller.  The method's pages have no
+ * counterpart to this entry point: it exists for callers that cannot call cudaMalloc --
+ * for example a plugin that runs inside a host application which owns the device memory
+ * pool, or code that must not allocate while a CUDA graph is being built -- and so cannot
+ * provide the workspace that irm_mla_attn_decode wants.
+ *
+ * Same arguments and results as irm_mla_attn_decode, minus the workspace.  The split-KV
+ * scratch lives in a fixed 32 MiB device array inside this library (every GPU that loads
+ * the library holds it until the process exits).  A decode whose scratch would exceed 32 MiB
+ * (IRM_ERR_WORKSPACE) is rejected before anything is launched; use irm_mla_attn_decode then.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.  Each call
+ * clears the array's status word and completion counters on `stream` (cudaMemsetAsync) and
+ * allocates nothing.  All calls share the one array: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialized by the caller.  Device-side status
+ * (timeouts, out-of-range rows) is not reported by this entry point.
+ */
+irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, int B, int H,
+                                       const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                       const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                       const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                       void* out, float* lse, cudaStream_t stream);
+
+/*
  * Fused delta-rotate + absorbed MLA prefill attention (n_q causal query tokens per request,
  * the last n_q positions of each request's assembled context).
  *   q_lat [B, n_q, H, 512], q_rope [B, n_q, H, 64], out [B, n_q, H, 512] bf16,

@@ -23,7 +23,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 
 EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_chunks",
            "irm_device_status", "irm_assemble_kv_workspace_size", "irm_assemble_kv",
-           "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
+           "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode", "irm_mla_attn_decode_noalloc",
            "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill"]
 
 
@@ -52,6 +52,8 @@ def lib():
         L.irm_mla_attn_decode_workspace_size.argtypes = [P, P, I, I, P]
         L.irm_mla_attn_decode.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float, P, P, P,
                                           SZ, P]
+        L.irm_mla_attn_decode_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float,
+                                                  P, P, P]
         L.irm_mla_attn_prefill_workspace_size.argtypes = [I, I, I, P]
         L.irm_mla_attn_prefill.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
                                            P, P, SZ, P]
@@ -190,6 +192,26 @@ def irm_mla_attn_decode(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale
         float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return out, lse, workspace
+
+
+def irm_mla_attn_decode_noalloc(q_lat, q_rope, table: ChunkTable, kv_rows,
+                                softmax_scale=DEFAULT_SCALE, out=None, lse=None, stream=None):
+    """Decode for callers that cannot allocate device memory: the library's own fixed
+    scratch array replaces the workspace (see include/irm.h for the limit)."""
+    B, H = int(q_lat.shape[0]), int(q_lat.shape[-2])
+    _need(q_lat, torch.bfloat16, "q_lat")
+    _need(q_rope, torch.bfloat16, "q_rope")
+    _need(kv_rows, torch.bfloat16, "kv_rows", 2)
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_lat.device)
+    _need(out, torch.bfloat16, "out")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    _check(lib().irm_mla_attn_decode_noalloc(
+        _ptr(q_lat), _ptr(q_rope), B, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
+        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
 
 
 def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,

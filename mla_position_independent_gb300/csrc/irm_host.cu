@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -218,6 +219,34 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   return IRM_OK;
 }
 
+// Scratch for irm_mla_attn_decode_noalloc: a fixed device array in this library, so that
+// callers that cannot allocate device memory still get split-KV decode.  It exists once
+// per device that loads the library and lives until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[128] = {};
+
+// Device address of the scratch array for the current device.  In host code the array's
+// name is only a host-side stand-in, so the address comes from cudaGetSymbolAddress, once
+// per device, with that device current.
+irm_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 128) return fail(IRM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return IRM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -346,6 +375,36 @@ irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int
                                cudaStream_t stream) {
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
                   n_rows, softmax_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, int B, int H,
+                                       const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                       const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                       const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                       void* out, float* lse, cudaStream_t stream) {
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
+  if (st != IRM_OK) return st;
+  AttnPlan pl;
+  if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
+  if (pl.ws_bytes > kNoAllocScratchBytes)
+    return fail(IRM_ERR_WORKSPACE,
+                "this decode needs %zu bytes of scratch, more than the %zu bytes the no-allocation "
+                "entry point holds; use irm_mla_attn_decode with a workspace",
+                pl.ws_bytes, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != IRM_OK) return st;
+  // The array keeps the last call's contents: clear the status word and the split-KV
+  // completion counters, which must start at zero.
+  cudaError_t e = cudaMemsetAsync(ws, 0, IRM_WORKSPACE_HEADER, stream);
+  if (e == cudaSuccess && pl.S > 1) {
+    const int units = pl.n_qtiles * pl.S;
+    const size_t off = IRM_WORKSPACE_HEADER + partial_o_bytes(B, units) + partial_lse_bytes(B, units);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + off, 0, counter_bytes(B, pl.n_qtiles), stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+                  n_rows, softmax_scale, out, lse, ws, kNoAllocScratchBytes, stream, true);
 }
 
 irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes) {

@@ -1,0 +1,73 @@
+"""The no-allocation decode entry point (irm_mla_attn_decode_noalloc), called through the C
+ABI, must give the same output as irm_mla_attn_decode with a caller workspace, on two
+calls in a row.  It serves callers that cannot call cudaMalloc themselves (for example a
+plugin inside an application that owns the device memory pool), so it uses a fixed scratch
+array inside the library instead of a workspace.
+
+This file is collected last on purpose, so that a run stopping at the first failure has
+already run every other test.  It must pass in a fresh process and after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from mla_position_independent_gb300 import synth
+from helpers import SCALE, TOL_MAX_ABS, TOL_REL_L2, max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _call_noalloc(L, case, table, ql, qr, out, lse):
+    st = L.irm_mla_attn_decode_noalloc(
+        ql.data_ptr(), qr.data_ptr(), ql.shape[0], ql.shape[1], table.chunks_host.ctypes.data,
+        table.indptr_host.ctypes.data, table.chunks_dev.data_ptr(), table.indptr_dev.data_ptr(),
+        case.kv_rows.data_ptr(), case.kv_rows.shape[0], ctypes.c_float(SCALE), out.data_ptr(),
+        lse.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+def test_noalloc_decode_matches_workspace_decode():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import mla_position_independent_gb300 as irm
+    L = irm.lib()
+    case = synth.v2lite_decode(0, device="cuda")
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    ql, qr = case.q_lat[:, 0].contiguous(), case.q_rope[:, 0].contiguous()
+    ref, ref_lse, ws = irm.irm_mla_attn_decode(
+        ql, qr, table, case.kv_rows, SCALE,
+        lse=torch.empty(ql.shape[:2], dtype=torch.float32, device="cuda"))
+    irm.device_status(ws)
+    ref = ref.float().cpu().numpy()
+    ref_lse = ref_lse.cpu().numpy()
+    for _ in range(2):  # the scratch keeps the previous call's contents
+        out = torch.full_like(case.q_lat[:, 0], float("nan"))
+        lse = torch.full(ql.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        assert _call_noalloc(L, case, table, ql, qr, out, lse) == 0, L.irm_last_error().decode()
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        assert rel_l2(got, ref) <= TOL_REL_L2 and max_abs(got, ref) <= TOL_MAX_ABS
+        assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) < 1e-3
+
+
+def test_noalloc_rejects_decode_larger_than_its_scratch():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import mla_position_independent_gb300 as irm
+    L = irm.lib()
+    # 64 requests x 128 heads x 32768 rows needs more split-KV scratch than the array holds
+    reqs = [[(0, 32, 0, 0), (32, 32736, 0, 0)] for _ in range(64)]
+    chunks, indptr = synth.make_table(reqs)
+    need = ctypes.c_size_t(0)
+    assert L.irm_mla_attn_decode_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 64, 128,
+                                                ctypes.byref(need)) == 0
+    if need.value <= 32 << 20:
+        pytest.skip("this device splits the decode too little to exceed the scratch")
+    dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: rejected first
+    st = L.irm_mla_attn_decode_noalloc(
+        dummy.data_ptr(), dummy.data_ptr(), 64, 128, chunks.ctypes.data, indptr.ctypes.data,
+        dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), 40000, ctypes.c_float(SCALE),
+        dummy.data_ptr(), None, None)
+    assert st == -8 and b"no-allocation" in L.irm_last_error()
