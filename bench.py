@@ -74,13 +74,8 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64,
-                     device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from mla_position_independent_gb300.replicas import max_over_ranks as _m
+    return _m(x, world, device="cuda" if torch.cuda.is_available() else "cpu")
 
 
 # --------------------------------------------------------------------------- clocks
