@@ -432,6 +432,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int spins = 0;
       while (np < ntiles) {
         bool progressed = false;
+        // P.V first: the softmax waits for it before writing the next P
+        if (np < ns && mbar_test_wait(bar(BAR_P_FULL), np & 1)) {
+          tc_fence_after();
+          const uint32_t stage = sb + L.kv + (uint32_t)sp * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(sb + L.p + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
+            umma_bf16(tO, ad, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(BAR_KV_EMPTY + sp));
+          umma_commit(bar(BAR_PV_DONE));
+          ++np;
+          if (++sp == NS) sp = 0;
+          progressed = true;
+        }
         if (ns < ntiles && mbar_test_wait(bar(BAR_KV_FULL + ss), phs) &&
             (ns < 2 || mbar_test_wait(bar(BAR_S_EMPTY + (ns & 1)), ((ns >> 1) - 1) & 1))) {
           tc_fence_after();
@@ -452,21 +468,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ss = 0;
             phs ^= 1u;
           }
-          progressed = true;
-        }
-        if (np < ns && mbar_test_wait(bar(BAR_P_FULL), np & 1)) {
-          tc_fence_after();
-          const uint32_t stage = sb + L.kv + (uint32_t)sp * kStage;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sb + L.p + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
-            umma_bf16(tO, ad, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(bar(BAR_KV_EMPTY + sp));
-          umma_commit(bar(BAR_PV_DONE));
-          ++np;
-          if (++sp == NS) sp = 0;
           progressed = true;
         }
         if (progressed) {
@@ -704,60 +705,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   if (a.S > 1 && last_sh) {
-    // all threads: item = (query row, 16-byte group of this rank's 256 columns)
+    // Merge, staged through shared memory (the pipeline is done): for a block of rows, every
+    // partial's 256 columns of this rank are fetched with one burst of cp.async, then each
+    // (row, 4-column group) item is merged from shared memory.
     __threadfence();
     const float* lse_r = a.lsepart + (int64_t)rank * a.B * a.n_qtiles * a.S * kBM;
     const int64_t ubase = ((int64_t)b * a.n_qtiles + qtile) * a.S;  // first unit of the tile
-    for (int it = tid; it < rows_valid * 64; it += kThreads) {
-      const int mm = it >> 6, c4 = it & 63;
-      // online merge over the partials, 8 at a time with all their loads in flight
-      float mx = -INFINITY, wsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int sp0 = 0; sp0 < a.S; sp0 += 8) {
-        float l[8];
-        float4 v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int sp = sp0 + k;
-          l[k] = -INFINITY;
-          v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (sp < a.S) {
-            l[k] = lse_r[(ubase + sp) * kBM + mm];
-            v[k] = reinterpret_cast<const float4*>(a.opart + ((ubase + sp) * kBM + mm) * kDLat + col0)[c4];
+    const uint32_t per_row = (uint32_t)a.S * (1024u + 4u);           // partial O row half + lse
+    const int rows_blk = max(1, min(rows_valid, (int)((L.total - 1024u) / per_row)));
+    float* so = reinterpret_cast<float*>(smem);                       // [S][rows_blk][256]
+    float* sl = so + (size_t)a.S * rows_blk * 256;                    // [S][rows_blk]
+    for (int r0 = 0; r0 < rows_valid; r0 += rows_blk) {
+      const int nr = min(rows_blk, rows_valid - r0);
+      const int n16 = a.S * nr * 64;
+      for (int it = tid; it < n16; it += kThreads) {
+        const int c16 = it & 63, rr = (it >> 6) % nr, sp = (it >> 6) / nr;
+        const float* src = a.opart + ((ubase + sp) * kBM + r0 + rr) * kDLat + col0 + c16 * 4;
+        cp_async_16(smem_u32(so + ((size_t)(sp * rows_blk + rr) * 256 + c16 * 4)), src, 16u);
+      }
+      cp_async_commit();
+      for (int it = tid; it < a.S * nr; it += kThreads) {
+        const int rr = it % nr, sp = it / nr;
+        sl[sp * rows_blk + rr] = lse_r[(ubase + sp) * kBM + r0 + rr];
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      for (int it = tid; it < nr * 64; it += kThreads) {
+        const int rr = it >> 6, c4 = it & 63;
+        float mx = -INFINITY;
+        for (int sp = 0; sp < a.S; ++sp) mx = fmaxf(mx, sl[sp * rows_blk + rr]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        if (mx != -INFINITY) {
+          for (int sp = 0; sp < a.S; ++sp) {
+            const float l = sl[sp * rows_blk + rr];
+            const float w = (l == -INFINITY) ? 0.f : __expf(l - mx);
+            const float4 v = reinterpret_cast<const float4*>(so + (size_t)(sp * rows_blk + rr) * 256)[c4];
+            wsum += w;
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
           }
         }
-        float cm = mx;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) cm = fmaxf(cm, l[k]);
-        if (cm == -INFINITY) continue;
-        const float corr = (mx == -INFINITY) ? 0.f : __expf(mx - cm);
-        wsum *= corr;
-        acc.x *= corr;
-        acc.y *= corr;
-        acc.z *= corr;
-        acc.w *= corr;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float w = (l[k] == -INFINITY) ? 0.f : __expf(l[k] - cm);
-          wsum += w;
-          acc.x += w * v[k].x;
-          acc.y += w * v[k].y;
-          acc.z += w * v[k].z;
-          acc.w += w * v[k].w;
-        }
-        mx = cm;
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const int mm = r0 + rr;
+        const int qi = q0 + mm / a.H, hh = mm % a.H;
+        const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        uint2 w2;
+        w2.x = *reinterpret_cast<const uint32_t*>(&h0);
+        w2.y = *reinterpret_cast<const uint32_t*>(&h1);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + col0 + c4 * 4) = w2;
+        if (c4 == 0 && rank == 0 && a.lse != nullptr)
+          a.lse[orow] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
       }
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      const int qi = q0 + mm / a.H, hh = mm % a.H;
-      const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 w2;
-      w2.x = *reinterpret_cast<const uint32_t*>(&h0);
-      w2.y = *reinterpret_cast<const uint32_t*>(&h1);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + col0 + c4 * 4) = w2;
-      if (c4 == 0 && rank == 0 && a.lse != nullptr)
-        a.lse[orow] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+      __syncthreads();
     }
     __syncthreads();
     if (tid == 0) a.counters[((int64_t)b * a.n_qtiles + qtile) * 2 + rank] = 0;

@@ -114,17 +114,20 @@ irm_status validate(const irm_chunk* chunks, const int32_t* indptr, int B, int64
 constexpr int kBM = 128;
 constexpr int kBN = 64;
 
-// Decode split-KV factor: the attention runs one 2-CTA cluster per (request, split); pick
-// the split count that minimises waves x (tiles per split + fixed cost).
-int choose_splits(int B, int64_t max_ctx, int sms) {
+// Decode split-KV factor: the attention runs one 2-CTA cluster per (request, split); pick the
+// split count that minimises waves x (tiles per split + fixed cost), charging each split
+// for the merge its query tile then needs (in tile-equivalents, grows with the head count).
+int choose_splits(int B, int64_t max_ctx, int H, int sms) {
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles = (max_ctx + kBN - 1) / kBN;
+  const double merge_per_split = 0.25 + 0.02 * H;
   int best = 1;
   double best_cost = 1e30;
   for (int S = 1; S <= 64 && S <= tiles; ++S) {
     const int64_t units = (int64_t)B * S;
     const int64_t waves = (units + pairs - 1) / pairs;
-    const double cost = (double)waves * ((double)((tiles + S - 1) / S) + 3.0) + (S > 1 ? 1.0 : 0.0);
+    const double cost = (double)waves * ((double)((tiles + S - 1) / S) + 3.0) +
+                        (S > 1 ? merge_per_split * S : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = S;
@@ -161,7 +164,7 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
   p->n_qtiles = (n_q + p->qpt - 1) / p->qpt;
   if (p->n_qtiles > 32767) return fail(IRM_ERR_UNSUPPORTED, "too many query tiles (%d)", p->n_qtiles);
   if (B > 65535) return fail(IRM_ERR_UNSUPPORTED, "B=%d exceeds 65535", B);
-  p->S = decode ? choose_splits(B, info.max_ctx, num_sms()) : 1;
+  p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms()) : 1;
   p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
   return IRM_OK;
 }
