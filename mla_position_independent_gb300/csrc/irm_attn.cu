@@ -16,15 +16,19 @@
 //     the identical online softmax, so P is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
+//   - TMEM holds O (256 columns), two score buffers (64 columns each) and the CTA's four
+//     cKV slabs of Q as bf16 pairs (128 columns); the softmax writes P as bf16 pairs over
+//     the score buffer it just read, and both Q.K^T and P.V take their A operand from
+//     TMEM.  Only CTA 1's q_rope slab sits in shared memory, so nearly all of shared memory
+//     is KV pipeline stages.
 //   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-7 gather KV rows with
 //     cp.async following the chunk table (completion tracked by an mbarrier, so they run
 //     ahead across stages) and, one tile behind, rotate k_r by R(delta) and publish the tile;
 //     8 allocates TMEM and issues the UMMAs in readiness order.
-//   - Only the first Mv rows (valid query rows rounded up to 8) of Q, P and the score
-//     exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
-//     whatever follows in shared memory.  Those rows only ever produce rows of S / O that
-//     are never read, and the space saved becomes extra KV pipeline stages (decode with
-//     16 heads runs 5 stages; 128-row tiles run 2).
+//   - Only the first Mv rows (valid query rows rounded up to 8) of the q_rope slab and the
+//     score exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
+//     whatever follows in shared memory (or TMEM lanes nobody wrote).  Those rows only
+//     ever produce rows of S / O that are never read.
 // Every pipeline wait is bounded (2 s) and reports a timeout in the status word.
 #include <cuda_runtime.h>
 #include <climits>
@@ -45,7 +49,6 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;            // 288
 constexpr int kLoaderThreads = kLoaderWarps * 32;
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
-constexpr uint32_t kStage = 5 * kSlabKV; // one KV pipeline stage (up to 5 slabs)
 constexpr uint32_t kSmemLimit = 232448;
 
 // Fixed area at the start of shared memory.
@@ -64,10 +67,10 @@ enum : int {
   BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every loader thread's copies landed
   BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
   BAR_S_FULL = BAR_MAP + kMaxStages,        // [2] UMMA commit after Q.K^T into S buffer
-  BAR_S_EMPTY = BAR_S_FULL + 2,             // [2] softmax warps read S (count 4)
-  BAR_P_FULL = BAR_S_EMPTY + 2,             // softmax wrote P (and rescaled O) (count 4)
-  BAR_PV_DONE = BAR_P_FULL + 1,             // UMMA commit after P.V
-  BAR_X_FULL = BAR_PV_DONE + 1,             // peer's partial scores landed (1 arrive + tx)
+  BAR_PV_DONE = BAR_S_FULL + 2,             // [2] UMMA commit after P.V of the P in S buffer
+  BAR_P_FULL = BAR_PV_DONE + 2,             // softmax wrote P (and rescaled O) (count 4)
+  BAR_Q_FULL = BAR_P_FULL + 1,              // softmax warps stored Q in TMEM (count 4)
+  BAR_X_FULL = BAR_Q_FULL + 1,              // peer's partial scores landed (1 arrive + tx)
   BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 4 softmax warps consumed our scores (remote)
   BAR_DRAIN = BAR_X_EMPTY + 1,              // all UMMAs done before TMEM is released
   NUM_BARS = BAR_DRAIN + 1,
@@ -75,7 +78,8 @@ enum : int {
 static_assert(NUM_BARS <= 64, "barrier area");
 
 constexpr uint32_t kTmemO = 0;    // O half: 256 fp32 columns
-constexpr uint32_t kTmemS = 256;  // S double buffer: 2 x 64 columns
+constexpr uint32_t kTmemS = 256;  // S double buffer: 2 x 64 columns (P overwrites the first 32)
+constexpr uint32_t kTmemQ = 384;  // Q, cKV slabs 0-3: 4 x 32 columns of bf16 pairs
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);   // A, B K-major
@@ -83,22 +87,30 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);  // B (cKV tile) M
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t FULL = 0xffffffffu;
 
-// Shared-memory layout for a given number of stored query rows (Mv, multiple of 8).
+// Shared-memory layout of CTA `rank` for a given number of stored query rows (Mv, multiple
+// of 8).  The score exchange buffer sits at the same offset in both CTAs (the peer addresses
+// it through its own layout); CTA 1 adds the q_rope slab of Q; the rest is KV stages of
+// `nslab` 64-column slabs.
 struct Layout {
-  uint32_t q, p, x, kv, total;
+  uint32_t x, qr, kv, stage, total;
   int stages;
 };
-__host__ __device__ inline Layout make_layout(int Mv) {
+__host__ __device__ inline Layout make_layout(int Mv, int rank) {
   Layout L;
-  L.q = kFixedBytes;                              // 5 slabs of Mv rows x 128 B
-  L.p = L.q + 5u * (uint32_t)Mv * 128u;            // Mv rows x 128 B
-  L.x = L.p + (uint32_t)Mv * 128u;                 // 16 float4 x Mv rows
-  L.kv = (L.x + (uint32_t)Mv * 256u + 1023u) & ~1023u;
+  L.x = kFixedBytes;                                // 16 float4 x Mv rows
+  L.qr = L.x + (uint32_t)Mv * 256u;                 // CTA 1: Mv rows x 128 B
+  const uint32_t end = L.qr + (rank == 1 ? (uint32_t)Mv * 128u : 0u);
+  L.kv = (end + 1023u) & ~1023u;
+  L.stage = (rank == 1 ? 5u : 4u) * kSlabKV;
   const uint32_t avail = kSmemLimit - 1024u - L.kv;  // 1024: base alignment slack
-  int st = (int)(avail / kStage);
+  int st = (int)(avail / L.stage);
   L.stages = st > kMaxStages ? kMaxStages : st;
-  L.total = L.kv + (uint32_t)L.stages * kStage + 1024u;
+  L.total = L.kv + (uint32_t)L.stages * L.stage + 1024u;
   return L;
+}
+__host__ __device__ inline uint32_t launch_smem(int Mv) {
+  const uint32_t t0 = make_layout(Mv, 0).total, t1 = make_layout(Mv, 1).total;
+  return t0 > t1 ? t0 : t1;
 }
 
 // Warp-uniform bounded wait: every lane polls (and so acquires) the barrier, and the
@@ -131,9 +143,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nslab = rank == 0 ? 4 : 5;
   const int col0 = (int)rank * 256;
   const int Mv = a.Mv;
-  const Layout L = make_layout(Mv);
+  const Layout L = make_layout(Mv, (int)rank);
   const int NS = L.stages;
-  const uint32_t slabQ = (uint32_t)Mv * 128u;
 
   // ---- work unit: request b, query tile, KV split --------------------------------------
   const int b = blockIdx.y;
@@ -175,10 +186,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(BAR_S_FULL + s), 1);
-      mbar_init(bar(BAR_S_EMPTY + s), kSoftmaxWarps);
+      mbar_init(bar(BAR_PV_DONE + s), 1);
     }
     mbar_init(bar(BAR_P_FULL), kSoftmaxWarps);
-    mbar_init(bar(BAR_PV_DONE), 1);
+    mbar_init(bar(BAR_Q_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_X_FULL), 1);
     mbar_init(bar(BAR_X_EMPTY), kSoftmaxWarps);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -203,12 +214,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int pw = warp - kSoftmaxWarps;
     const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
     const int rsub = tp >> 3;   // row within a group of kLoaderThreads / 8
-    const __nv_bfloat16* ql = static_cast<const __nv_bfloat16*>(a.q_lat);
     const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
     const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
 
-    // Q columns of this CTA: Mv rows (rows past the tile's valid rows are zero filled).
-    if (ntiles > 0) {
+    // CTA 1's q_rope slab: Mv rows (rows past the tile's valid rows are zero filled); it
+    // lands with the first KV tile (same cp.async group).
+    if (ntiles > 0 && rank == 1) {
       for (int m = rsub; m < Mv; m += kLoaderThreads / 8) {
         const bool valid = m < rows_valid;
         int64_t row = 0;
@@ -216,14 +227,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int qi = q0 + m / a.H, h = m % a.H;
           row = ((int64_t)b * a.n_q + qi) * a.H + h;
         }
-        const uint32_t dst = sb + L.q + sw128_offset(m, chk);
-        for (int slab = 0; slab < nslab; ++slab) {
-          const void* src = a.q_lat;
-          if (valid)
-            src = (slab < 4) ? (const void*)(ql + row * kDLat + col0 + slab * 64 + chk * 8)
-                             : (const void*)(qr + row * kDRope + chk * 8);
-          cp_async_16(dst + slab * slabQ, src, valid ? 16u : 0u);
-        }
+        const void* src = valid ? (const void*)(qr + row * kDRope + chk * 8) : a.q_rope;
+        cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
       }
     }
 
@@ -313,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
       __syncwarp();
       if (rank == 1) {
-        uint8_t* kr = smem + L.kv + (uint32_t)sp * kStage + 4 * kSlabKV;
+        uint8_t* kr = smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV;
         const int dA = map_delta[sp * kBN + lane], dB = map_delta[sp * kBN + lane + 32];
         const int pA = __shfl_up_sync(FULL, dA, 1), pBu = __shfl_up_sync(FULL, dB, 1);
         const int d31 = __shfl_sync(FULL, dA, 31);
@@ -393,7 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
         }
         if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
-        const uint32_t stage = sb + L.kv + (uint32_t)s * kStage;
+        const uint32_t stage = sb + L.kv + (uint32_t)s * L.stage;
 #pragma unroll 2
         for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
           const int row = rr + rsub;
@@ -427,39 +432,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int ns = 0, np = 0;            // next Q.K^T tile, next P.V tile
       int ss = 0, sp = 0;            // their KV stages
       uint32_t phs = 0;              // kv_full parity of stage ss
-      bool ok = true;
+      bool ok = mbar_wait(bar(BAR_Q_FULL), 0, abort_flag);
+      tc_fence_after();
       uint64_t t_idle = 0;
       int spins = 0;
-      while (np < ntiles) {
+      while (ok && np < ntiles) {
         bool progressed = false;
-        // P.V first: the softmax waits for it before writing the next P
+        // P.V first: it frees the KV stage and the score buffer
         if (np < ns && mbar_test_wait(bar(BAR_P_FULL), np & 1)) {
           tc_fence_after();
-          const uint32_t stage = sb + L.kv + (uint32_t)sp * kStage;
+          const uint32_t stage = sb + L.kv + (uint32_t)sp * L.stage;
+          const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sb + L.p + kk * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
-            umma_bf16(tO, ad, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tO, tP + 8u * kk, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(BAR_KV_EMPTY + sp));
-          umma_commit(bar(BAR_PV_DONE));
+          umma_commit(bar(BAR_PV_DONE + (np & 1)));
           ++np;
           if (++sp == NS) sp = 0;
           progressed = true;
         }
+        // Q.K^T of tile ns overwrites score buffer ns&1, which holds P of tile ns-2 until
+        // that tile's P.V has completed
         if (ns < ntiles && mbar_test_wait(bar(BAR_KV_FULL + ss), phs) &&
-            (ns < 2 || mbar_test_wait(bar(BAR_S_EMPTY + (ns & 1)), ((ns >> 1) - 1) & 1))) {
+            (ns < 2 || (np > ns - 2 &&
+                        mbar_test_wait(bar(BAR_PV_DONE + (ns & 1)), ((ns >> 1) - 1) & 1)))) {
           tc_fence_after();
           fence_proxy_async_smem();
-          const uint32_t stage = sb + L.kv + (uint32_t)ss * kStage;
+          const uint32_t stage = sb + L.kv + (uint32_t)ss * L.stage;
           const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
-          for (int slab = 0; slab < nslab; ++slab) {
+          for (int slab = 0; slab < 4; ++slab) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(sb + L.q + slab * slabQ + kk * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
-              umma_bf16(tS, ad, bd, kIdescS, (slab | kk) ? 1u : 0u);
+              umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, bd, kIdescS, (slab | kk) ? 1u : 0u);
+            }
+          }
+          if (nslab == 5) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(stage + 4 * kSlabKV + kk * 32, 16, 1024);
+              umma_bf16(tS, ad, bd, kIdescS, 1u);
             }
           }
           umma_commit(bar(BAR_S_FULL + (ns & 1)));
@@ -509,6 +525,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rXempty = mapa_shared(bar(BAR_X_EMPTY), peer);
     const float4* X = reinterpret_cast<const float4*>(smem + L.x);
     bool ok = true;
+    // Q, this CTA's cKV columns, into TMEM: thread m stores row m's 256 columns as bf16 pairs
+    // (rows past the valid ones are zero; warps holding no stored rows leave their lanes)
+    if (ntiles > 0 && warp_live) {
+      const bool valid = m < rows_valid;
+      int64_t row = 0;
+      if (valid) row = ((int64_t)b * a.n_q + (q0 + m / a.H)) * a.H + (m % a.H);
+      const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_lat) +
+                                                         row * kDLat + col0);
+#pragma unroll 1
+      for (int slab = 0; slab < 4; ++slab) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = valid ? __ldg(qsrc + slab * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + kTmemQ + 32u * slab + lane_base, r);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(BAR_Q_FULL));
     for (int j = 0; j < ntiles && ok; ++j) {
       const int s = j & 1;
       const int T = (kb + j) * kBN;
@@ -526,9 +568,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY + s));
 
       // exchange partial scores with the peer (each side owns part of the contraction)
       if (j >= 1 && !(ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag))) break;
@@ -578,10 +617,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         want = (m < rows_valid) && (mx > m_run + 8.f);
       }
       const float corr = want ? fast_exp2(m_run - mx) : 1.f;
-      bool pv_waited = false;
       if (j > 0 && __any_sync(FULL, want)) {
-        if (!(ok = warp_wait(bar(BAR_PV_DONE), (j - 1) & 1, abort_flag))) break;
-        pv_waited = true;
+        if (!(ok = warp_wait(bar(BAR_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -614,22 +651,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
         l_run += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-      }
-      if (j > 0 && !pv_waited &&
-          !(ok = warp_wait(bar(BAR_PV_DONE), (j - 1) & 1, abort_flag)))
-        break;
-      if (row_live) {
+      } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(m, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int i = 0; i < kBN / 2; ++i) pk[i] = 0u;
       }
-      fence_proxy_async_smem();
+      // P over the first 32 columns of the score buffer just read (bf16 pairs)
+      if (warp_live) {
+        tmem_st32(tmem + kTmemS + 64u * (uint32_t)s + lane_base, pk);
+        tmem_st_wait();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
     }
-    if (ok && ntiles > 0) ok = warp_wait(bar(BAR_PV_DONE), (ntiles - 1) & 1, abort_flag);
+    if (ok && ntiles > 0)
+      ok = warp_wait(bar(BAR_PV_DONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, abort_flag);
     if (!ok) {
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
@@ -770,16 +806,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t attn_smem_bytes(int Mv) { return make_layout(Mv).total; }
+size_t attn_smem_bytes(int Mv) { return launch_smem(Mv); }
 
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream) {
-  const Layout L = make_layout(a.Mv);
-  if (L.stages < 2) return cudaErrorInvalidConfiguration;
+  if (make_layout(a.Mv, 0).stages < 2 || make_layout(a.Mv, 1).stages < 2)
+    return cudaErrorInvalidConfiguration;
+  const uint32_t smem = launch_smem(a.Mv);
   cudaError_t e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)L.total);
+                                       (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.n_qtiles * a.S, a.B);
-  mla_attn_kernel<<<grid, kThreads, L.total, stream>>>(a);
+  mla_attn_kernel<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
