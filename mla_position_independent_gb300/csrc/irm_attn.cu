@@ -34,8 +34,8 @@
 #include <climits>
 #include <cmath>
 
-#include "irm_common.cuh"
 #include "irm_internal.h"
+#include "irm_pipeline.cuh"
 
 namespace irm {
 namespace {
@@ -68,8 +68,8 @@ enum : int {
   BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
   BAR_S_FULL = BAR_MAP + kMaxStages,        // [2] UMMA commit after Q.K^T into S buffer
   BAR_PV_DONE = BAR_S_FULL + 2,             // [2] UMMA commit after P.V of the P in S buffer
-  BAR_P_FULL = BAR_PV_DONE + 2,             // softmax wrote P (and rescaled O) (count 4)
-  BAR_Q_FULL = BAR_P_FULL + 1,              // softmax warps stored Q in TMEM (count 4)
+  BAR_P_FULL = BAR_PV_DONE + 2,             // [2] softmax wrote P over S buffer (and rescaled O) (count 4)
+  BAR_Q_FULL = BAR_P_FULL + 2,              // softmax warps stored Q in TMEM (count 4)
   BAR_X_FULL = BAR_Q_FULL + 1,              // peer's partial scores landed (1 arrive + tx)
   BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 4 softmax warps consumed our scores (remote)
   BAR_DRAIN = BAR_X_EMPTY + 1,              // all UMMAs done before TMEM is released
@@ -85,7 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);   // A, B K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);  // B (cKV tile) MN-major
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t FULL = 0xffffffffu;
+constexpr uint32_t FULL = kFullMask;
 
 // Shared-memory layout of CTA `rank` for a given number of stored query rows (Mv, multiple
 // of 8).  The score exchange buffer sits at the same offset in both CTAs (the peer addresses
@@ -111,24 +111,6 @@ __host__ __device__ inline Layout make_layout(int Mv, int rank) {
 __host__ __device__ inline uint32_t launch_smem(int Mv) {
   const uint32_t t0 = make_layout(Mv, 0).total, t1 = make_layout(Mv, 1).total;
   return t0 > t1 ? t0 : t1;
-}
-
-// Warp-uniform bounded wait: every lane polls (and so acquires) the barrier, and the
-// verdict is agreed with __all_sync so no lane leaves a loop its warp-mates stay in.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, abort_flag);
-  return __all_sync(FULL, ok);
-}
-__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  const volatile int* abort_flag) {
-  const bool ok = mbar_wait_cluster(bar, parity, abort_flag);
-  return __all_sync(FULL, ok);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -187,8 +169,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(BAR_S_FULL + s), 1);
       mbar_init(bar(BAR_PV_DONE + s), 1);
+      mbar_init(bar(BAR_P_FULL + s), kSoftmaxWarps);
     }
-    mbar_init(bar(BAR_P_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_Q_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_X_FULL), 1);
     mbar_init(bar(BAR_X_EMPTY), kSoftmaxWarps);
@@ -234,129 +216,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // Loader warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
     // per-tile row maps: source row (-1 = outside the context, zero filled) and delta.
-    int win = c_begin;
-    int w_start = INT_MAX, w_end = INT_MAX, w_delta = 0;
-    long long w_off = 0;
-    auto load_window = [&]() {
-      const int c = win + lane;
-      if (c < c_end) {
-        const irm_chunk ch = a.chunks[c];
-        w_start = ch.p_tgt;
-        w_end = ch.p_tgt + ch.len;
-        w_off = ch.pool_offset;
-        w_delta = ch.reused ? ch.p_tgt - ch.p_src : 0;
-      } else {
-        w_start = INT_MAX;
-        w_end = INT_MAX;
-        w_off = 0;
-        w_delta = 0;
-      }
-    };
-    if (pw == 0 && ntiles > 0) {
-      const int T0 = kb * kBN;  // find the last chunk with p_tgt <= T0
-      int lo = c_begin, hi = c_end;
-      while (hi - lo > 32) {
-        const int step = (hi - lo + 31) / 32;
-        const int c = lo + lane * step;
-        const bool le = (c < hi) && (a.chunks[c].p_tgt <= T0);
-        const unsigned msk = __ballot_sync(FULL, le);
-        const int k = msk ? 31 - __clz((int)msk) : 0;
-        lo = lo + k * step;
-        hi = min(hi, lo + step);
-      }
-      win = lo;
-      load_window();
-    }
-    auto build_map = [&](int T, int s) {
-      // rows T+lane and T+lane+32; the few window chunks overlapping the tile are found with
-      // one ballot and broadcast in turn (no per-row search)
-      const int t0 = T + lane, t1 = T + lane + 32;
-      const int t_end = min(T + kBN, ctx);
-      int src0 = -1, src1 = -1, d0 = 0, d1 = 0;
-      for (int guard = 0; guard < kBN + 1 && T < t_end; ++guard) {
-        const int nvalid = min(32, c_end - win);
-        if (nvalid <= 0) {  // the device table does not cover the context
-          if (lane == 0) set_status(a.status, kDevErrBounds);
-          break;
-        }
-        unsigned ov = __ballot_sync(FULL, lane < nvalid && w_start < t_end && w_end > T);
-        while (ov != 0u) {
-          const int k = __ffs(ov) - 1;
-          ov &= ov - 1u;
-          const int st = __shfl_sync(FULL, w_start, k), en = __shfl_sync(FULL, w_end, k);
-          const long long of = __shfl_sync(FULL, w_off, k);
-          const int dd = __shfl_sync(FULL, w_delta, k);
-          if (t0 >= st && t0 < en && t0 < t_end) {
-            const long long r = of + (t0 - st);
-            if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src0 = (int)r;
-            d0 = dd;
-          }
-          if (t1 >= st && t1 < en && t1 < t_end) {
-            const long long r = of + (t1 - st);
-            if (r < 0 || r >= a.n_rows) set_status(a.status, kDevErrBounds); else src1 = (int)r;
-            d1 = dd;
-          }
-        }
-        const int last_end = __shfl_sync(FULL, w_end, nvalid - 1);
-        if (last_end >= t_end) break;  // the window covers the rest of the tile
-        win += nvalid;                 // slide to the chunk holding row last_end
-        load_window();
-      }
-      map_src[s * kBN + lane] = src0;
-      map_src[s * kBN + lane + 32] = src1;
-      map_delta[s * kBN + lane] = d0;
-      map_delta[s * kBN + lane + 32] = d1;
-    };
+    ChunkWindow cw;
+    cw.chunks = a.chunks;
+    cw.c_end = c_end;
+    cw.win = c_begin;
+    if (pw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
 
     // Publish a landed tile: rank 1 rotates k_r by R(delta) in shared memory (loader warp pw
     // owns rows 16pw..16pw+15), then every warp fences its writes for the async proxy and
-    // arrives on KV_FULL.  Rows form runs of equal delta (chunks): per run every lane
-    // computes the (cos, sin) of its two pairs once and the warp walks the run's rows two at a
-    // time, lane = (row parity h, pair-pair i) rotating pairs 2i, 2i+1 (k_r[2i], k_r[2i+1]
-    // with k_r[32+2i], k_r[33+2i]) through 32-bit shared-memory accesses.
+    // arrives on KV_FULL.
     auto publish = [&](int sp, uint32_t php) -> bool {
       if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
       __syncwarp();
-      if (rank == 1) {
-        uint8_t* kr = smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV;
-        const int dA = map_delta[sp * kBN + lane], dB = map_delta[sp * kBN + lane + 32];
-        const int pA = __shfl_up_sync(FULL, dA, 1), pBu = __shfl_up_sync(FULL, dB, 1);
-        const int d31 = __shfl_sync(FULL, dA, 31);
-        const int pB = lane == 0 ? d31 : pBu;
-        const unsigned mA = __ballot_sync(FULL, lane == 0 || dA != pA);
-        const unsigned mB = __ballot_sync(FULL, dB != pB);
-        const int lo = 16 * pw, hi = lo + 16;
-        // runs overlapping [lo, hi): keep starts inside, plus the run containing lo
-        uint64_t all = (uint64_t)mA | ((uint64_t)mB << 32);
-        uint64_t rem = all & (((hi == 64) ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull));
-        rem |= 1ull << lo;  // the run containing row lo starts (for this warp) at lo
-        const int h = lane >> 4, i = lane & 15;
-        const uint32_t woff = (uint32_t)(i & 3) * 4u, xc = (uint32_t)(i >> 2), yc = 4u + (uint32_t)(i >> 2);
-        while (rem != 0) {
-          const int r0 = __ffsll((long long)rem) - 1;
-          rem &= rem - 1;
-          const int r1 = rem != 0 ? __ffsll((long long)rem) - 1 : hi;
-          const int d = map_delta[sp * kBN + r0];
-          if (d == 0) continue;
-          float c0, s0, c1, s1;
-          rope_cos_sin(d, phaseF[2 * i], c0, s0);
-          rope_cos_sin(d, phaseF[2 * i + 1], c1, s1);
-#pragma unroll 4
-          for (int r = r0 + h; r < r1; r += 2) {
-            uint8_t* rowp = kr + r * 128;
-            uint32_t* px = reinterpret_cast<uint32_t*>(rowp + ((xc ^ (uint32_t)(r & 7)) << 4) + woff);
-            uint32_t* py = reinterpret_cast<uint32_t*>(rowp + ((yc ^ (uint32_t)(r & 7)) << 4) + woff);
-            const uint32_t xw = *px, yw = *py;
-            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw));
-            const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw));
-            const __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(xf.x, c0, -yf.x * s0), fmaf(xf.y, c1, -yf.y * s1));
-            const __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(xf.x, s0, yf.x * c0), fmaf(xf.y, s1, yf.y * c1));
-            *px = *reinterpret_cast<const uint32_t*>(&xo);
-            *py = *reinterpret_cast<const uint32_t*>(&yo);
-          }
-        }
-      }
-      // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads them
+      if (rank == 1)
+        rotate_krope_rows(smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV, map_delta + sp * kBN, phaseF, pw,
+                          lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + sp));
@@ -372,7 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the map slot is free once tile j-NS was published; build the map now, while stage
           // s may still be in use by the P.V of tile j-NS
           if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
-          build_map((kb + j) * kBN, s);
+          cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + s * kBN, map_delta + s * kBN, a.status, lane);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
         }
@@ -439,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && np < ntiles) {
         bool progressed = false;
         // P.V first: it frees the KV stage and the score buffer
-        if (np < ns && mbar_test_wait(bar(BAR_P_FULL), np & 1)) {
+        if (np < ns && mbar_test_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1)) {
           tc_fence_after();
           const uint32_t stage = sb + L.kv + (uint32_t)sp * L.stage;
           const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
@@ -662,7 +536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + s));
     }
     if (ok && ntiles > 0)
       ok = warp_wait(bar(BAR_PV_DONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, abort_flag);

@@ -152,8 +152,60 @@ size_t partial_bytes(int B, int n_qtiles, int S) {
 
 struct AttnPlan {
   int qpt, n_qtiles, S;
+  bool few_heads;  // decode with H in {16, 32}: the split-KV decode kernel
+  int C, G;        // its cluster size and clusters per request
   size_t ws_bytes;
 };
+
+// Largest number of co-resident clusters of the decode kernel per cluster size, cached per
+// device (the query needs the device; it is made once).
+int decode_clusters(int H, int C) {
+  static std::mutex mu;
+  static int cache[64][2][5];
+  static bool have[64][2][5];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return irm::decode_max_active_clusters(H, C);
+  const int hi = H == 16 ? 0 : 1, ci = C == 1 ? 0 : C == 2 ? 1 : C == 4 ? 2 : C == 8 ? 3 : 4;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev][hi][ci]) {
+    cache[dev][hi][ci] = irm::decode_max_active_clusters(H, C);
+    have[dev][hi][ci] = true;
+  }
+  return cache[dev][hi][ci];
+}
+
+// Split of a decode over the decode kernel's clusters: C CTAs per cluster (a power of two
+// up to 16), G clusters per request.  Minimises, in tile times, waves x (tiles per split +
+// pipeline fill) plus the merge of G cluster partials (a fixed cost and the slice each
+// last cluster CTA reads: G x H x 2 KiB / C).
+void choose_decode_split(int B, int64_t max_ctx, int H, int* C_out, int* G_out) {
+  const int64_t tiles = std::max<int64_t>(1, (max_ctx + kBN - 1) / kBN);
+  int bestC = 1, bestG = 1;
+  double best_cost = 1e30;
+  for (int C = 1; C <= irm::kMaxDecodeCluster; C *= 2) {
+    if (C > 1 && C > tiles) break;
+    const int n = decode_clusters(H, C);
+    if (n <= 0) continue;
+    for (int G = 1; G <= 64; ++G) {
+      const int64_t S = (int64_t)C * G;
+      if (S > tiles && G > 1) break;
+      const int64_t waves = ((int64_t)B * G + n - 1) / n;
+      const double cost = (double)waves * ((double)((tiles + S - 1) / S) + 2.0) +
+                          (G > 1 ? 0.5 + 0.01 * G * H / C : 0.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        bestC = C;
+        bestG = G;
+      }
+    }
+  }
+  *C_out = bestC;
+  *G_out = bestG;
+}
+
+size_t decode_gpart_bytes(int B, int G, int H) { return ((size_t)B * G * H * IRM_D_LAT * 4 + 255) / 256 * 256; }
+size_t decode_glse_bytes(int B, int G, int H) { return ((size_t)B * G * H * 4 + 255) / 256 * 256; }
+size_t decode_counter_bytes(int B, int C) { return ((size_t)B * C * 4 + 255) / 256 * 256; }
 
 irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p) {
   if (H < 1 || H > IRM_MAX_HEADS) return fail(IRM_ERR_UNSUPPORTED, "H=%d outside [1, %d]", H, IRM_MAX_HEADS);
@@ -164,6 +216,15 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
   p->n_qtiles = (n_q + p->qpt - 1) / p->qpt;
   if (p->n_qtiles > 32767) return fail(IRM_ERR_UNSUPPORTED, "too many query tiles (%d)", p->n_qtiles);
   if (B > 65535) return fail(IRM_ERR_UNSUPPORTED, "B=%d exceeds 65535", B);
+  p->few_heads = decode && n_q == 1 && irm::decode_supported(H);
+  if (p->few_heads) {
+    p->S = 1;
+    choose_decode_split(B, info.max_ctx, H, &p->C, &p->G);
+    p->ws_bytes = IRM_WORKSPACE_HEADER;
+    if (p->G > 1)
+      p->ws_bytes += decode_gpart_bytes(B, p->G, H) + decode_glse_bytes(B, p->G, H) + decode_counter_bytes(B, p->C);
+    return IRM_OK;
+  }
   p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms()) : 1;
   p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
   return IRM_OK;
@@ -189,6 +250,34 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.ws_bytes)
     return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
                 pl.ws_bytes, workspace_bytes);
+  if (pl.few_heads) {
+    irm::DecodeArgs d{};
+    d.q_lat = q_lat;
+    d.q_rope = q_rope;
+    d.kv = kv_rows;
+    d.chunks = chunks_dev;
+    d.indptr = indptr_dev;
+    d.n_rows = n_rows;
+    d.n_chunks = info.n_chunks;
+    d.B = B;
+    d.H = H;
+    d.C = pl.C;
+    d.G = pl.G;
+    if (pl.G > 1) {
+      uint8_t* ws = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
+      d.gpart = reinterpret_cast<float*>(ws);
+      d.glse = reinterpret_cast<float*>(ws + decode_gpart_bytes(B, pl.G, H));
+      d.counters = reinterpret_cast<int*>(ws + decode_gpart_bytes(B, pl.G, H) + decode_glse_bytes(B, pl.G, H));
+    }
+    d.scale_log2 = softmax_scale * 1.4426950408889634f;
+    d.out = out;
+    d.lse = lse;
+    d.status = static_cast<int*>(workspace);
+    std::memcpy(d.phase.F, rope_phase().F, sizeof d.phase.F);
+    cudaError_t e = irm::launch_mla_decode(d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla decode launch");
+    return IRM_OK;
+  }
   irm::AttnArgs a{};
   a.q_lat = q_lat;
   a.q_rope = q_rope;
@@ -400,7 +489,11 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   // The array keeps the last call's contents: clear the status word and the split-KV
   // completion counters, which must start at zero.
   cudaError_t e = cudaMemsetAsync(ws, 0, IRM_WORKSPACE_HEADER, stream);
-  if (e == cudaSuccess && pl.S > 1) {
+  if (e == cudaSuccess && pl.few_heads && pl.G > 1) {
+    const size_t off = IRM_WORKSPACE_HEADER + decode_gpart_bytes(B, pl.G, H) + decode_glse_bytes(B, pl.G, H);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + off, 0, decode_counter_bytes(B, pl.C), stream);
+  }
+  if (e == cudaSuccess && !pl.few_heads && pl.S > 1) {
     const int units = pl.n_qtiles * pl.S;
     const size_t off = IRM_WORKSPACE_HEADER + partial_o_bytes(B, units) + partial_lse_bytes(B, units);
     e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + off, 0, counter_bytes(B, pl.n_qtiles), stream);

@@ -58,10 +58,39 @@ struct AttnArgs {
   } phase;
 };
 
+// Split-KV decode for a few heads (one query token per request): one CTA per (request,
+// split), the C splits of a request in one cluster that merges them in shared memory.
+constexpr int kMaxDecodeCluster = 16;
+struct DecodeArgs {
+  const void* q_lat;    // bf16 [B, H, 512]
+  const void* q_rope;   // bf16 [B, H, 64]
+  const void* kv;       // bf16 [n_rows, 576]
+  const irm_chunk* chunks;
+  const int32_t* indptr;
+  int64_t n_rows;
+  int64_t n_chunks;
+  int B, H;
+  int C;          // CTAs per cluster (power of two, <= kMaxDecodeCluster)
+  int G;          // clusters per request; the request's KV splits are C * G
+  float scale_log2;
+  void* out;      // bf16 [B, H, 512]
+  float* lse;     // fp32 [B, H] or nullptr
+  float* gpart;   // G > 1: fp32 [B, G, H, 512] normalised partial O of each cluster
+  float* glse;    // G > 1: fp32 [B, G, H] its log2-sum-exp (scaled scores, log2 units)
+  int* counters;  // G > 1: int [B, C] finished clusters per output slice, zero between calls
+  int* status;
+  struct {
+    uint64_t F[32];
+  } phase;
+};
+
 cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int B,
                              int64_t* row_start, cudaStream_t stream);
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
 size_t attn_smem_bytes(int Mv);
+bool decode_supported(int H);
+int decode_max_active_clusters(int H, int C);  // 0 when C does not fit
+cudaError_t launch_mla_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace irm

@@ -1,0 +1,221 @@
+// Pieces of the KV gather pipeline shared by the attention kernels: the chunk-table window
+// that turns target positions into source rows and deltas, and the in-shared-memory
+// rotation of a staged k_r slab by R(delta) ("Irminsul论文详解" §4 δ-rotation; technical
+// summary §2.2).
+#pragma once
+#include <climits>
+#include <cstdint>
+
+#include "irm_common.cuh"
+
+namespace irm {
+
+constexpr uint32_t kFullMask = 0xffffffffu;
+
+// A warp's window of 32 consecutive chunk records of one request (one record per lane).
+struct ChunkWindow {
+  const irm_chunk* chunks;
+  int c_end;  // one past the request's last chunk
+  int win;    // first chunk of the window
+  int start, end, delta;
+  long long off;
+
+  __device__ __forceinline__ void load(int lane) {
+    const int c = win + lane;
+    if (c < c_end) {
+      const irm_chunk ch = chunks[c];
+      start = ch.p_tgt;
+      end = ch.p_tgt + ch.len;
+      off = ch.pool_offset;
+      delta = ch.reused ? ch.p_tgt - ch.p_src : 0;
+    } else {
+      start = end = INT_MAX;
+      off = 0;
+      delta = 0;
+    }
+  }
+
+  // Position the window at the last chunk with p_tgt <= T0 (chunks tile the context in
+  // target order), narrowing [c_begin, c_end) 32-fold per step with one ballot.
+  __device__ __forceinline__ void seek(int c_begin, int T0, int lane) {
+    int lo = c_begin, hi = c_end;
+    while (hi - lo > 32) {
+      const int step = (hi - lo + 31) / 32;
+      const int c = lo + lane * step;
+      const bool le = (c < hi) && (chunks[c].p_tgt <= T0);
+      const unsigned msk = __ballot_sync(kFullMask, le);
+      const int k = msk ? 31 - __clz((int)msk) : 0;
+      lo = lo + k * step;
+      hi = min(hi, lo + step);
+    }
+    win = lo;
+    load(lane);
+  }
+
+  // Row map of the 64-row tile starting at target position T: src[r] = source row of
+  // position T + r (-1 past the context: zero filled), dl[r] = its delta.  The few window
+  // chunks overlapping the tile are found with one ballot and broadcast in turn; the window
+  // slides forward when the tile runs past it.  A table that does not cover the context or
+  // points outside the row store sets the bounds bit of `status`.
+  __device__ __forceinline__ void build_map(int T, int ctx, int64_t n_rows, int32_t* src, int32_t* dl,
+                                            int* status, int lane) {
+    const int t0 = T + lane, t1 = T + lane + 32;
+    const int t_end = min(T + 64, ctx);
+    int src0 = -1, src1 = -1, d0 = 0, d1 = 0;
+    for (int guard = 0; guard < 65 && T < t_end; ++guard) {
+      const int nvalid = min(32, c_end - win);
+      if (nvalid <= 0) {
+        if (lane == 0) set_status(status, kDevErrBounds);
+        break;
+      }
+      unsigned ov = __ballot_sync(kFullMask, lane < nvalid && start < t_end && end > T);
+      while (ov != 0u) {
+        const int k = __ffs(ov) - 1;
+        ov &= ov - 1u;
+        const int st = __shfl_sync(kFullMask, start, k), en = __shfl_sync(kFullMask, end, k);
+        const long long of = __shfl_sync(kFullMask, off, k);
+        const int dd = __shfl_sync(kFullMask, delta, k);
+        if (t0 >= st && t0 < en && t0 < t_end) {
+          const long long r = of + (t0 - st);
+          if (r < 0 || r >= n_rows) set_status(status, kDevErrBounds); else src0 = (int)r;
+          d0 = dd;
+        }
+        if (t1 >= st && t1 < en && t1 < t_end) {
+          const long long r = of + (t1 - st);
+          if (r < 0 || r >= n_rows) set_status(status, kDevErrBounds); else src1 = (int)r;
+          d1 = dd;
+        }
+      }
+      const int last_end = __shfl_sync(kFullMask, end, nvalid - 1);
+      if (last_end >= t_end) break;
+      win += nvalid;
+      load(lane);
+    }
+    src[lane] = src0;
+    src[lane + 32] = src1;
+    dl[lane] = d0;
+    dl[lane + 32] = d1;
+  }
+};
+
+// Rotate rows [16 pw, 16 pw + 16) of a staged k_r slab (64 rows x 128 bytes, 128-byte
+// swizzle) by R(delta[row]), NeoX half split: pair j couples k_r[j] and k_r[32 + j].
+// Rows form runs of equal delta (chunks): per run every lane computes the (cos, sin) of its
+// two pairs once and the warp walks the run two rows at a time, lane = (row parity h,
+// pair-pair i) rotating pairs 2i, 2i+1 through 32-bit shared-memory accesses.
+__device__ __forceinline__ void rotate_krope_rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
+                                                  int pw, int lane) {
+  const int dA = delta[lane], dB = delta[lane + 32];
+  const int pA = __shfl_up_sync(kFullMask, dA, 1), pBu = __shfl_up_sync(kFullMask, dB, 1);
+  const int d31 = __shfl_sync(kFullMask, dA, 31);
+  const int pB = lane == 0 ? d31 : pBu;
+  const unsigned mA = __ballot_sync(kFullMask, lane == 0 || dA != pA);
+  const unsigned mB = __ballot_sync(kFullMask, dB != pB);
+  const int lo = 16 * pw, hi = lo + 16;
+  // runs overlapping [lo, hi): keep starts inside, plus the run containing lo
+  const uint64_t all = (uint64_t)mA | ((uint64_t)mB << 32);
+  uint64_t rem = all & (((hi == 64) ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull));
+  rem |= 1ull << lo;
+  const int h = lane >> 4, i = lane & 15;
+  const uint32_t woff = (uint32_t)(i & 3) * 4u, xc = (uint32_t)(i >> 2), yc = 4u + (uint32_t)(i >> 2);
+  while (rem != 0) {
+    const int r0 = __ffsll((long long)rem) - 1;
+    rem &= rem - 1;
+    const int r1 = rem != 0 ? __ffsll((long long)rem) - 1 : hi;
+    const int d = delta[r0];
+    if (d == 0) continue;
+    float c0, s0, c1, s1;
+    rope_cos_sin(d, phaseF[2 * i], c0, s0);
+    rope_cos_sin(d, phaseF[2 * i + 1], c1, s1);
+#pragma unroll 4
+    for (int r = r0 + h; r < r1; r += 2) {
+      uint8_t* rowp = kr + r * 128;
+      uint32_t* px = reinterpret_cast<uint32_t*>(rowp + ((xc ^ (uint32_t)(r & 7)) << 4) + woff);
+      uint32_t* py = reinterpret_cast<uint32_t*>(rowp + ((yc ^ (uint32_t)(r & 7)) << 4) + woff);
+      const uint32_t xw = *px, yw = *py;
+      const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw));
+      const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw));
+      const __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(xf.x, c0, -yf.x * s0), fmaf(xf.y, c1, -yf.y * s1));
+      const __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(xf.x, s0, yf.x * c0), fmaf(xf.y, s1, yf.y * c1));
+      *px = *reinterpret_cast<const uint32_t*>(&xo);
+      *py = *reinterpret_cast<const uint32_t*>(&yo);
+    }
+  }
+}
+
+// Rotate a whole staged k_r slab (64 rows x 128 bytes, 128-byte swizzle) by R(delta[row])
+// with one warp: lane = (row r8 of 8, 16-byte chunk v of 4) takes k_r[8v .. 8v+7] and its NeoX
+// partners k_r[32+8v .. 32+8v+7] of rows r8, r8 + 8, ...; the (cos, sin) of its 8 frequencies
+// are recomputed only when the row's delta differs from the lane's previous row (chunks are
+// runs of equal delta).
+__device__ __forceinline__ void rotate_krope_slab(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
+                                                  int lane) {
+  const int r8 = lane >> 2, v = lane & 3;
+  int dprev = 0;
+  float cs_c[8], cs_s[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cs_c[e] = 1.f;
+    cs_s[e] = 0.f;
+  }
+#pragma unroll 2
+  for (int it = 0; it < 8; ++it) {
+    const int r = 8 * it + r8;
+    const int d = delta[r];
+    if (d == 0) continue;
+    if (d != dprev) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[8 * v + e], cs_c[e], cs_s[e]);
+      dprev = d;
+    }
+    uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)v ^ (uint32_t)(r & 7)) << 4));
+    uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(4 + v) ^ (uint32_t)(r & 7)) << 4));
+    uint4 x = *px, y = *py;
+    rotate_pairs8(x, y, cs_c, cs_s);
+    *px = x;
+    *py = y;
+  }
+}
+
+// Rotate 8 rows [r0, r0 + 8) of a staged k_r slab by R(delta[row]) with one warp: lane =
+// (row of 8, 16-byte chunk v of 4) takes k_r[8v .. 8v+7] and its NeoX partners
+// k_r[32+8v .. 32+8v+7].  dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls
+// (recomputed only when the row's delta changes; chunks are runs of equal delta).
+__device__ __forceinline__ void rotate_krope_8rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
+                                                   int r0, int lane, int& dprev, float (&cs_c)[8],
+                                                   float (&cs_s)[8]) {
+  const int r = r0 + (lane >> 2), v = lane & 3;
+  const int d = delta[r];
+  if (d == 0) return;
+  if (d != dprev) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[8 * v + e], cs_c[e], cs_s[e]);
+    dprev = d;
+  }
+  uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)v ^ (uint32_t)(r & 7)) << 4));
+  uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(4 + v) ^ (uint32_t)(r & 7)) << 4));
+  uint4 x = *px, y = *py;
+  rotate_pairs8(x, y, cs_c, cs_s);
+  *px = x;
+  *py = y;
+}
+
+// Warp-uniform bounded waits: every lane polls (and so acquires) the barrier, and the
+// verdict is agreed with __all_sync so no lane leaves a loop its warp-mates stay in.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(kFullMask, ok);
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort_flag) {
+  const bool ok = mbar_wait_cluster(bar, parity, abort_flag);
+  return __all_sync(kFullMask, ok);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace irm

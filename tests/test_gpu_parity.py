@@ -181,7 +181,7 @@ def test_prefill_chunked_sampled(oracle_mod):
     _check_attn(case, oracle_mod, prefill=True, select=sel)
 
 
-@pytest.mark.parametrize("H", [16, 64, 128])
+@pytest.mark.parametrize("H", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("lens", [[40], [32, 1, 31, 33, 63, 64, 65], [32, 17], [32, 200, 128, 3]])
 def test_attention_edge_cases(oracle_mod, H, lens):
     rng = np.random.default_rng(H + len(lens))
@@ -202,6 +202,39 @@ def test_attention_edge_cases(oracle_mod, H, lens):
         _check_attn(case, oracle_mod, prefill=True, what=f"H={H} lens={lens} n_q={n_q}")
         if n_q == 1:
             _check_attn(case, oracle_mod, prefill=False, what=f"decode H={H} lens={lens}")
+
+
+def _ragged_decode_case(ctxs, H, seed):
+    """Requests of very different context lengths in one decode batch: with the splits of a
+    request sized for the longest one, short requests leave whole splits without tiles."""
+    rng = np.random.default_rng(seed)
+    n_rows = 12000
+    reqs = []
+    for ctx in ctxs:
+        p, req = 0, []
+        while p < ctx:
+            n = 32 if p == 0 else int(min(ctx - p, rng.integers(1, 300)))
+            n = min(n, ctx - p)
+            reused = p >= 32 and rng.random() < 0.75
+            d = int(rng.integers(-4096, 4097)) if reused else 0
+            req.append((int(rng.integers(0, n_rows - n)), n, p - d, reused))
+            p += n
+        reqs.append(req)
+    return to_device(synth.custom_case(reqs, n_rows=n_rows, n_q=1, H=H, q_std=1.0, seed=seed))
+
+
+@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("ctxs", [[9000], [33, 100, 4000, 64, 9000], [64] * 3 + [4097]])
+def test_decode_ragged_batch(oracle_mod, H, ctxs):
+    case = _ragged_decode_case(ctxs, H, seed=len(ctxs) + H)
+    _check_attn(case, oracle_mod, prefill=False, what=f"decode H={H} ctxs={ctxs}")
+
+
+def test_decode_many_requests(oracle_mod):
+    """More clusters than fit at once (several waves), sampled outputs."""
+    case = _ragged_decode_case([700 + 37 * b for b in range(40)], 16, seed=3)
+    sel = np.array([[b, 0, h] for b in (0, 17, 39) for h in (0, 5, 15)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel, what="decode 40 requests")
 
 
 def test_device_table_mismatch_is_recorded_not_faulted(oracle_mod):
