@@ -181,6 +181,7 @@ class Workload:
             self.q_lat = case.q_lat[:, 0].contiguous()
             self.q_rope = case.q_rope[:, 0].contiguous()
             B, H = self.q_lat.shape[:2]
+            self.H = H
             self.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
             self.lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
             self.ws = irm.new_workspace(irm.decode_workspace_size(self.table, H))
@@ -218,6 +219,13 @@ class Workload:
 
     def launches_per_step(self):
         return 1  # one fused kernel per call (the split-KV merge runs inside it)
+
+    def kernel_name(self):
+        if self.kind == "gather":
+            return "rotate_gather_kernel"
+        if self.kind == "decode" and self.H in (16, 32):
+            return "mla_decode_kernel"  # split-KV decode for a few heads
+        return "mla_attn_kernel"
 
     def check_status(self):
         self.irm.device_status(self.ws)
@@ -414,7 +422,7 @@ def main():
         unit = "GB/s"
     rf = roofline(wl, ms, pk)
     rf["peak_source"] = pk["src"]
-    rf["kernel"] = "rotate_gather_kernel" if wl.kind == "gather" else "mla_attn_kernel"
+    rf["kernel"] = wl.kernel_name()
     rf["traffic"] = traffic_for(args.workload)
     e2e = None
     if wl.kind == "decode":
@@ -451,6 +459,7 @@ def main():
             st = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_4M": 50}[name]
             t = statistics.mean(time_steps(wl, st, 3))
             r = roofline(wl, t, pk)
+            r["kernel"] = wl.kernel_name()
             ent = dict(ms_per_step=round(t, 4), roofline=r, steps=st)
             if wl.kind == "gather":
                 ent["rows_per_s"] = round(wl.ctx_total / (t * 1e-3), 1)

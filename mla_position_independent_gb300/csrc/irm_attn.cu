@@ -24,7 +24,8 @@
 //   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-7 gather KV rows with
 //     cp.async following the chunk table (completion tracked by an mbarrier, so they run
 //     ahead across stages) and, one tile behind, rotate k_r by R(delta) and publish the tile;
-//     8 allocates TMEM and issues the UMMAs in readiness order.
+//     8 allocates TMEM and issues Q.K^T, 9 issues P.V (one issuing thread per product: a
+//     thread issues UMMAs no faster than one per ~40 cycles).
 //   - Only the first Mv rows (valid query rows rounded up to 8) of the q_rope slab and the
 //     score exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
 //     whatever follows in shared memory (or TMEM lanes nobody wrote).  Those rows only
@@ -44,8 +45,9 @@ constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 64;   // KV rows per tile
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoaderWarps = 4;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 8
-constexpr int kThreads = (kMmaWarp + 1) * 32;            // 288
+constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 8: TMEM allocation, Q.K^T issue
+constexpr int kPvWarp = kMmaWarp + 1;                    // 9: P.V issue
+constexpr int kThreads = (kPvWarp + 1) * 32;             // 320
 constexpr int kLoaderThreads = kLoaderWarps * 32;
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
@@ -72,8 +74,8 @@ enum : int {
   BAR_Q_FULL = BAR_P_FULL + 2,              // softmax warps stored Q in TMEM (count 4)
   BAR_X_FULL = BAR_Q_FULL + 1,              // peer's partial scores landed (1 arrive + tx)
   BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 4 softmax warps consumed our scores (remote)
-  BAR_DRAIN = BAR_X_EMPTY + 1,              // all UMMAs done before TMEM is released
-  NUM_BARS = BAR_DRAIN + 1,
+  BAR_DRAIN = BAR_X_EMPTY + 1,              // [2] all UMMAs of the Q.K^T / P.V issuer done
+  NUM_BARS = BAR_DRAIN + 2,
 };
 static_assert(NUM_BARS <= 64, "barrier area");
 
@@ -175,6 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_X_FULL), 1);
     mbar_init(bar(BAR_X_EMPTY), kSoftmaxWarps);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -223,15 +226,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (pw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
 
     // Publish a landed tile: rank 1 rotates k_r by R(delta) in shared memory (loader warp pw
-    // owns rows 16pw..16pw+15), then every warp fences its writes for the async proxy and
-    // arrives on KV_FULL.
+    // owns rows 16pw..16pw+15), then every warp arrives on KV_FULL.  The Q.K^T issuer fences
+    // the bytes for the async proxy after acquiring KV_FULL (a loader's own fence would also
+    // wait for its copies of later tiles in flight).
+    int dprev = 0;
+    float cs_c[8], cs_s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      cs_c[e] = 1.f;
+      cs_s[e] = 0.f;
+    }
     auto publish = [&](int sp, uint32_t php) -> bool {
       if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
       __syncwarp();
-      if (rank == 1)
-        rotate_krope_rows(smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV, map_delta + sp * kBN, phaseF, pw,
-                          lane);
-      fence_proxy_async_smem();
+      if (rank == 1) {
+        uint8_t* kr = smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV;
+        rotate_krope_8rows(kr, map_delta + sp * kBN, phaseF, 16 * pw, lane, dprev, cs_c, cs_s);
+        rotate_krope_8rows(kr, map_delta + sp * kBN, phaseF, 16 * pw + 8, lane, dprev, cs_c, cs_s);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + sp));
       return true;
@@ -300,78 +312,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       set_status(a.status, kDevErrTimeout);
     }
   } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer (one thread), issues in readiness order ========
+    // ======================= Q.K^T issuer (one thread) ===================================
     if (lane == 0 && ntiles > 0) {
-      const uint32_t tO = tmem + kTmemO;
-      int ns = 0, np = 0;            // next Q.K^T tile, next P.V tile
-      int ss = 0, sp = 0;            // their KV stages
-      uint32_t phs = 0;              // kv_full parity of stage ss
       bool ok = mbar_wait(bar(BAR_Q_FULL), 0, abort_flag);
       tc_fence_after();
-      uint64_t t_idle = 0;
-      int spins = 0;
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        // P.V first: it frees the KV stage and the score buffer
-        if (np < ns && mbar_test_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1)) {
-          tc_fence_after();
-          const uint32_t stage = sb + L.kv + (uint32_t)sp * L.stage;
-          const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
+      int ss = 0;
+      uint32_t phs = 0;  // kv_full parity of stage ss
+      for (int ns = 0; ns < ntiles && ok; ++ns) {
+        if (!(ok = mbar_wait(bar(BAR_KV_FULL + ss), phs, abort_flag))) break;
+        // score buffer ns&1 holds P of tile ns-2 until that tile's P.V has completed
+        if (ns >= 2 && !(ok = mbar_wait(bar(BAR_PV_DONE + (ns & 1)), ((ns >> 1) - 1) & 1, abort_flag))) break;
+        // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads
+        tc_fence_after();
+        fence_proxy_async_smem();
+        const uint32_t stage = sb + L.kv + (uint32_t)ss * L.stage;
+        const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
+        for (int slab = 0; slab < 4; ++slab) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
-            umma_bf16_ts(tO, tP + 8u * kk, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
+            umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, bd, kIdescS, (slab | kk) ? 1u : 0u);
           }
-          umma_commit(bar(BAR_KV_EMPTY + sp));
-          umma_commit(bar(BAR_PV_DONE + (np & 1)));
-          ++np;
-          if (++sp == NS) sp = 0;
-          progressed = true;
         }
-        // Q.K^T of tile ns overwrites score buffer ns&1, which holds P of tile ns-2 until
-        // that tile's P.V has completed
-        if (ns < ntiles && mbar_test_wait(bar(BAR_KV_FULL + ss), phs) &&
-            (ns < 2 || (np > ns - 2 &&
-                        mbar_test_wait(bar(BAR_PV_DONE + (ns & 1)), ((ns >> 1) - 1) & 1)))) {
-          tc_fence_after();
-          fence_proxy_async_smem();
-          const uint32_t stage = sb + L.kv + (uint32_t)ss * L.stage;
-          const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
-          for (int slab = 0; slab < 4; ++slab) {
+        if (nslab == 5) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
-              umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, bd, kIdescS, (slab | kk) ? 1u : 0u);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(stage + 4 * kSlabKV + kk * 32, 16, 1024);
+            umma_bf16(tS, ad, bd, kIdescS, 1u);
           }
-          if (nslab == 5) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(stage + 4 * kSlabKV + kk * 32, 16, 1024);
-              umma_bf16(tS, ad, bd, kIdescS, 1u);
-            }
-          }
-          umma_commit(bar(BAR_S_FULL + (ns & 1)));
-          ++ns;
-          if (++ss == NS) {
-            ss = 0;
-            phs ^= 1u;
-          }
-          progressed = true;
         }
-        if (progressed) {
-          spins = 0;
-          t_idle = 0;
-        } else if (++spins >= 64) {
-          spins = 0;
-          __nanosleep(64);
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (*abort_flag || now - t_idle > kWaitLimitNs) {
-            ok = false;
-            break;
-          }
+        umma_commit(bar(BAR_S_FULL + (ns & 1)));
+        if (++ss == NS) {
+          ss = 0;
+          phs ^= 1u;
         }
       }
       if (!ok) {
@@ -380,6 +354,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       umma_commit(bar(BAR_DRAIN));
       if (!mbar_wait(bar(BAR_DRAIN), 0, nullptr)) set_status(a.status, kDevErrTimeout);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ======================= P.V issuer (one thread) =====================================
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t tO = tmem + kTmemO;
+      bool ok = true;
+      int sp = 0;
+      for (int np = 0; np < ntiles && ok; ++np) {
+        if (!(ok = mbar_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t stage = sb + L.kv + (uint32_t)sp * L.stage;
+        const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
+          umma_bf16_ts(tO, tP + 8u * kk, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(BAR_KV_EMPTY + sp));
+        umma_commit(bar(BAR_PV_DONE + (np & 1)));
+        if (++sp == NS) sp = 0;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, kDevErrTimeout);
+      }
+      umma_commit(bar(BAR_DRAIN + 1));
+      if (!mbar_wait(bar(BAR_DRAIN + 1), 0, nullptr)) set_status(a.status, kDevErrTimeout);
     }
     __syncwarp();
   } else {

@@ -98,85 +98,6 @@ struct ChunkWindow {
   }
 };
 
-// Rotate rows [16 pw, 16 pw + 16) of a staged k_r slab (64 rows x 128 bytes, 128-byte
-// swizzle) by R(delta[row]), NeoX half split: pair j couples k_r[j] and k_r[32 + j].
-// Rows form runs of equal delta (chunks): per run every lane computes the (cos, sin) of its
-// two pairs once and the warp walks the run two rows at a time, lane = (row parity h,
-// pair-pair i) rotating pairs 2i, 2i+1 through 32-bit shared-memory accesses.
-__device__ __forceinline__ void rotate_krope_rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
-                                                  int pw, int lane) {
-  const int dA = delta[lane], dB = delta[lane + 32];
-  const int pA = __shfl_up_sync(kFullMask, dA, 1), pBu = __shfl_up_sync(kFullMask, dB, 1);
-  const int d31 = __shfl_sync(kFullMask, dA, 31);
-  const int pB = lane == 0 ? d31 : pBu;
-  const unsigned mA = __ballot_sync(kFullMask, lane == 0 || dA != pA);
-  const unsigned mB = __ballot_sync(kFullMask, dB != pB);
-  const int lo = 16 * pw, hi = lo + 16;
-  // runs overlapping [lo, hi): keep starts inside, plus the run containing lo
-  const uint64_t all = (uint64_t)mA | ((uint64_t)mB << 32);
-  uint64_t rem = all & (((hi == 64) ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull));
-  rem |= 1ull << lo;
-  const int h = lane >> 4, i = lane & 15;
-  const uint32_t woff = (uint32_t)(i & 3) * 4u, xc = (uint32_t)(i >> 2), yc = 4u + (uint32_t)(i >> 2);
-  while (rem != 0) {
-    const int r0 = __ffsll((long long)rem) - 1;
-    rem &= rem - 1;
-    const int r1 = rem != 0 ? __ffsll((long long)rem) - 1 : hi;
-    const int d = delta[r0];
-    if (d == 0) continue;
-    float c0, s0, c1, s1;
-    rope_cos_sin(d, phaseF[2 * i], c0, s0);
-    rope_cos_sin(d, phaseF[2 * i + 1], c1, s1);
-#pragma unroll 4
-    for (int r = r0 + h; r < r1; r += 2) {
-      uint8_t* rowp = kr + r * 128;
-      uint32_t* px = reinterpret_cast<uint32_t*>(rowp + ((xc ^ (uint32_t)(r & 7)) << 4) + woff);
-      uint32_t* py = reinterpret_cast<uint32_t*>(rowp + ((yc ^ (uint32_t)(r & 7)) << 4) + woff);
-      const uint32_t xw = *px, yw = *py;
-      const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw));
-      const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw));
-      const __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(xf.x, c0, -yf.x * s0), fmaf(xf.y, c1, -yf.y * s1));
-      const __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(xf.x, s0, yf.x * c0), fmaf(xf.y, s1, yf.y * c1));
-      *px = *reinterpret_cast<const uint32_t*>(&xo);
-      *py = *reinterpret_cast<const uint32_t*>(&yo);
-    }
-  }
-}
-
-// Rotate a whole staged k_r slab (64 rows x 128 bytes, 128-byte swizzle) by R(delta[row])
-// with one warp: lane = (row r8 of 8, 16-byte chunk v of 4) takes k_r[8v .. 8v+7] and its NeoX
-// partners k_r[32+8v .. 32+8v+7] of rows r8, r8 + 8, ...; the (cos, sin) of its 8 frequencies
-// are recomputed only when the row's delta differs from the lane's previous row (chunks are
-// runs of equal delta).
-__device__ __forceinline__ void rotate_krope_slab(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
-                                                  int lane) {
-  const int r8 = lane >> 2, v = lane & 3;
-  int dprev = 0;
-  float cs_c[8], cs_s[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    cs_c[e] = 1.f;
-    cs_s[e] = 0.f;
-  }
-#pragma unroll 2
-  for (int it = 0; it < 8; ++it) {
-    const int r = 8 * it + r8;
-    const int d = delta[r];
-    if (d == 0) continue;
-    if (d != dprev) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[8 * v + e], cs_c[e], cs_s[e]);
-      dprev = d;
-    }
-    uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)v ^ (uint32_t)(r & 7)) << 4));
-    uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(4 + v) ^ (uint32_t)(r & 7)) << 4));
-    uint4 x = *px, y = *py;
-    rotate_pairs8(x, y, cs_c, cs_s);
-    *px = x;
-    *py = y;
-  }
-}
-
 // Rotate 8 rows [r0, r0 + 8) of a staged k_r slab by R(delta[row]) with one warp: lane =
 // (row of 8, 16-byte chunk v of 4) takes k_r[8v .. 8v+7] and its NeoX partners
 // k_r[32+8v .. 32+8v+7].  dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls
