@@ -8,9 +8,10 @@
 // load and the tensor-core read, so rotated keys are never written back to HBM.
 //
 // Structure (one 2-CTA cluster per 128-row query tile and KV split):
-//   - The [cKV | k_r] contraction of Q K^T is split by columns: CTA 0 owns cKV[0:256),
-//     CTA 1 owns cKV[256:512) and k_r (and therefore the rotation).  Each CTA loads only
-//     its own columns of every KV row, so each row is read from memory exactly once.
+//   - The [cKV | k_r] contraction of Q K^T is split by columns: CTA r owns cKV[256r, 256r+256)
+//     and the NeoX pairs j = 16r .. 16r+15 of k_r (columns j and 32 + j), and rotates them.
+//     The two CTAs thus load, rotate and multiply equal shares, and each loads only its own
+//     columns of every KV row, so each row is read from memory exactly once.
 //   - Each CTA computes its partial scores S_r = Q_r K_r^T (tcgen05, M=128, N=64) into
 //     TMEM and ships them to the peer with st.async; both add the two partials and run
 //     the identical online softmax, so P is bit-identical in both CTAs.
@@ -19,8 +20,8 @@
 //   - TMEM holds O (256 columns), two score buffers (64 columns each) and the CTA's four
 //     cKV slabs of Q as bf16 pairs (128 columns); the softmax writes P as bf16 pairs over
 //     the score buffer it just read, and both Q.K^T and P.V take their A operand from
-//     TMEM.  Only CTA 1's q_rope slab sits in shared memory, so nearly all of shared memory
-//     is KV pipeline stages.
+//     TMEM.  Only the CTA's half of q_rope sits in shared memory, so nearly all of shared
+//     memory is KV pipeline stages.
 //   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-7 gather KV rows with
 //     cp.async following the chunk table (completion tracked by an mbarrier, so they run
 //     ahead across stages) and, one tile behind, rotate k_r by R(delta) and publish the tile;
@@ -51,7 +52,7 @@ constexpr int kThreads = (kPvWarp + 1) * 32;             // 320
 constexpr int kLoaderThreads = kLoaderWarps * 32;
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
-constexpr uint32_t kSmemLimit = 232448;
+constexpr uint32_t kSmemLimit = 232448 - 128;  // opt-in maximum, less room for static shared memory
 
 // Fixed area at the start of shared memory.
 constexpr uint32_t kOffBars = 0;                                   // 64 mbarriers
@@ -89,25 +90,29 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);  // B (cKV tile) M
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t FULL = kFullMask;
 
-// Shared-memory layout of CTA `rank` for a given number of stored query rows (Mv, multiple
-// of 8).  The score exchange buffer sits at the same offset in both CTAs (the peer addresses
-// it through its own layout); CTA 1 adds the q_rope slab of Q; the rest is KV stages of
-// `nslab` 64-column slabs.
+// Shared-memory layout for a given number of stored query rows (Mv, multiple of 8), the same
+// in both CTAs (the peer addresses the score exchange buffer through its own layout): the
+// exchange buffer, the CTA's q_rope half (Mv rows x 128 B, first 64 B used), the KV stages'
+// cKV slabs (4 per stage), then their k_r halves: stage s owns chunks 4 (s & 1) .. 4 (s & 1) + 3
+// of k_r slab s / 2.
 struct Layout {
-  uint32_t x, qr, kv, stage, total;
+  uint32_t x, qr, kv, kr, stage, total;
   int stages;
 };
 __host__ __device__ inline Layout make_layout(int Mv, int rank) {
   Layout L;
   L.x = kFixedBytes;                                // 16 float4 x Mv rows
-  L.qr = L.x + (uint32_t)Mv * 256u;                 // CTA 1: Mv rows x 128 B
-  const uint32_t end = L.qr + (rank == 1 ? (uint32_t)Mv * 128u : 0u);
+  L.qr = L.x + (uint32_t)Mv * 256u;                 // Mv rows x 128 B
+  (void)rank;
+  const uint32_t end = L.qr + (uint32_t)Mv * 128u;
   L.kv = (end + 1023u) & ~1023u;
-  L.stage = (rank == 1 ? 5u : 4u) * kSlabKV;
+  L.stage = 4u * kSlabKV;  // cKV slabs of a stage; the k_r halves of stages 2i, 2i+1 share a slab
   const uint32_t avail = kSmemLimit - 1024u - L.kv;  // 1024: base alignment slack
-  int st = (int)(avail / L.stage);
-  L.stages = st > kMaxStages ? kMaxStages : st;
-  L.total = L.kv + (uint32_t)L.stages * L.stage + 1024u;
+  int st = kMaxStages;
+  while (st > 0 && (uint32_t)st * L.stage + (uint32_t)((st + 1) / 2) * kSlabKV > avail) --st;
+  L.stages = st;
+  L.kr = L.kv + (uint32_t)st * L.stage;
+  L.total = L.kr + (uint32_t)((st + 1) / 2) * kSlabKV + 1024u;
   return L;
 }
 __host__ __device__ inline uint32_t launch_smem(int Mv) {
@@ -124,11 +129,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int nslab = rank == 0 ? 4 : 5;
   const int col0 = (int)rank * 256;
+  const int p0 = (int)rank * 16;  // this CTA's NeoX pairs of k_r: p0 .. p0+15
   const int Mv = a.Mv;
   const Layout L = make_layout(Mv, (int)rank);
   const int NS = L.stages;
+  auto kr_slab = [&](int st) -> uint32_t { return L.kr + (uint32_t)(st >> 1) * kSlabKV; };  // smem offset
 
   // ---- work unit: request b, query tile, KV split --------------------------------------
   const int b = blockIdx.y;
@@ -202,9 +208,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
     const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
 
-    // CTA 1's q_rope slab: Mv rows (rows past the tile's valid rows are zero filled); it
+    // Stored chunk c (0..3) of this CTA's k_r / q_rope half: columns (c < 2 ? 0 : 32) + p0 +
+    // 8 (c & 1) of the 64 rope columns (its pairs' first then second halves).
+    const int kr_col = (chk < 2 ? 0 : 32) + p0 + 8 * (chk & 1);
+    // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
     // lands with the first KV tile (same cp.async group).
-    if (ntiles > 0 && rank == 1) {
+    if (ntiles > 0 && chk < 4) {
       for (int m = rsub; m < Mv; m += kLoaderThreads / 8) {
         const bool valid = m < rows_valid;
         int64_t row = 0;
@@ -212,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int qi = q0 + m / a.H, h = m % a.H;
           row = ((int64_t)b * a.n_q + qi) * a.H + h;
         }
-        const void* src = valid ? (const void*)(qr + row * kDRope + chk * 8) : a.q_rope;
+        const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
         cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
       }
     }
@@ -225,8 +234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cw.win = c_begin;
     if (pw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
 
-    // Publish a landed tile: rank 1 rotates k_r by R(delta) in shared memory (loader warp pw
-    // owns rows 16pw..16pw+15), then every warp arrives on KV_FULL.  The Q.K^T issuer fences
+    // Publish a landed tile: rotate this CTA's k_r pairs by R(delta) in shared memory (loader
+    // warp pw owns rows 16pw..16pw+15), then every warp arrives on KV_FULL.  The Q.K^T issuer fences
     // the bytes for the async proxy after acquiring KV_FULL (a loader's own fence would also
     // wait for its copies of later tiles in flight).
     int dprev = 0;
@@ -239,11 +248,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto publish = [&](int sp, uint32_t php) -> bool {
       if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
       __syncwarp();
-      if (rank == 1) {
-        uint8_t* kr = smem + L.kv + (uint32_t)sp * L.stage + 4 * kSlabKV;
-        rotate_krope_8rows(kr, map_delta + sp * kBN, phaseF, 16 * pw, lane, dprev, cs_c, cs_s);
-        rotate_krope_8rows(kr, map_delta + sp * kBN, phaseF, 16 * pw + 8, lane, dprev, cs_c, cs_s);
-      }
+      rotate_krope_half_16rows(smem + kr_slab(sp), map_delta + sp * kBN, phaseF, 16 * pw, p0, 4 * (sp & 1), lane,
+                               dprev, cs_c, cs_s);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + sp));
       return true;
@@ -289,10 +295,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
           const int row = rr + rsub;
           const int sr = map_src[s * kBN + row];
-          const __nv_bfloat16* rowp = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + col0 + chk * 8;
+          const __nv_bfloat16* kvrow = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow;
+          const __nv_bfloat16* rowp = kvrow + col0 + chk * 8;
           const uint32_t dst = stage + sw128_offset(row, chk);
           const uint32_t nb = sr >= 0 ? 16u : 0u;
-          for (int slab = 0; slab < nslab; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
+#pragma unroll
+          for (int slab = 0; slab < 4; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
+          if (chk < 4)
+            cp_async_16(sb + kr_slab(s) + sw128_offset(row, chk + 4 * (s & 1)), kvrow + kDLat + kr_col, nb);
         }
         cp_async_arrive_noinc(bar(BAR_LANDED + s));
       }
@@ -334,13 +344,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, bd, kIdescS, (slab | kk) ? 1u : 0u);
           }
         }
-        if (nslab == 5) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(stage + 4 * kSlabKV + kk * 32, 16, 1024);
-            umma_bf16(tS, ad, bd, kIdescS, 1u);
-          }
+        for (int kk = 0; kk < 2; ++kk) {  // the half k_r slab: 32 columns, 2 K-steps
+          const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64 + kk * 32, 16, 1024);
+          umma_bf16(tS, ad, bd, kIdescS, 1u);
         }
         umma_commit(bar(BAR_S_FULL + (ns & 1)));
         if (++ss == NS) {

@@ -121,6 +121,29 @@ __device__ __forceinline__ void rotate_krope_8rows(uint8_t* kr, const int32_t* d
   *py = y;
 }
 
+// Rotate 16 rows [r0, r0 + 16) of a staged half k_r slab: 16 NeoX pairs j = p0 .. p0+15 per
+// row, stored as chunks cb, cb+1 = k_r[p0 .. p0+15] and chunks cb+2, cb+3 = their partners
+// k_r[32+p0 .. 32+p0+15] (128-byte swizzle; cb = 0 or 4, two stages share a slab).  Lane =
+// (row of 16, chunk c of 2); dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls.
+__device__ __forceinline__ void rotate_krope_half_16rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
+                                                         int r0, int p0, int cb, int lane, int& dprev,
+                                                         float (&cs_c)[8], float (&cs_s)[8]) {
+  const int r = r0 + (lane >> 1), c = lane & 1;
+  const int d = delta[r];
+  if (d == 0) return;
+  if (d != dprev) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[p0 + 8 * c + e], cs_c[e], cs_s[e]);
+    dprev = d;
+  }
+  uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(cb + c) ^ (uint32_t)(r & 7)) << 4));
+  uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(cb + 2 + c) ^ (uint32_t)(r & 7)) << 4));
+  uint4 x = *px, y = *py;
+  rotate_pairs8(x, y, cs_c, cs_s);
+  *px = x;
+  *py = y;
+}
+
 // Warp-uniform bounded waits: every lane polls (and so acquires) the barrier, and the
 // verdict is agreed with __all_sync so no lane leaves a loop its warp-mates stay in.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
