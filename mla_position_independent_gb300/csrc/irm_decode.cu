@@ -33,7 +33,8 @@
 // a tile as they land.
 // Warp roles: 0-3 softmax, 4-11 loaders (cp.async row gather following the chunk table, and
 // the k_r rotation: each loader warp rotates 8 rows of every landed k_r slot between its
-// copies), 12 TMEM allocation and the S^T UMMAs, 13 the P.V UMMAs.  A single thread issues
+// copies), 12 TMEM allocation and the S^T UMMAs, 13 the P.V UMMAs, 14 the row maps (built up to
+// three tiles ahead, so the loaders never wait for one).  A single thread issues
 // these small UMMAs no faster than one per ~40 cycles, so the two products get one issuing
 // thread each (each thread commits and drains only its own UMMAs).  Bytes written by cp.async
 // or by the rotation reach the tensor core through a proxy fence that the S^T issuer executes
@@ -65,7 +66,8 @@ struct Roles {
   static constexpr int kLoaderWarps = H <= 16 ? 8 : 4;
   static constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // S^T issuer
   static constexpr int kPvWarp = kMmaWarp + 1;                    // P.V issuer
-  static constexpr int kThreads = (kPvWarp + 1) * 32;
+  static constexpr int kMapWarp = kPvWarp + 1;                    // row maps, ahead of the loaders
+  static constexpr int kThreads = (kMapWarp + 1) * 32;
   static constexpr int kLoaderThreads = kLoaderWarps * 32;
   static constexpr int kRowsPerPass = kLoaderThreads / 8;  // rows one pass of the loaders covers
   static constexpr int kLoadPasses = kBN / kRowsPerPass;
@@ -154,7 +156,8 @@ __device__ __forceinline__ void tmem_st_h<32>(uint32_t taddr, const uint32_t (&r
 template <int H>
 __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
   using R = Roles<H>;
-  constexpr int kLoaderWarps = R::kLoaderWarps, kMmaWarp = R::kMmaWarp, kPvWarp = R::kPvWarp;
+  constexpr int kLoaderWarps = R::kLoaderWarps, kMmaWarp = R::kMmaWarp, kPvWarp = R::kPvWarp,
+                kMapWarp = R::kMapWarp;
   constexpr int kThreads = R::kThreads, kLoaderThreads = R::kLoaderThreads;
   constexpr int kRowsPerPass = R::kRowsPerPass, kLoadPasses = R::kLoadPasses;
   extern __shared__ uint8_t smem_raw[];
@@ -243,12 +246,6 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       }
     }
 
-    ChunkWindow cw;
-    cw.chunks = a.chunks;
-    cw.c_end = c_end;
-    cw.win = c_begin;
-    if (pw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
-
     // k_r rotation, in tile order: this warp's 8 rows of every slot whose bytes have landed
     int rot = 0;
     int dprev = 0;
@@ -289,11 +286,6 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       const uint32_t kph = (uint32_t)(j / kKrSlots) & 1u;
       // k_r slot ks and its row map are free once the S^T of tile j - kKrSlots is done
       if (j >= kKrSlots && !(ok = wait_rotating(bar(BAR_KR_EMPTY + ks), kph ^ 1u, j))) break;
-      if (pw == 0) {
-        cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + ks * kBN, map_delta + ks * kBN, a.status, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_MAP + ks));
-      }
       if (!(ok = warp_wait(bar(BAR_MAP + ks), kph, abort_flag))) break;
       const __nv_bfloat16* rowp[kLoadPasses];
       uint32_t nb[kLoadPasses];
@@ -330,6 +322,27 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       rotate_landed(rot + 1);
     }
     cp_async_wait_all();
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.status, kDevErrTimeout);
+    }
+  } else if (warp == kMapWarp) {
+    // ======================= row maps: tile t into slot t % 3 once tile t-3's S^T is done ======
+    ChunkWindow cw;
+    cw.chunks = a.chunks;
+    cw.c_end = c_end;
+    cw.win = c_begin;
+    bool ok = true;
+    if (ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int ks = t % kKrSlots;
+      if (t >= kKrSlots &&
+          !(ok = warp_wait(bar(BAR_KR_EMPTY + ks), ((uint32_t)(t / kKrSlots) & 1u) ^ 1u, abort_flag)))
+        break;
+      cw.build_map((kb + t) * kBN, ctx, a.n_rows, map_src + ks * kBN, map_delta + ks * kBN, a.status, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_MAP + ks));
+    }
     if (!ok) {
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
