@@ -137,6 +137,8 @@ def _prep_case(name, seed):
         return synth.v3_decode(seed, device="cuda")
     if name == "chunked_prefill":
         return synth.chunked_prefill(seed, device="cuda")
+    if name == "chunked_prefill_256":
+        return synth.chunked_prefill(seed, device="cuda", n_q=256)
     if name.startswith("rotate_gather_"):
         n = int(name.split("_")[-1].rstrip("M")) << 20
         return synth.rotate_gather_case(n, seed, device="cuda", fill_kv=False)
@@ -150,6 +152,8 @@ DESCR = {
                  "chunks in shuffled order (~80% of tokens), delta ~ U[-16384,16384]",
     "chunked_prefill": "chunked prefill: 128 heads, 4 requests, 2048 causal queries over a "
                        "16384-token prefix (4096 exact-prefix delta=0, 12288 moved delta ~ U[-8192,8192])",
+    "chunked_prefill_256": "profiling-size slice of the chunked prefill: the same prefix, 256 new "
+                           "causal queries per request",
 }
 
 
@@ -336,7 +340,8 @@ def oracle_sample(name, budget_s=None, steps=None, warmup=0):
     import oracle
     from mla_position_independent_gb300 import synth
     case = {"v2lite_decode": synth.v2lite_decode, "v3_decode": synth.v3_decode,
-            "chunked_prefill": synth.chunked_prefill}[name](0)
+            "chunked_prefill": synth.chunked_prefill,
+            "chunked_prefill_256": lambda seed: synth.chunked_prefill(seed, n_q=256)}[name](0)
     kv = synth.bits(case.kv_rows)
     ql, qr = synth.bits(case.q_lat), synth.bits(case.q_rope)
     B, n_q, H = ql.shape[:3]
