@@ -13,8 +13,10 @@
 //     The two CTAs thus load, rotate and multiply equal shares, and each loads only its own
 //     columns of every KV row, so each row is read from memory exactly once.
 //   - Each CTA computes its partial scores S_r = Q_r K_r^T (tcgen05, M=128, N=64) into
-//     TMEM and ships them to the peer with st.async; both add the two partials and run
-//     the identical online softmax, so P is bit-identical in both CTAs.
+//     TMEM and ships them to the peer with st.async, as fp16 (half the bytes and stores of
+//     the exchange; the rounding, ~5e-4 of a partial, is well below P's own bf16 rounding).
+//     Both add the same two fp16-rounded partials and run the identical online softmax, so
+//     P is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
 //   - TMEM holds O (256 columns), two score buffers (64 columns each) and the CTA's four
@@ -101,8 +103,8 @@ struct Layout {
 };
 __host__ __device__ inline Layout make_layout(int Mv, int rank) {
   Layout L;
-  L.x = kFixedBytes;                                // 16 float4 x Mv rows
-  L.qr = L.x + (uint32_t)Mv * 256u;                 // Mv rows x 128 B
+  L.x = kFixedBytes;                                // 8 x Mv 16-byte words (8 fp16 scores each)
+  L.qr = L.x + (uint32_t)Mv * 128u;                 // Mv rows x 128 B
   (void)rank;
   const uint32_t end = L.qr + (uint32_t)Mv * 128u;
   L.kv = (end + 1023u) & ~1023u;
@@ -407,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rX = mapa_shared(sb + L.x, peer);
     const uint32_t rXfull = mapa_shared(bar(BAR_X_FULL), peer);
     const uint32_t rXempty = mapa_shared(bar(BAR_X_EMPTY), peer);
-    const float4* X = reinterpret_cast<const float4*>(smem + L.x);
+    const uint4* X = reinterpret_cast<const uint4*>(smem + L.x);
     bool ok = true;
     // Q, this CTA's cKV columns, into TMEM: thread m stores row m's 256 columns as bf16 pairs
     // (rows past the valid ones are zero; warps holding no stored rows leave their lanes)
@@ -455,22 +457,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // exchange partial scores with the peer (each side owns part of the contraction)
       if (j >= 1 && !(ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag))) break;
-      if (m == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 4u);
+      if (m == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
       if (row_live) {
+        // own partial rounded to fp16 exactly as the peer receives it, packed 8 per 16 bytes
 #pragma unroll
-        for (int i = 0; i < kBN / 4; ++i)
-          st_async_v4(rX + (uint32_t)(i * Mv + m) * 16u, sv[4 * i], sv[4 * i + 1], sv[4 * i + 2],
-                      sv[4 * i + 3], rXfull);
+        for (int i = 0; i < kBN / 8; ++i) {
+          uint4 w;
+          __half2 h;
+          h = __floats2half2_rn(sv[8 * i], sv[8 * i + 1]);
+          w.x = *reinterpret_cast<uint32_t*>(&h);
+          h = __floats2half2_rn(sv[8 * i + 2], sv[8 * i + 3]);
+          w.y = *reinterpret_cast<uint32_t*>(&h);
+          h = __floats2half2_rn(sv[8 * i + 4], sv[8 * i + 5]);
+          w.z = *reinterpret_cast<uint32_t*>(&h);
+          h = __floats2half2_rn(sv[8 * i + 6], sv[8 * i + 7]);
+          w.w = *reinterpret_cast<uint32_t*>(&h);
+          st_async_v4_b32(rX + (uint32_t)(i * Mv + m) * 16u, w, rXfull);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+            sv[8 * i + 2 * k] = f.x;
+            sv[8 * i + 2 * k + 1] = f.y;
+          }
+        }
       }
       if (!(ok = warp_wait_cluster(bar(BAR_X_FULL), j & 1, abort_flag))) break;
       if (row_live) {
 #pragma unroll
-        for (int i = 0; i < kBN / 4; ++i) {
-          const float4 v = X[i * Mv + m];
-          sv[4 * i] += v.x;
-          sv[4 * i + 1] += v.y;
-          sv[4 * i + 2] += v.z;
-          sv[4 * i + 3] += v.w;
+        for (int i = 0; i < kBN / 8; ++i) {
+          const uint4 v = X[i * Mv + m];
+          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
+            sv[8 * i + 2 * k] += f.x;
+            sv[8 * i + 2 * k + 1] += f.y;
+          }
         }
       }
       __syncwarp();

@@ -188,12 +188,11 @@ __device__ __forceinline__ void cluster_wait() {
 }
 // 16-byte store into a peer CTA's shared memory; completion is counted in bytes on the
 // peer's mbarrier (complete_tx).
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
-                                            float d, uint32_t cluster_bar) {
+__device__ __forceinline__ void st_async_v4_b32(uint32_t cluster_addr, uint4 v, uint32_t cluster_bar) {
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
           cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
       : "memory");
 }
 
