@@ -12,7 +12,7 @@
 //     splits of a request form G thread-block clusters of C CTAs: after the pipeline every
 //     CTA parks its unnormalised O^T and per-head (max, sum) in shared memory, and each
 //     cluster merges its C splits through distributed shared memory, CTA r producing output
-//     slice r.  With G = 1 that is the output; otherwise each cluster writes its slice as a
+//     slice r (remote loads issued in batches of 8 splits, one round trip per batch).  With G = 1 that is the output; otherwise each cluster writes its slice as a
 //     normalised partial, and the last cluster to finish a slice (a self-resetting counter
 //     per request and slice) merges the G partials of that slice.
 //   - Small UMMAs cost a fixed ~46 cycles each, so S^T is issued as few instructions as
@@ -152,6 +152,29 @@ template <>
 __device__ __forceinline__ void tmem_st_h<16>(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 template <>
 __device__ __forceinline__ void tmem_st_h<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
+
+// Fold 8 partial results (log2 max or log2-sum-exp mq, sum lq, output vq) into a running
+// (M, den, acc): acc and den are kept relative to M, rescaled when M grows.
+__device__ __forceinline__ void merge_batch(const float (&mq)[8], const float (&lq)[8], const float4 (&vq)[8],
+                                            float& M, float& den, float4& acc) {
+  float Mn = M;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mq[k]);
+  if (Mn == -INFINITY) return;
+  const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+  den *= sc;
+  acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float w = (mq[k] == -INFINITY) ? 0.f : fast_exp2(mq[k] - Mn);
+    den += w * lq[k];
+    acc.x += w * vq[k].x;
+    acc.y += w * vq[k].y;
+    acc.z += w * vq[k].z;
+    acc.w += w * vq[k].w;
+  }
+  M = Mn;
+}
 
 template <int H>
 __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -625,23 +648,27 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   for (int it = tid; it < per; it += kThreads) {
     const int item = crank * per + it;
     const int h = item >> 7, c4 = item & 127;
-    float M = -INFINITY;
-    for (int q = 0; q < C; ++q) M = fmaxf(M, ld_cluster_f32(mapa_shared(sb + kOffML + 4u * h, (uint32_t)q)));
+    // online merge over the splits, 8 at a time: every remote load of a batch is issued before
+    // any is used, so a batch costs one round trip through the cluster
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
-    if (M != -INFINITY) {
-      for (int q = 0; q < C; ++q) {
-        const uint32_t base = mapa_shared(sb, (uint32_t)q);
-        const float mq = ld_cluster_f32(base + kOffML + 4u * h);
-        if (mq == -INFINITY) continue;
-        const float w = fast_exp2(mq - M);
-        den += w * ld_cluster_f32(base + kOffML + 128u + 4u * h);
-        const float4 v = ld_cluster_v4(base + L.ring + (uint32_t)(h * kDLat + 4 * c4) * 4u);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+    for (int q0 = 0; q0 < C; q0 += 8) {
+      float mq[8], lq[8];
+      float4 vq[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (q0 + k < C) {
+          const uint32_t base = mapa_shared(sb, (uint32_t)(q0 + k));
+          mq[k] = ld_cluster_f32(base + kOffML + 4u * h);
+          lq[k] = ld_cluster_f32(base + kOffML + 128u + 4u * h);
+          vq[k] = ld_cluster_v4(base + L.ring + (uint32_t)(h * kDLat + 4 * c4) * 4u);
+        } else {
+          mq[k] = -INFINITY;
+          lq[k] = 0.f;
+          vq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+      merge_batch(mq, lq, vq, M, den, acc);
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -679,22 +706,24 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         const int item = crank * per + it;
         const int h = item >> 7, c4 = item & 127;
         const float* gl = a.glse + (int64_t)b * G * H + h;
-        float M = -INFINITY;
-        for (int q = 0; q < G; ++q) M = fmaxf(M, __ldcg(gl + (int64_t)q * H));
+        float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.f;
-        if (M != -INFINITY) {
-          for (int q = 0; q < G; ++q) {
-            const float lq = __ldcg(gl + (int64_t)q * H);
-            if (lq == -INFINITY) continue;
-            const float w = fast_exp2(lq - M);
-            const float4 v = __ldcg(gpart + ((int64_t)b * G + q) * (H * 128) + item);
-            den += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+        for (int q0 = 0; q0 < G; q0 += 8) {
+          float mq[8], lq[8];
+          float4 vq[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (q0 + k < G) {
+              mq[k] = __ldcg(gl + (int64_t)(q0 + k) * H);  // log2-sum-exp of a normalised partial
+              lq[k] = 1.f;
+              vq[k] = __ldcg(gpart + ((int64_t)b * G + q0 + k) * (H * 128) + item);
+            } else {
+              mq[k] = -INFINITY;
+              lq[k] = 0.f;
+              vq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
+          merge_batch(mq, lq, vq, M, den, acc);
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
         const int64_t orow = (int64_t)b * H + h;

@@ -196,18 +196,19 @@ __device__ __forceinline__ void st_async_v4_b32(uint32_t cluster_addr, uint4 v, 
       : "memory");
 }
 
-// Loads from a (possibly remote) CTA's shared memory through a shared::cluster address.
+// Loads from a (possibly remote) CTA's shared memory through a shared::cluster address, for
+// data that no longer changes (published before a cluster barrier): not volatile, so the
+// compiler may batch and reorder them.
 __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
 }
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
   float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
+  asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "r"(cluster_addr));
   return v;
 }
 
