@@ -10,7 +10,7 @@ A step is one pass of the whole hot path over one batch: chunk-table walk, per-c
 rotation angles, gather of [cKV | k_r] rows, delta-rotation in shared memory, Q.K^T,
 online softmax, P.cKV (and the split-KV merge for decode) -- one call of the C ABI.
 Steps are timed with CUDA events on the launching stream, each step replayed from a CUDA
-graph, with L2 flushed (256 MiB write, untimed) between steps.  The oracle arm
+graph, with L2 flushed (256 MiB write then 256 MiB read, untimed) between steps.  The oracle arm
 (--impl reference) times the fp64 CPU oracle on a bounded sample of the same workload.
 Under torchrun every rank runs its own replica (weak scaling); rank 0 prints one JSON line.
 """
@@ -235,10 +235,30 @@ class Workload:
         self.irm.device_status(self.ws)
 
 
+class L2Flush:
+    """Untimed L2 flush between steps: write a buffer twice the size of L2, then read another
+    one.  The read evicts the written (dirty) lines, so the timed step starts with an L2 that
+    holds neither its inputs nor write-backs owed by the flush itself (the cold-cache state
+    that ncu's cache control also gives a kernel)."""
+
+    def __init__(self):
+        self.wr = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.rd = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device="cuda")
+        self.acc = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def __call__(self, i):
+        self.wr.fill_(i & 0xff)
+        torch.sum(self.rd, dim=0, out=self.acc)
+
+
+L2_NOTE = ("flushed between steps (untimed): 256 MiB write, then 256 MiB read so that no "
+           "dirty flush lines are written back inside the timed step")
+
+
 def time_steps(wl: Workload, steps: int, warmup: int, use_graph=True):
     """Per-step CUDA-event time (ms) of `steps` steps, L2 flushed before each (untimed)."""
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     for _ in range(max(warmup, 1)):
         wl.step()
     torch.cuda.synchronize()
@@ -258,7 +278,7 @@ def time_steps(wl: Workload, steps: int, warmup: int, use_graph=True):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush.fill_(i & 0xff)
+        flush(i)
         starts[i].record(stream)
         if graph is not None:
             graph.replay()
@@ -279,10 +299,10 @@ def e2e_decode(wl: Workload, steps: int):
     qr_h = wl.q_rope.cpu().pin_memory()
     ch_h = torch.from_numpy(wl.table.chunks_host.view(np.uint8).copy()).pin_memory()
     out_h = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     times = []
     for i in range(steps + 3):
-        flush.fill_(i & 0xff)
+        flush(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         wl.q_lat.copy_(ql_h, non_blocking=True)
@@ -442,7 +462,7 @@ def main():
                 scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
                 config=dict(workload=args.workload, description=DESCR.get(args.workload),
                             requests=wl.table.B, ctx_total=wl.ctx_total,
-                            l2="flushed between steps (256 MiB write, untimed)",
+                            l2=L2_NOTE,
                             parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
                 roofline=rf, e2e=e2e, gpu_launches=args.steps * wl.launches_per_step(),
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"],

@@ -15,20 +15,24 @@
 //   - Each CTA computes its partial scores S_r = Q_r K_r^T (tcgen05, M=128, N=64) into
 //     TMEM and ships them to the peer with st.async, as fp16 (half the bytes and stores of
 //     the exchange; the rounding, ~5e-4 of a partial, is well below P's own bf16 rounding).
-//     Both add the same two fp16-rounded partials and run the identical online softmax, so
-//     P is bit-identical in both CTAs.
+//     Both form round_f32(fp16 own + fp16 peer) and run the identical online softmax, so P
+//     is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
 //   - TMEM holds O (256 columns), two score buffers (64 columns each) and the CTA's four
 //     cKV slabs of Q as bf16 pairs (128 columns); the softmax writes P as bf16 pairs over
 //     the score buffer it just read, and both Q.K^T and P.V take their A operand from
-//     TMEM.  Only the CTA's half of q_rope sits in shared memory, so nearly all of shared
-//     memory is KV pipeline stages.
-//   - Warp roles: 0-3 softmax (thread = TMEM lane = query row); 4-7 gather KV rows with
-//     cp.async following the chunk table (completion tracked by an mbarrier, so they run
-//     ahead across stages) and, one tile behind, rotate k_r by R(delta) and publish the tile;
-//     8 allocates TMEM and issues Q.K^T, 9 issues P.V (one issuing thread per product: a
-//     thread issues UMMAs no faster than one per ~40 cycles).
+//     TMEM.  Both issuers build their operand descriptors once per tile and step them by
+//     constants (a thread issues one UMMA per ~50 cycles at best, so small UMMAs are
+//     issue-bound).  Only the CTA's half of q_rope sits in shared memory, so nearly all of
+//     shared memory is KV pipeline stages.
+//   - Warp roles: 0-7 softmax, two warps per TMEM lane quadrant (thread = TMEM lane = query
+//     row; warps 0-3 take keys 0-31 of every tile, warps 4-7 keys 32-63, and the two halves
+//     agree on the row's running max through one barrier reduction per tile); 8-9 gather KV
+//     rows with cp.async following the chunk table (completion tracked by an mbarrier, so
+//     they run ahead across stages); 10-11 rotate each landed tile's k_r by R(delta) and
+//     publish it; 12 allocates TMEM and issues Q.K^T, 13 issues P.V (one issuing thread per
+//     product).
 //   - Only the first Mv rows (valid query rows rounded up to 8) of the q_rope slab and the
 //     score exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
 //     whatever follows in shared memory (or TMEM lanes nobody wrote).  Those rows only
@@ -46,12 +50,15 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 64;   // KV rows per tile
-constexpr int kSoftmaxWarps = 4;
-constexpr int kLoaderWarps = 4;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 8: TMEM allocation, Q.K^T issue
-constexpr int kPvWarp = kMmaWarp + 1;                    // 9: P.V issue
-constexpr int kThreads = (kPvWarp + 1) * 32;             // 320
-constexpr int kLoaderThreads = kLoaderWarps * 32;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant: keys 0-31 / 32-63 of a tile
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kLoaderWarps = 4;   // 2 copy warps + 2 publishers
+constexpr int kCopyWarps = 2;
+constexpr int kCopyThreads = kCopyWarps * 32;
+constexpr int kPubWarps = kLoaderWarps - kCopyWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 12: TMEM allocation, Q.K^T issue
+constexpr int kPvWarp = kMmaWarp + 1;                    // 13: P.V issue
+constexpr int kThreads = (kPvWarp + 1) * 32;             // 448
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
 constexpr uint32_t kSmemLimit = 232448 - 128;  // opt-in maximum, less room for static shared memory
@@ -63,20 +70,28 @@ constexpr uint32_t kOffMapDelta = kOffMapSrc + kMaxStages * kBN * 4;
 constexpr uint32_t kOffPhase = kOffMapDelta + kMaxStages * kBN * 4;  // uint64 [32]
 constexpr uint32_t kOffTmemPtr = kOffPhase + 32 * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kFixedBytes = 4096;
-static_assert(kOffAbort + 4 <= kFixedBytes, "fixed area overflow");
+constexpr uint32_t kOffHalfMax = kOffAbort + 12;          // float [2 halves][128 rows]: tile max
+constexpr uint32_t kOffHalfL = kOffHalfMax + 2 * 128 * 4;   // float [2 halves][128 rows]: row sum
+constexpr uint32_t kFixedBytes = 6144;
+static_assert(kOffHalfL + 2 * 128 * 4 <= kFixedBytes, "fixed area overflow");
+
+// Named barriers (0 is __syncthreads): the softmax warps' per-tile reduction and the rare
+// second round of it, and the split-KV completion count.
+constexpr int kBarSmRed = 2;
+constexpr int kBarSmRed2 = 3;
+constexpr int kBarSmMerge = 1;
 
 enum : int {
-  BAR_KV_FULL = 0,                      // [kMaxStages] loaders published the tile (count 4)
+  BAR_KV_FULL = 0,                      // [kMaxStages] publishers published the tile (count 2)
   BAR_KV_EMPTY = BAR_KV_FULL + kMaxStages,  // [kMaxStages] UMMA commit after P.V of the stage
-  BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every loader thread's copies landed
+  BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every copy thread's copies landed
   BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
   BAR_S_FULL = BAR_MAP + kMaxStages,        // [2] UMMA commit after Q.K^T into S buffer
   BAR_PV_DONE = BAR_S_FULL + 2,             // [2] UMMA commit after P.V of the P in S buffer
-  BAR_P_FULL = BAR_PV_DONE + 2,             // [2] softmax wrote P over S buffer (and rescaled O) (count 4)
-  BAR_Q_FULL = BAR_P_FULL + 2,              // softmax warps stored Q in TMEM (count 4)
+  BAR_P_FULL = BAR_PV_DONE + 2,             // [2] softmax wrote P over S buffer (and rescaled O) (count 8)
+  BAR_Q_FULL = BAR_P_FULL + 2,              // softmax warps stored Q in TMEM (count 8)
   BAR_X_FULL = BAR_Q_FULL + 1,              // peer's partial scores landed (1 arrive + tx)
-  BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 4 softmax warps consumed our scores (remote)
+  BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 8 softmax warps consumed our scores (remote)
   BAR_DRAIN = BAR_X_EMPTY + 1,              // [2] all UMMAs of the Q.K^T / P.V issuer done
   NUM_BARS = BAR_DRAIN + 2,
 };
@@ -171,9 +186,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     last_sh = 0;
     if (!table_ok) set_status(a.status, kDevErrBounds);
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), kLoaderWarps);
+      mbar_init(bar(BAR_KV_FULL + s), kPubWarps);
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
-      mbar_init(bar(BAR_LANDED + s), kLoaderThreads);
+      mbar_init(bar(BAR_LANDED + s), kCopyThreads);
       mbar_init(bar(BAR_MAP + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -181,9 +196,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_PV_DONE + s), 1);
       mbar_init(bar(BAR_P_FULL + s), kSoftmaxWarps);
     }
-    mbar_init(bar(BAR_Q_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_X_FULL), 1);
     mbar_init(bar(BAR_X_EMPTY), kSoftmaxWarps);
+    mbar_init(bar(BAR_Q_FULL), kSoftmaxWarps);
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_DRAIN + 1), 1);
     *abort_flag = 0;
@@ -202,67 +217,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
 
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-    // ======================= loaders: row gather with cp.async =========================
-    const int tp = tid - kSoftmaxWarps * 32;
-    const int pw = warp - kSoftmaxWarps;
-    const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
-    const int rsub = tp >> 3;   // row within a group of kLoaderThreads / 8
-    const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
-    const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
-
-    // Stored chunk c (0..3) of this CTA's k_r / q_rope half: columns (c < 2 ? 0 : 32) + p0 +
-    // 8 (c & 1) of the 64 rope columns (its pairs' first then second halves).
-    const int kr_col = (chk < 2 ? 0 : 32) + p0 + 8 * (chk & 1);
-    // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
-    // lands with the first KV tile (same cp.async group).
-    if (ntiles > 0 && chk < 4) {
-      for (int m = rsub; m < Mv; m += kLoaderThreads / 8) {
-        const bool valid = m < rows_valid;
-        int64_t row = 0;
-        if (valid) {
-          const int qi = q0 + m / a.H, h = m % a.H;
-          row = ((int64_t)b * a.n_q + qi) * a.H + h;
+    // ======================= loaders =====================================================
+    // Warps 8-9 gather KV rows with cp.async following the chunk table (warp 8 also builds the
+    // row maps); warps 10-11 wait for each tile's bytes to land, rotate this CTA's k_r pairs by
+    // R(delta) in shared memory and publish the tile.  Every role blocks in mbarrier waits, so
+    // no loader warp spins for issue slots the softmax warps need, and the copies run up to NS
+    // tiles ahead.  The Q.K^T issuer fences the bytes for the async proxy after acquiring
+    // KV_FULL (a writer's own fence would also wait for its copies of later tiles in flight).
+    const int lw = warp - kSoftmaxWarps;  // 0-1 copy warps, 2-3 publishers
+    bool ok = true;
+    if (lw < kCopyWarps) {
+      const int tp = tid - kSoftmaxWarps * 32;  // 0 .. kCopyThreads - 1
+      const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
+      const int rsub = tp >> 3;   // row within a group of kCopyThreads / 8
+      const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
+      const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
+      // Stored chunk c (0..3) of this CTA's k_r / q_rope half: columns (c < 2 ? 0 : 32) + p0 +
+      // 8 (c & 1) of the 64 rope columns (its pairs' first then second halves).
+      const int kr_col = (chk < 2 ? 0 : 32) + p0 + 8 * (chk & 1);
+      // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
+      // lands with the first KV tile (same cp.async group).
+      if (ntiles > 0 && chk < 4) {
+        for (int m = rsub; m < Mv; m += kCopyThreads / 8) {
+          const bool valid = m < rows_valid;
+          int64_t row = 0;
+          if (valid) {
+            const int qi = q0 + m / a.H, h = m % a.H;
+            row = ((int64_t)b * a.n_q + qi) * a.H + h;
+          }
+          const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
+          cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
         }
-        const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
-        cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
       }
-    }
-
-    // Loader warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
-    // per-tile row maps: source row (-1 = outside the context, zero filled) and delta.
-    ChunkWindow cw;
-    cw.chunks = a.chunks;
-    cw.c_end = c_end;
-    cw.win = c_begin;
-    if (pw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
-
-    // Publish a landed tile: rotate this CTA's k_r pairs by R(delta) in shared memory (loader
-    // warp pw owns rows 16pw..16pw+15), then every warp arrives on KV_FULL.  The Q.K^T issuer fences
-    // the bytes for the async proxy after acquiring KV_FULL (a loader's own fence would also
-    // wait for its copies of later tiles in flight).
-    int dprev = 0;
-    float cs_c[8], cs_s[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      cs_c[e] = 1.f;
-      cs_s[e] = 0.f;
-    }
-    auto publish = [&](int sp, uint32_t php) -> bool {
-      if (!warp_wait(bar(BAR_LANDED + sp), php, abort_flag)) return false;
-      __syncwarp();
-      rotate_krope_half_16rows(smem + kr_slab(sp), map_delta + sp * kBN, phaseF, 16 * pw, p0, 4 * (sp & 1), lane,
-                               dprev, cs_c, cs_s);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + sp));
-      return true;
-    };
-
-    bool ok = true, pending = false;
-    int s = 0, sprev = 0;
-    uint32_t ph = 0, phprev = 0;
-    for (int j = 0; j <= ntiles; ++j) {
-      if (j < ntiles) {
-        if (pw == 0) {
+      // Copy warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
+      // per-tile row maps: source row (-1 = outside the context, zero filled) and delta.
+      ChunkWindow cw;
+      cw.chunks = a.chunks;
+      cw.c_end = c_end;
+      cw.win = c_begin;
+      if (lw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        if (lw == 0) {
           // the map slot is free once tile j-NS was published; build the map now, while stage
           // s may still be in use by the P.V of tile j-NS
           if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
@@ -270,31 +267,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
         }
-        // stage s is free once the P.V of tile j-NS completed; while waiting for it, publish
-        // the previous tile as soon as its bytes have landed (with few stages the P.V of tile
-        // j-NS may itself be waiting for that tile's scores)
-        if (j >= NS) {
-          const uint64_t t0 = globaltimer_ns();
-          for (;;) {
-            if (pending && __all_sync(FULL, mbar_test_wait(bar(BAR_LANDED + sprev), phprev))) {
-              if (!(ok = publish(sprev, phprev))) break;
-              pending = false;
-            }
-            if (__all_sync(FULL, mbar_test_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u))) break;
-            __nanosleep(32);
-            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
-              ok = false;
-              break;
-            }
-          }
-          if (!ok) break;
-          // every lane polled the phase above; one acquiring wait keeps the memory order
-          if (!(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
-        }
+        // stage s is free once the P.V of tile j-NS completed
+        if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
         if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
         const uint32_t stage = sb + L.kv + (uint32_t)s * L.stage;
 #pragma unroll 2
-        for (int rr = 0; rr < kBN; rr += kLoaderThreads / 8) {
+        for (int rr = 0; rr < kBN; rr += kCopyThreads / 8) {
           const int row = rr + rsub;
           const int sr = map_src[s * kBN + row];
           const __nv_bfloat16* kvrow = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow;
@@ -307,18 +285,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             cp_async_16(sb + kr_slab(s) + sw128_offset(row, chk + 4 * (s & 1)), kvrow + kDLat + kr_col, nb);
         }
         cp_async_arrive_noinc(bar(BAR_LANDED + s));
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
-      // publish the previous tile while this one is in flight
-      if (pending && !(ok = publish(sprev, phprev))) break;
-      pending = j < ntiles;
-      sprev = s;
-      phprev = ph;
-      if (++s == NS) {
-        s = 0;
-        ph ^= 1u;
+      cp_async_wait_all();
+    } else {
+      // publisher pb owns rows 32 pb .. 32 pb + 31 of every tile; each 16-row half keeps its
+      // lane's last (cos, sin) (recomputed only when the row's delta changes)
+      const int pb = lw - kCopyWarps;
+      int dprev[2] = {0, 0};
+      float cs_c[2][8], cs_s[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cs_c[h][e] = 1.f;
+          cs_s[h][e] = 0.f;
+        }
+      int s = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
+        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;  // orders the map's deltas
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          rotate_krope_half_16rows(smem + kr_slab(s), map_delta + s * kBN, phaseF, 32 * pb + 16 * h, p0,
+                                   4 * (s & 1), lane, dprev[h], cs_c[h], cs_s[h]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
-    cp_async_wait_all();
     if (!ok) {
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
@@ -330,6 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int ss = 0;
       uint32_t phs = 0;  // kv_full parity of stage ss
+      const uint64_t aq = sdesc_sw128(sb + L.qr, 16, 1024);  // the q_rope half (A, K-major)
       for (int ns = 0; ns < ntiles && ok; ++ns) {
         if (!(ok = mbar_wait(bar(BAR_KV_FULL + ss), phs, abort_flag))) break;
         // score buffer ns&1 holds P of tile ns-2 until that tile's P.V has completed
@@ -337,21 +340,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads
         tc_fence_after();
         fence_proxy_async_smem();
-        const uint32_t stage = sb + L.kv + (uint32_t)ss * L.stage;
+        const uint64_t bd = sdesc_sw128(sb + L.kv + (uint32_t)ss * L.stage, 16, 1024);
+        const uint64_t bk = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64, 16, 1024);
         const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
+#pragma unroll
         for (int slab = 0; slab < 4; ++slab) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(stage + slab * kSlabKV + kk * 32, 16, 1024);
-            umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, bd, kIdescS, (slab | kk) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, sdesc_add(bd, slab * kSlabKV + kk * 32),
+                         kIdescS, (slab | kk) ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {  // the half k_r slab: 32 columns, 2 K-steps
-          const uint64_t ad = sdesc_sw128(sb + L.qr + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64 + kk * 32, 16, 1024);
-          umma_bf16(tS, ad, bd, kIdescS, 1u);
-        }
+        for (int kk = 0; kk < 2; ++kk)  // the half k_r slab: 32 columns, 2 K-steps
+          umma_bf16(tS, sdesc_add(aq, kk * 32), sdesc_add(bk, kk * 32), kIdescS, 1u);
         umma_commit(bar(BAR_S_FULL + (ns & 1)));
         if (++ss == NS) {
           ss = 0;
@@ -375,13 +376,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int np = 0; np < ntiles && ok; ++np) {
         if (!(ok = mbar_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t stage = sb + L.kv + (uint32_t)sp * L.stage;
+        const uint64_t bv = sdesc_sw128(sb + L.kv + (uint32_t)sp * L.stage, kSlabKV, 1024);
         const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = sdesc_sw128(stage + kk * 2048, kSlabKV, 1024);
-          umma_bf16_ts(tO, tP + 8u * kk, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts(tO, tP + 8u * kk, sdesc_add(bv, kk * 2048), kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(BAR_KV_EMPTY + sp));
         umma_commit(bar(BAR_PV_DONE + (np & 1)));
         if (++sp == NS) sp = 0;
@@ -396,23 +395,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ======================= softmax + epilogue (thread = query row) ===================
-    const int m = tid;
-    const bool warp_live = warp * 32 < Mv;       // this warp holds stored query rows
+    // Warps w and w + 4 share TMEM lane quadrant w & 3; `half` 0 takes keys 0-31 of every
+    // tile and O columns [0, 128) of this CTA's 256, half 1 keys 32-63 and columns [128, 256).
+    const int half = warp >> 2;
+    const int m = tid & (kBM - 1);
+    const int wq = warp & 3;
+    const bool warp_live = wq * 32 < Mv;       // this warp holds stored query rows
     const bool row_live = m < Mv;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + kTmemO + lane_base;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tO = tmem + kTmemO + lane_base + 128u * (uint32_t)half;
     const int pos_m = (m < rows_valid) ? ctx - a.n_q + q0 + m / a.H : pos_last;
     const int pos_first = ctx - a.n_q + q0;  // position of the tile's first query
-    float m_run = -INFINITY, l_run = 0.f;
-    // score exchange buffer, transposed ([16 float4][Mv rows]) so that consecutive rows
-    // are consecutive 16-byte words: conflict-free for both the peer's stores and our loads
+    float* half_max = reinterpret_cast<float*>(smem + kOffHalfMax);  // [2][128]
+    float* half_l = reinterpret_cast<float*>(smem + kOffHalfL);      // [2][128]
+    float m_run = -INFINITY, l_run = 0.f;  // m_run agrees in both halves; l_run is this half's
+    // score exchange buffer, transposed ([8 words][Mv rows], word = 8 fp16 scores; words 0-3
+    // hold keys 0-31, 4-7 keys 32-63) so that consecutive rows are consecutive 16-byte words:
+    // conflict-free for both the peer's stores and our loads
     const uint32_t rX = mapa_shared(sb + L.x, peer);
     const uint32_t rXfull = mapa_shared(bar(BAR_X_FULL), peer);
     const uint32_t rXempty = mapa_shared(bar(BAR_X_EMPTY), peer);
     const uint4* X = reinterpret_cast<const uint4*>(smem + L.x);
     bool ok = true;
-    // Q, this CTA's cKV columns, into TMEM: thread m stores row m's 256 columns as bf16 pairs
-    // (rows past the valid ones are zero; warps holding no stored rows leave their lanes)
+    // Q, this CTA's cKV columns, into TMEM: half h stores cKV slabs 2h, 2h + 1 of row m as
+    // bf16 pairs (rows past the valid ones are zero; warps holding no stored rows leave their
+    // lanes)
     if (ntiles > 0 && warp_live) {
       const bool valid = m < rows_valid;
       int64_t row = 0;
@@ -420,7 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_lat) +
                                                          row * kDLat + col0);
 #pragma unroll 1
-      for (int slab = 0; slab < 4; ++slab) {
+      for (int slab = 2 * half; slab < 2 * half + 2; ++slab) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -437,134 +444,154 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(BAR_Q_FULL));
-    for (int j = 0; j < ntiles && ok; ++j) {
+    // Every softmax warp runs every iteration up to the tile's barrier reduction, also after a
+    // failed wait (it then skips its work): the reduction tells all 256 threads of a failure,
+    // and they leave the loop together, so no warp is left waiting at a named barrier.
+    for (int j = 0; j < ntiles; ++j) {
       const int s = j & 1;
-      const int T = (kb + j) * kBN;
-      float sv[kBN];
-      if (!(ok = warp_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, abort_flag))) break;
-      tc_fence_after();
-      if (warp_live) {
-        uint32_t r[32];
-        tmem_ld32(tmem + kTmemS + 64u * (uint32_t)s + lane_base, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-        tmem_ld32(tmem + kTmemS + 64u * (uint32_t)s + 32u + lane_base, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
-      }
-
-      // exchange partial scores with the peer (each side owns part of the contraction)
-      if (j >= 1 && !(ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag))) break;
-      if (m == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
-      if (row_live) {
-        // own partial rounded to fp16 exactly as the peer receives it, packed 8 per 16 bytes
-#pragma unroll
-        for (int i = 0; i < kBN / 8; ++i) {
-          uint4 w;
-          __half2 h;
-          h = __floats2half2_rn(sv[8 * i], sv[8 * i + 1]);
-          w.x = *reinterpret_cast<uint32_t*>(&h);
-          h = __floats2half2_rn(sv[8 * i + 2], sv[8 * i + 3]);
-          w.y = *reinterpret_cast<uint32_t*>(&h);
-          h = __floats2half2_rn(sv[8 * i + 4], sv[8 * i + 5]);
-          w.z = *reinterpret_cast<uint32_t*>(&h);
-          h = __floats2half2_rn(sv[8 * i + 6], sv[8 * i + 7]);
-          w.w = *reinterpret_cast<uint32_t*>(&h);
-          st_async_v4_b32(rX + (uint32_t)(i * Mv + m) * 16u, w, rXfull);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
-            sv[8 * i + 2 * k] = f.x;
-            sv[8 * i + 2 * k + 1] = f.y;
-          }
-        }
-      }
-      if (!(ok = warp_wait_cluster(bar(BAR_X_FULL), j & 1, abort_flag))) break;
-      if (row_live) {
-#pragma unroll
-        for (int i = 0; i < kBN / 8; ++i) {
-          const uint4 v = X[i * Mv + m];
-          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
-            sv[8 * i + 2 * k] += f.x;
-            sv[8 * i + 2 * k + 1] += f.y;
-          }
-        }
-      }
-      __syncwarp();
-      // this warp is done with the peer's scores (the values are in registers and used, so a
-      // relaxed arrive suffices; a release would stall on this lane's outstanding st.async)
-      if (lane == 0) mbar_arrive_remote_relaxed(rXempty);
-
-      bool want = false;
-      float mx = -INFINITY;
-      if (row_live) {
-        // causal mask t <= pos_m, only on tiles that reach past the tile's first query
-        if (T + kBN - 1 > pos_first) {
-#pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (T + i > pos_m) sv[i] = -INFINITY;
-        }
-        // row max as a tree (scale > 0, so max(s) * scale = max(s * scale))
-        float t32[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) t32[i] = fmaxf(sv[i], sv[i + 32]);
-#pragma unroll
-        for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) t32[i] = fmaxf(t32[i], t32[i + w]);
-        mx = t32[0] * a.scale_log2;  // log2 units
-        // The running max only moves when it grows by more than 2^8: P stays <= 256 and O
-        // is rescaled rarely (the final 1/l uses the same max, so the result is exact).
-        want = (m < rows_valid) && (mx > m_run + 8.f);
-      }
-      const float corr = want ? fast_exp2(m_run - mx) : 1.f;
-      if (j > 0 && __any_sync(FULL, want)) {
-        if (!(ok = warp_wait(bar(BAR_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag))) break;
+      const int T = (kb + j) * kBN + 32 * half;  // position of this half's first key
+      float sv[32];
+      if (ok) ok = warp_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, abort_flag);
+      if (ok) {
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        if (warp_live) {
           uint32_t r[32];
-          tmem_ld32(tO + c, r);
+          tmem_ld32(tmem + kTmemS + 64u * (uint32_t)s + 32u * (uint32_t)half + lane_base, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-          tmem_st32(tO + c, r);
+          for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
         }
-        tmem_st_wait();
+        // exchange partial scores with the peer (each side owns part of the contraction)
+        if (j >= 1) ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag);
+      }
+      if (ok) {
+        if (m == 0 && half == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
+        if (row_live) {
+          // own partial rounded to fp16 exactly as the peer receives it, packed 8 per 16 bytes
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            __half2 h;
+            h = __floats2half2_rn(sv[8 * i], sv[8 * i + 1]);
+            w.x = *reinterpret_cast<uint32_t*>(&h);
+            h = __floats2half2_rn(sv[8 * i + 2], sv[8 * i + 3]);
+            w.y = *reinterpret_cast<uint32_t*>(&h);
+            h = __floats2half2_rn(sv[8 * i + 4], sv[8 * i + 5]);
+            w.z = *reinterpret_cast<uint32_t*>(&h);
+            h = __floats2half2_rn(sv[8 * i + 6], sv[8 * i + 7]);
+            w.w = *reinterpret_cast<uint32_t*>(&h);
+            st_async_v4_b32(rX + (uint32_t)((4 * half + i) * Mv + m) * 16u, w, rXfull);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+              sv[8 * i + 2 * k] = f.x;
+              sv[8 * i + 2 * k + 1] = f.y;
+            }
+          }
+        }
+        ok = warp_wait_cluster(bar(BAR_X_FULL), j & 1, abort_flag);
+      }
+      float lmx = -INFINITY;
+      bool need = false;
+      if (ok) {
+        if (row_live) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = X[(4 * half + i) * Mv + m];
+            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
+              sv[8 * i + 2 * k] += f.x;
+              sv[8 * i + 2 * k + 1] += f.y;
+            }
+          }
+        }
+        __syncwarp();
+        // this warp is done with the peer's scores (the values are in registers and used, so
+        // a relaxed arrive suffices; a release would stall on this lane's outstanding st.async)
+        if (lane == 0) mbar_arrive_remote_relaxed(rXempty);
+        if (row_live) {
+          // causal mask t <= pos_m, only on tiles that reach past the tile's first query
+          if (T + 31 > pos_first) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (T + i > pos_m) sv[i] = -INFINITY;
+          }
+          // this half's row max, three-input max tree (scale > 0, so max(s) * scale =
+          // max(s * scale))
+          float t[11];
+#pragma unroll
+          for (int i = 0; i < 10; ++i) t[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          t[10] = fmaxf(sv[30], sv[31]);
+          const float u0 = fmax3(t[0], t[1], t[2]), u1 = fmax3(t[3], t[4], t[5]);
+          const float u2 = fmax3(t[6], t[7], t[8]), u3 = fmaxf(t[9], t[10]);
+          lmx = fmaxf(fmax3(u0, u1, u2), u3) * a.scale_log2;  // log2 units
+          // The running max only moves when it grows by more than 2^8: P stays <= 256 and O
+          // is rescaled rarely (the final 1/l uses the same max, so the result is exact).
+          need = (m < rows_valid) && (lmx > m_run + 8.f);
+        }
+      }
+      // One reduction per tile over both halves (and a fence pair around it): it orders both
+      // halves' reads of the score buffer before either writes P over it, and flags the rare
+      // tile where a row's max moves or a wait failed.
+      tc_fence_before();
+      if (named_bar_red_or(kBarSmRed, kSoftmaxThreads, need || !ok)) {
+        half_max[half * kBM + m] = lmx;
+        if (named_bar_red_or(kBarSmRed2, kSoftmaxThreads, !ok)) {
+          ok = false;
+          break;
+        }
+        lmx = fmaxf(lmx, half_max[(half ^ 1) * kBM + m]);  // the row's max over both halves
+      }
+      tc_fence_after();
+      const bool want = (m < rows_valid) && (lmx > m_run + 8.f);  // same in both halves
+      const float corr = want ? fast_exp2(m_run - lmx) : 1.f;
+      if (j > 0 && __any_sync(FULL, want)) {
+        // rescale this half's O columns once the previous tile's P.V is complete
+        if (warp_wait(bar(BAR_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+            tmem_st32(tO + c, r);
+          }
+          tmem_st_wait();
+        } else {
+          ok = false;  // reported at the next tile's reduction (or after the loop)
+        }
       }
       if (want) {
         l_run *= corr;
-        m_run = mx;
+        m_run = lmx;
       }
-      uint32_t pk[kBN / 2];
+      uint32_t pk[16];
       if (row_live) {
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         const float c = a.scale_log2;
-        float part[8];
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i] = 0.f;
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
+        for (int i = 0; i < 32; i += 2) {
           const float p0 = fast_exp2(fmaf(sv[i], c, -m_use));
           const float p1 = fast_exp2(fmaf(sv[i + 1], c, -m_use));
-          part[(i >> 1) & 7] += p0 + p1;
+          part[(i >> 1) & 3] += p0 + p1;
           const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
           pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        l_run += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+        l_run += (part[0] + part[1]) + (part[2] + part[3]);
       } else {
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) pk[i] = 0u;
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
       }
-      // P over the first 32 columns of the score buffer just read (bf16 pairs)
+      // P over the first 32 columns of the score buffer just read (bf16 pairs): this half's
+      // 32 keys are columns 16 * half .. 16 * half + 15
       if (warp_live) {
-        tmem_st32(tmem + kTmemS + 64u * (uint32_t)s + lane_base, pk);
+        tmem_st16(tmem + kTmemS + 64u * (uint32_t)s + 16u * (uint32_t)half + lane_base, pk);
         tmem_st_wait();
       }
       tc_fence_before();
@@ -578,16 +605,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       set_status(a.status, kDevErrTimeout);
     }
     tc_fence_after();
-    // ---- epilogue: O / l for this CTA's 256 columns ------------------------------------
+    // the row's sum over both halves
+    half_l[half * kBM + m] = l_run;
+    named_bar_sync(kBarSmRed2, kSoftmaxThreads);
+    const float l_tot = l_run + half_l[(half ^ 1) * kBM + m];
+    // ---- epilogue: O / l for this half's 128 of the CTA's 256 columns -------------------
     if (warp_live) {
-      const bool have = ntiles > 0 && ok && l_run > 0.f;
-      const float inv_l = have ? 1.f / l_run : 0.f;
-      const float lse_v = have ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      const bool have = ntiles > 0 && ok && l_tot > 0.f;
+      const float inv_l = have ? 1.f / l_tot : 0.f;
+      const float lse_v = have ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
       const bool write_row = m < rows_valid;
       const int qi = q0 + (write_row ? m / a.H : 0), hh = write_row ? m % a.H : 0;
       const int64_t orow = ((int64_t)b * a.n_q + qi) * a.H + hh;
       const int64_t prow = ((int64_t)b * a.n_qtiles * a.S + unit) * kBM + m;
-      for (int c = 0; c < 256; c += 32) {
+      const int cbase = col0 + 128 * half;
+      for (int c = 0; c < 128; c += 32) {
         uint32_t r[32];
         if (ntiles > 0) {
           tmem_ld32(tO + c, r);  // warp-collective: every lane executes it
@@ -599,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!write_row) continue;
         if (a.S == 1) {
           uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat +
-                                              col0 + c);
+                                              cbase + c);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
@@ -614,12 +646,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             o[q] = w;
           }
         } else {
-          float4* o = reinterpret_cast<float4*>(a.opart + prow * kDLat + col0 + c);
+          float4* o = reinterpret_cast<float4*>(a.opart + prow * kDLat + cbase + c);
 #pragma unroll
           for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
-      if (write_row) {
+      if (write_row && half == 0) {
         if (a.S == 1) {
           if (a.lse != nullptr && rank == 0) a.lse[orow] = lse_v;
         } else {
@@ -632,8 +664,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // partials of its 256 columns after teardown (threadfence-reduction pattern; the
       // counter resets itself, so the workspace stays reusable).
       __threadfence();
-      named_bar_sync(1, kSoftmaxWarps * 32);
-      if (m == 0) {
+      named_bar_sync(kBarSmMerge, kSoftmaxThreads);
+      if (tid == 0) {
         int* cnt = a.counters + ((int64_t)b * a.n_qtiles + qtile) * 2 + rank;
         last_sh = (atomicAdd(cnt, 1) == a.S - 1) ? 1 : 0;
       }

@@ -156,6 +156,27 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
   return __all_sync(kFullMask, ok);
 }
 
+// Element-wise round_f32(a + b) of two fp16 pairs (low halves first), with the mixed-precision
+// add of sm_100 and later: the first add widens b exactly, the second rounds once.  The result
+// does not depend on which pair is a and which is b.
+__device__ __forceinline__ float2 add_f16x2_f16x2_f32(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n .reg .f16 a0, a1, b0, b1;\n .reg .f32 t0, t1;\n"
+      " mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+      " add.rn.f32.f16 t0, b0, 0f00000000;\n add.rn.f32.f16 t1, b1, 0f00000000;\n"
+      " add.rn.f32.f16 %0, a0, t0;\n add.rn.f32.f16 %1, a1, t1;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
+}
+
+// max(a, b, c) in one instruction (three-input form of max.f32 on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

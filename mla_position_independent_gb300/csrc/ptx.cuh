@@ -186,6 +186,13 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// 16-byte store into this CTA's shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 // 16-byte store into a peer CTA's shared memory; completion is counted in bytes on the
 // peer's mbarrier (complete_tx).
 __device__ __forceinline__ void st_async_v4_b32(uint32_t cluster_addr, uint4 v, uint32_t cluster_bar) {
@@ -239,6 +246,13 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// A descriptor advanced by `bytes` (a multiple of 16): the start address sits in bits 0-13 in
+// 16-byte units, and shared-memory addresses stay below 256 KiB, so the add never carries out
+// of that field.  Lets an issuing thread build one descriptor per tile and step it by constants.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
