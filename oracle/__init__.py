@@ -14,6 +14,8 @@ Functions and the passages they follow:
   rope_theta   NeoX frequencies theta_j = 10000^(-2j/64)   (convention fixed for this build;
                the pages warn the rotary class must match the model, [walkthrough §11])
   rotate       R(steps) on 64-d rows                        [walkthrough §4, §15]
+               (rope=(theta[32], pairing) selects a RoPE variant: any frequency table, NeoX
+               half split (pairing 0) or interleaved pairs (pairing 1) [walkthrough §11])
   plan         chunk table -> per-row src_row, delta, pos_src [walkthrough §5 pseudo-code]
   assemble     [cKV | R(delta) k_r] in fp64                 [walkthrough §4], [summary §2.2]
   attn         absorbed MLA softmax attention in fp64       [walkthrough §4]
@@ -64,6 +66,8 @@ def _load():
             I = ctypes.c_int64
             lib.oracle_rope_theta.argtypes = [P]
             lib.oracle_rotate.argtypes = [P, I, P, P]
+            lib.oracle_rotate_ex.argtypes = [P, I, P, P, ctypes.c_int, P]
+            lib.oracle_assemble_ex.argtypes = [P, I, P, P, P, ctypes.c_int, P]
             lib.oracle_plan.argtypes = [I, P, P, P, P, P, P, P, P, P, P]
             lib.oracle_plan.restype = ctypes.c_int
             lib.oracle_assemble.argtypes = [P, I, P, P, P]
@@ -92,12 +96,27 @@ def rope_theta() -> np.ndarray:
     return out
 
 
-def rotate(k, steps) -> np.ndarray:
-    """R(steps[r]) k[r] for rows of 64 values (fp64)."""
+def _rope(rope):
+    """(theta[32] fp64, pairing) of a RoPE spec; None is the default convention."""
+    if rope is None:
+        return None
+    theta, pairing = rope
+    theta = _c(np.asarray(theta, np.float64).reshape(32), np.float64)
+    if int(pairing) not in (0, 1):
+        raise ValueError("pairing must be 0 (NeoX half split) or 1 (interleaved)")
+    return theta, int(pairing)
+
+
+def rotate(k, steps, rope=None) -> np.ndarray:
+    """R(steps[r]) k[r] for rows of 64 values (fp64); rope=(theta[32], pairing) or None."""
     k = _c(np.atleast_2d(k), np.float64)
     steps = _c(np.broadcast_to(np.asarray(steps, np.int64), (k.shape[0],)), np.int64)
     out = np.empty_like(k)
-    _load().oracle_rotate(_p(k), k.shape[0], _p(steps), _p(out))
+    rp = _rope(rope)
+    if rp is None:
+        _load().oracle_rotate(_p(k), k.shape[0], _p(steps), _p(out))
+    else:
+        _load().oracle_rotate_ex(_p(k), k.shape[0], _p(steps), _p(rp[0]), rp[1], _p(out))
     return out
 
 
@@ -140,7 +159,7 @@ def plan(chunks, indptr):
                 pos_src=pss[:total])
 
 
-def assemble(kv_rows_bits, src_row, delta) -> np.ndarray:
+def assemble(kv_rows_bits, src_row, delta, rope=None) -> np.ndarray:
     """fp64 [n, 576] rows [cKV | R(delta) k_r] gathered from the bf16 row store."""
     kv = kv_rows_bits
     assert kv.dtype == np.uint16 and kv.ndim == 2 and kv.shape[1] == D_ROW
@@ -150,7 +169,12 @@ def assemble(kv_rows_bits, src_row, delta) -> np.ndarray:
     if src_row.size and (src_row.min() < 0 or src_row.max() >= kv.shape[0]):
         raise ValueError("source row outside the row store")
     out = np.empty((src_row.shape[0], D_ROW), np.float64)
-    _load().oracle_assemble(_p(kv), src_row.shape[0], _p(src_row), _p(delta), _p(out))
+    rp = _rope(rope)
+    if rp is None:
+        _load().oracle_assemble(_p(kv), src_row.shape[0], _p(src_row), _p(delta), _p(out))
+    else:
+        _load().oracle_assemble_ex(_p(kv), src_row.shape[0], _p(src_row), _p(delta), _p(rp[0]),
+                                   rp[1], _p(out))
     return out
 
 
@@ -171,7 +195,8 @@ def attn(q, visible, K, scale):
     return O, lse
 
 
-def mla_attention(q_lat_bits, q_rope_bits, chunks, indptr, kv_rows_bits, scale, select=None):
+def mla_attention(q_lat_bits, q_rope_bits, chunks, indptr, kv_rows_bits, scale, select=None,
+                  rope=None):
     """fp64 MLA attention of a batch, following the reuse-time reconstruction.
 
     q_lat_bits [B, n_q, H, 512] and q_rope_bits [B, n_q, H, 64] are bf16 bit patterns;
@@ -192,7 +217,7 @@ def mla_attention(q_lat_bits, q_rope_bits, chunks, indptr, kv_rows_bits, scale, 
         rows = np.nonzero(sel[:, 0] == b)[0]
         r0, r1 = pl["row_start"][b], pl["row_start"][b + 1]
         ctx = int(r1 - r0)
-        K = assemble(kv_rows_bits, pl["src_row"][r0:r1], pl["delta"][r0:r1])
+        K = assemble(kv_rows_bits, pl["src_row"][r0:r1], pl["delta"][r0:r1], rope)
         ii, hh = sel[rows, 1], sel[rows, 2]
         q = np.concatenate([widen(q_lat_bits[b, ii, hh]), widen(q_rope_bits[b, ii, hh])], axis=1)
         visible = ctx - n_q + ii + 1
@@ -202,7 +227,7 @@ def mla_attention(q_lat_bits, q_rope_bits, chunks, indptr, kv_rows_bits, scale, 
     return O, lse
 
 
-def rotate_gather(kv_rows_bits, chunks, indptr, page_table, rows=None):
+def rotate_gather(kv_rows_bits, chunks, indptr, page_table, rows=None, rope=None):
     """Expected paged rows of the standalone rotate+gather path.
 
     Target row t of request b lands in slot page_table[b, t // 64] * 64 + t % 64 with value
@@ -219,5 +244,5 @@ def rotate_gather(kv_rows_bits, chunks, indptr, page_table, rows=None):
         b_of, t_of = rows[:, 0], rows[:, 1]
     flat = pl["row_start"][b_of] + t_of
     slot = page_table[b_of, t_of // 64].astype(np.int64) * 64 + t_of % 64
-    vals = assemble(kv_rows_bits, pl["src_row"][flat], pl["delta"][flat])
+    vals = assemble(kv_rows_bits, pl["src_row"][flat], pl["delta"][flat], rope)
     return slot, vals

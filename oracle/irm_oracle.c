@@ -27,8 +27,13 @@
  *   - absorbed MLA attention: scores use [cKV | k_r] against [q_lat | q_rope], the output
  *     is the softmax-weighted sum of cKV (W_UV applied outside)          [walkthrough §4]
  * Readings where the pages are silent (each is also listed in the design notes):
- *   - RoPE convention: NeoX half split, pair j couples dims (j, j+32), frequency
+ *   - default RoPE convention: NeoX half split, pair j couples dims (j, j+32), frequency
  *     theta_j = 10000^(-2j/64), j = 0..31; R(p) turns pair j by angle +p*theta_j.
+ *   - RoPE variants [walkthrough §11: the rotary class and inv_freq must match the model]:
+ *     the *_ex functions take the 32 frequencies theta_j (radians per position) and the
+ *     pairing (0: NeoX half split, pair j = dims (j, j+32); 1: interleaved, pair j = dims
+ *     (2j, 2j+1)).  Attention scaling does not enter R(delta): the cached k_r already
+ *     carries it and R(delta) only turns pairs.
  *   - a fresh row (reused = 0) has delta = 0 and is passed through unchanged.
  *   - softmax scale is a caller argument (1/sqrt(192) for the configurations used here).
  *   - query i of n_q sits at position ctx - n_q + i and sees keys t <= that position.
@@ -62,23 +67,43 @@ void oracle_rope_theta(double *theta) {
   for (int j = 0; j < N_PAIRS; ++j) theta[j] = pow(10000.0, -2.0 * (double)j / (double)D_ROPE);
 }
 
-/* R(angle_scale) applied to one 64-d row: pair j = (x_j, x_{j+32}) is turned by
- * angle_scale * theta_j.  Used both for R(delta) [walkthrough §4] and for R(p). */
-static void rotate_row(const double *k, i64 steps, const double *theta, double *out) {
-  for (int j = 0; j < N_PAIRS; ++j) {
-    double ang = (double)steps * theta[j];
-    double c = cos(ang), s = sin(ang);
-    double x = k[j], y = k[j + N_PAIRS];
-    out[j] = x * c - y * s;
-    out[j + N_PAIRS] = x * s + y * c;
+/* The two dims of pair j: NeoX half split (j, j+32) or interleaved (2j, 2j+1). */
+static void pair_dims(int pairing, int j, int *dx, int *dy) {
+  if (pairing == 1) {
+    *dx = 2 * j;
+    *dy = 2 * j + 1;
+  } else {
+    *dx = j;
+    *dy = j + N_PAIRS;
   }
 }
 
-/* out[r] = R(steps[r]) k[r] for n rows of 64 values. */
+/* R(steps) applied to one 64-d row: pair j = (x, y) is turned by angle steps * theta_j,
+ * (x, y) -> (x cos - y sin, x sin + y cos).  Used both for R(delta) [walkthrough §4] and
+ * for R(p). */
+static void rotate_row(const double *k, i64 steps, const double *theta, int pairing, double *out) {
+  for (int j = 0; j < N_PAIRS; ++j) {
+    int dx, dy;
+    pair_dims(pairing, j, &dx, &dy);
+    double ang = (double)steps * theta[j];
+    double c = cos(ang), s = sin(ang);
+    double x = k[dx], y = k[dy];
+    out[dx] = x * c - y * s;
+    out[dy] = x * s + y * c;
+  }
+}
+
+/* out[r] = R(steps[r]) k[r] for n rows of 64 values, with an explicit RoPE spec. */
+void oracle_rotate_ex(const double *k, i64 n, const i64 *steps, const double *theta, int pairing,
+                      double *out) {
+  for (i64 r = 0; r < n; ++r) rotate_row(k + r * D_ROPE, steps[r], theta, pairing, out + r * D_ROPE);
+}
+
+/* Same with the default convention. */
 void oracle_rotate(const double *k, i64 n, const i64 *steps, double *out) {
   double theta[N_PAIRS];
   oracle_rope_theta(theta);
-  for (i64 r = 0; r < n; ++r) rotate_row(k + r * D_ROPE, steps[r], theta, out + r * D_ROPE);
+  oracle_rotate_ex(k, n, steps, theta, 0, out);
 }
 
 /*
@@ -119,11 +144,10 @@ int oracle_plan(i64 B, const i64 *indptr, const i64 *pool_offset, const i64 *len
 /*
  * Assembled KV rows in fp64: out[r] = [cKV(src_row[r]) | R(delta[r]) k_r(src_row[r])].
  * kv_rows is the bf16 row store [n_rows, 576]; cKV is only widened, never modified.
+ * RoPE spec as in oracle_rotate_ex.
  */
-void oracle_assemble(const uint16_t *kv_rows, i64 n, const i64 *src_row, const i64 *delta,
-                     double *out) {
-  double theta[N_PAIRS];
-  oracle_rope_theta(theta);
+void oracle_assemble_ex(const uint16_t *kv_rows, i64 n, const i64 *src_row, const i64 *delta,
+                        const double *theta, int pairing, double *out) {
 #pragma omp parallel for schedule(static)
   for (i64 r = 0; r < n; ++r) {
     const uint16_t *src = kv_rows + src_row[r] * D_ROW;
@@ -134,9 +158,17 @@ void oracle_assemble(const uint16_t *kv_rows, i64 n, const i64 *src_row, const i
     if (delta[r] == 0) {
       for (int d = 0; d < D_ROPE; ++d) dst[D_LAT + d] = kr[d];
     } else {
-      rotate_row(kr, delta[r], theta, dst + D_LAT);
+      rotate_row(kr, delta[r], theta, pairing, dst + D_LAT);
     }
   }
+}
+
+/* Same with the default convention. */
+void oracle_assemble(const uint16_t *kv_rows, i64 n, const i64 *src_row, const i64 *delta,
+                     double *out) {
+  double theta[N_PAIRS];
+  oracle_rope_theta(theta);
+  oracle_assemble_ex(kv_rows, n, src_row, delta, theta, 0, out);
 }
 
 /*

@@ -351,6 +351,121 @@ def test_rotate_gather_slots(oracle_mod):
     np.testing.assert_array_equal(vals, oracle_mod.assemble(kv, pl["src_row"], pl["delta"]))
 
 
+# --------------------------------------------------------------------------- RoPE variants
+# Walkthrough §11: the delta-rotation must use the model's own rotary class and inv_freq
+# (a plain base-10000 fallback made reuse collapse in the pages' TransMLA case study).  The
+# oracle takes the spec as (theta[32] radians per position, pairing: 0 NeoX, 1 interleaved).
+
+def rope_tables():
+    """Frequency tables used as inputs by the variant tests (model configurations, not
+    method arithmetic): the default base 10000, a plain base 500000, and a YaRN-like table
+    whose low-frequency pairs are slowed down by up to 40x with a linear ramp."""
+    j = np.arange(32)
+    base10k = 10000.0 ** (-2.0 * j / 64.0)
+    base500k = 500000.0 ** (-2.0 * j / 64.0)
+    ramp = np.clip((j - 16) / 8.0, 0.0, 1.0)
+    yarn = base10k / (1.0 + 39.0 * ramp)
+    return {"base10k": base10k, "base500k": base500k, "yarn": yarn}
+
+
+def test_rope_table_of_default_is_the_default(oracle_mod):
+    """The spec path with the default table and NeoX pairing is the default rotation, bit
+    for bit; the test's base-10000 table is that table to the last ulp."""
+    rng = np.random.default_rng(31)
+    k = rng.standard_normal((16, 64))
+    d = rng.integers(-70000, 70000, 16)
+    np.testing.assert_array_equal(oracle_mod.rotate(k, d, rope=(oracle_mod.rope_theta(), 0)),
+                                  oracle_mod.rotate(k, d))
+    np.testing.assert_allclose(rope_tables()["base10k"], oracle_mod.rope_theta(), rtol=2.3e-16)
+
+
+@pytest.mark.parametrize("name", ["base10k", "base500k", "yarn"])
+def test_interleaved_is_neox_on_even_odd_split(oracle_mod, name):
+    """Interleaved pairs (2j, 2j+1) are the NeoX pairs (j, j+32) of the vector whose first
+    half holds the even dims and second half the odd dims: R_int = P^T R_neox P."""
+    th = rope_tables()[name]
+    rng = np.random.default_rng(32)
+    k = rng.standard_normal((12, 64))
+    d = rng.integers(-5000, 5000, 12)
+    perm = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2)])
+    via_neox = np.empty_like(k)
+    via_neox[:, perm] = oracle_mod.rotate(k[:, perm], d, rope=(th, 0))
+    np.testing.assert_array_equal(oracle_mod.rotate(k, d, rope=(th, 1)), via_neox)
+
+
+def test_interleaved_pairs_and_angles(oracle_mod):
+    """Pairing 1: pair j moves only dims 2j, 2j+1, turned by delta * theta_j."""
+    th = rope_tables()["yarn"]
+    for j in (0, 5, 16, 20, 31):
+        k = np.zeros(64)
+        k[2 * j], k[2 * j + 1] = 0.6, -0.8
+        for delta in (1, -3, 250, 40000):
+            r = oracle_mod.rotate(k, delta, rope=(th, 1))[0]
+            assert np.all(np.delete(r, [2 * j, 2 * j + 1]) == 0.0)
+            turned = (math.atan2(r[2 * j + 1], r[2 * j]) - math.atan2(k[2 * j + 1], k[2 * j])) % (2 * math.pi)
+            expect = (delta * th[j]) % (2 * math.pi)
+            assert min(abs(turned - expect), 2 * math.pi - abs(turned - expect)) < 1e-10
+
+
+@pytest.mark.parametrize("pairing", [0, 1])
+@pytest.mark.parametrize("name", ["base500k", "yarn"])
+def test_variant_composition_identity_and_norm(oracle_mod, name, pairing):
+    """R(delta) R(p_src) = R(p_tgt) for any frequency table and pairing; delta = 0 is the
+    identity and R preserves the norm."""
+    rope = (rope_tables()[name], pairing)
+    rng = np.random.default_rng(33)
+    k = rng.standard_normal((128, 64))
+    ps = rng.integers(0, 4096, 128)
+    d = rng.integers(-4096, 4096, 128)
+    lhs = oracle_mod.rotate(oracle_mod.rotate(k, ps, rope=rope), d, rope=rope)
+    # each angle p * theta_j (|angle| <= 8192 rad) carries fp64 rounding of up to 2^-53
+    # relative, i.e. <= 9.1e-13 rad, and three such angles enter the comparison
+    assert np.max(np.abs(lhs - oracle_mod.rotate(k, ps + d, rope=rope))) < 4e-12
+    np.testing.assert_array_equal(oracle_mod.rotate(k, 0, rope=rope), k)
+    r = oracle_mod.rotate(k, d, rope=rope)
+    np.testing.assert_allclose(np.linalg.norm(r, axis=1), np.linalg.norm(k, axis=1), rtol=1e-14)
+
+
+def test_wrong_rotary_class_breaks_reuse(oracle_mod):
+    """Walkthrough §11: keys cached under the model's rotary class (here interleaved pairs
+    with a YaRN-like table) are moved correctly only by the same class; the default class
+    (NeoX, base 10000) moves them somewhere else and changes the attention output."""
+    rng = np.random.default_rng(34)
+    content = rng.standard_normal((96, 64))
+    p_src = 700 + np.arange(96)
+    p_tgt = 3100 + np.arange(96)
+    model = (rope_tables()["yarn"], 1)
+    cached = oracle_mod.rotate(content, p_src, rope=model)
+    fresh = oracle_mod.rotate(content, p_tgt, rope=model)
+    right = oracle_mod.rotate(cached, p_tgt - p_src, rope=model)
+    wrong = oracle_mod.rotate(cached, p_tgt - p_src)
+    assert np.max(np.abs(right - fresh)) < 1e-11
+    assert np.linalg.norm(wrong - fresh) / np.linalg.norm(fresh) > 0.5
+    K = np.concatenate([rng.standard_normal((96, 512)), fresh], 1)
+    q = rng.standard_normal((4, 576))
+    O_ref, _ = oracle_mod.attn(q, 96, K, 1.0 / 8)
+    K_right, K_wrong = K.copy(), K.copy()
+    K_right[:, 512:], K_wrong[:, 512:] = right, wrong
+    assert np.max(np.abs(oracle_mod.attn(q, 96, K_right, 1.0 / 8)[0] - O_ref)) < 1e-10
+    assert np.max(np.abs(oracle_mod.attn(q, 96, K_wrong, 1.0 / 8)[0] - O_ref)) > 1e-2
+
+
+def test_assemble_and_gather_follow_the_rope_spec(oracle_mod):
+    """assemble / rotate_gather apply the spec they are given to exactly the rows rotate
+    would, and leave cKV untouched."""
+    case = synth.custom_case([[(0, 32, 0, 0), (64, 70, 9, 1), (300, 40, 5000, 1)]], n_rows=600,
+                             n_q=0, pages=True)
+    kv = synth.bits(case.kv_rows)
+    rope = (rope_tables()["yarn"], 1)
+    pl = oracle_mod.plan(case.chunks, case.indptr)
+    K = oracle_mod.assemble(kv, pl["src_row"], pl["delta"], rope)
+    np.testing.assert_array_equal(K[:, :512], oracle_mod.widen(kv[pl["src_row"], :512]))
+    kr = oracle_mod.widen(kv[pl["src_row"], 512:])
+    np.testing.assert_array_equal(K[:, 512:], oracle_mod.rotate(kr, pl["delta"], rope=rope))
+    slot, vals = oracle_mod.rotate_gather(kv, case.chunks, case.indptr, case.page_table, rope=rope)
+    np.testing.assert_array_equal(vals, K)
+
+
 # --------------------------------------------------------------------------- planted mistakes
 
 def _theta():
@@ -387,3 +502,33 @@ def test_pins_catch_planted_rotation_mistakes(oracle_mod, mode):
     np.testing.assert_allclose(good, oracle_mod.rotate(k, 250), atol=1e-12)
     bad = _rotate_variant(k, 250, mode)
     assert np.max(np.abs(bad - oracle_mod.rotate(k, 250))) > 1e-3
+
+
+def _rotate_interleaved_variant(k, steps, theta, mode):
+    """A CPU copy of the interleaved rotation with one planted mistake."""
+    k = np.atleast_2d(k).astype(np.float64)
+    steps = np.broadcast_to(np.asarray(steps), (k.shape[0],))
+    th = theta[::-1] if mode == "freq_order" else theta
+    ang = steps[:, None] * th[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    if mode == "sign":
+        s = -s
+    if mode == "neox":
+        x, y = k[:, :32], k[:, 32:]
+        return np.concatenate([x * c - y * s, x * s + y * c], 1)
+    x, y = k[:, 0::2], k[:, 1::2]
+    out = np.empty_like(k)
+    out[:, 0::2], out[:, 1::2] = x * c - y * s, x * s + y * c
+    return out
+
+
+@pytest.mark.parametrize("mode", ["sign", "freq_order", "neox"])
+def test_variant_pins_catch_planted_mistakes(oracle_mod, mode):
+    """The unplanted copy matches the oracle's interleaved YaRN-like rotation; each planted
+    mistake (sign, frequency order, pairing) does not."""
+    th = rope_tables()["yarn"]
+    rng = np.random.default_rng(35)
+    k = rng.standard_normal((8, 64))
+    ref = oracle_mod.rotate(k, 777, rope=(th, 1))
+    np.testing.assert_allclose(_rotate_interleaved_variant(k, 777, th, "none"), ref, atol=1e-12)
+    assert np.max(np.abs(_rotate_interleaved_variant(k, 777, th, mode) - ref)) > 1e-3
