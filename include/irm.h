@@ -13,9 +13,10 @@
  *   LLM Serving" (gist.science technical summary) §2.1-2.2.
  *
  * Conventions fixed here where the pages are silent:
- *   - RoPE is the NeoX half split: pair j couples k_r[j] and k_r[j+32] and turns by
- *     angle delta * theta_j, theta_j = 10000^(-2j/64), j = 0..31.  Rotation math is fp32,
- *     the rotated k_r is rounded to bf16 (round to nearest even) once.
+ *   - The default RoPE is the NeoX half split: pair j couples k_r[j] and k_r[j+32] and
+ *     turns by angle delta * theta_j, theta_j = 10000^(-2j/64), j = 0..31.  The *_rope entry
+ *     points take the model's own frequencies and pairing instead (irm_rope).  Rotation
+ *     math is fp32, the rotated k_r is rounded to bf16 (round to nearest even) once.
  *   - A fresh chunk (reused = 0) has delta = 0; its p_src is ignored.
  *   - Query i of n_q sits at position ctx - n_q + i and sees keys t <= that position.
  *
@@ -83,6 +84,30 @@ typedef struct irm_chunk {
   uint8_t pad[3];
 } irm_chunk;
 
+/*
+ * RoPE variant of the cached k_r slice.  The delta-rotation is only right when it uses the
+ * model's own rotary class: the same inv_freq table and pairing as the prefill that wrote
+ * the cache ["Irminsul论文详解" §11: with a plain base-10000 fallback instead of the model's
+ * rotary class, reuse was worse than naive reuse].
+ *   inv_freq[j]  theta_j, the angle per position of pair j in radians (any finite value;
+ *                base-b RoPE has theta_j = b^(-2j/64); scaled tables such as YaRN's are
+ *                passed as they are)
+ *   pairing      IRM_ROPE_NEOX: pair j = dims (j, j+32) of k_r;
+ *                IRM_ROPE_INTERLEAVED: pair j = dims (2j, 2j+1)
+ * A RoPE attention scaling factor does not enter the delta-rotation: it is already part of
+ * the cached k_r, and R(delta) only turns pairs.  The host turns theta_j into a 64-bit
+ * fixed-point phase step (one turn = 2^64, theta_j / 2pi rounded in fp64), and the kernels
+ * reduce delta * step to one turn exactly in integer arithmetic for every int32 delta.
+ * Passing NULL selects the default convention above.
+ */
+#define IRM_ROPE_NEOX 0
+#define IRM_ROPE_INTERLEAVED 1
+typedef struct irm_rope {
+  double inv_freq[32];
+  int32_t pairing;
+  int32_t reserved; /* 0 */
+} irm_rope;
+
 /* Text for a status code (static storage). */
 const char* irm_status_string(int status);
 
@@ -138,6 +163,15 @@ irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_h
                            int32_t* out_src_row,
                            int32_t* out_delta, int32_t* out_pos_src, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
+/* Same, with the model's RoPE variant (rope == NULL: the default).  IRM_ERR_INVALID_ARG for a
+ * pairing other than the two above, a non-zero reserved field or a non-finite frequency. */
+irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                const void* kv_rows, int64_t n_rows, void* paged_out,
+                                int64_t n_pages, const int32_t* page_table, int max_pages,
+                                int32_t* out_src_row, int32_t* out_delta, int32_t* out_pos_src,
+                                const irm_rope* rope, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
 
 /*
  * Fused delta-rotate + absorbed MLA decode attention (one query token per request).
@@ -163,6 +197,14 @@ irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int
                                const void* kv_rows, int64_t n_rows, float softmax_scale,
                                void* out, float* lse, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+/* Same, with the model's RoPE variant (rope == NULL: the default; errors as for
+ * irm_assemble_kv_rope). */
+irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B, int H,
+                                    const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                    const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                    const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                    void* out, float* lse, const irm_rope* rope, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Decode without any device allocation by the caller.  The method's pages have no
@@ -202,6 +244,14 @@ irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, in
                                 const void* kv_rows, int64_t n_rows, float softmax_scale,
                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
+/* Same, with the model's RoPE variant (rope == NULL: the default; errors as for
+ * irm_assemble_kv_rope). */
+irm_status irm_mla_attn_prefill_rope(const void* q_lat, const void* q_rope, int B, int n_q, int H,
+                                     const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                     const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                     const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                     void* out, float* lse, const irm_rope* rope, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

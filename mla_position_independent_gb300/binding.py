@@ -23,8 +23,27 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 
 EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_chunks",
            "irm_device_status", "irm_assemble_kv_workspace_size", "irm_assemble_kv",
-           "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode", "irm_mla_attn_decode_noalloc",
-           "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill"]
+           "irm_assemble_kv_rope", "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
+           "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc",
+           "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope"]
+
+ROPE_NEOX, ROPE_INTERLEAVED = 0, 1
+
+
+class Rope(ctypes.Structure):
+    """irm_rope: the model's RoPE variant (32 frequencies theta_j in radians per position and
+    the pairing, ROPE_NEOX = dims (j, j+32) or ROPE_INTERLEAVED = dims (2j, 2j+1))."""
+    _fields_ = [("inv_freq", ctypes.c_double * 32), ("pairing", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, inv_freq, pairing=ROPE_NEOX):
+        f = np.asarray(inv_freq, np.float64).reshape(32)
+        return cls((ctypes.c_double * 32)(*f.tolist()), int(pairing), 0)
+
+
+def _rope_ptr(rope):
+    return None if rope is None else ctypes.cast(ctypes.pointer(rope), ctypes.c_void_p)
 
 
 class IrmError(RuntimeError):
@@ -57,6 +76,11 @@ def lib():
         L.irm_mla_attn_prefill_workspace_size.argtypes = [I, I, I, P]
         L.irm_mla_attn_prefill.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
                                            P, P, SZ, P]
+        L.irm_assemble_kv_rope.argtypes = [P, P, I, P, P, P, I64, P, I64, P, I, P, P, P, P, P, SZ, P]
+        L.irm_mla_attn_decode_rope.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
+                                               P, P, P, SZ, P]
+        L.irm_mla_attn_prefill_rope.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float,
+                                                P, P, P, P, SZ, P]
         for name in EXPORTS:
             if name not in ("irm_status_string", "irm_last_error", "irm_version"):
                 getattr(L, name).restype = I
@@ -138,7 +162,9 @@ def assemble_kv_workspace_size(B: int) -> int:
 
 def irm_assemble_kv(table: ChunkTable, kv_rows: torch.Tensor, paged_out=None, page_table=None,
                     out_src_row=None, out_delta=None, out_pos_src=None, workspace=None,
-                    stream=None):
+                    stream=None, rope: Rope | None = None):
+    """Rotate+gather and/or the assembly plan; rope selects the model's RoPE variant
+    (irm_assemble_kv_rope), None the default."""
     _need(kv_rows, torch.bfloat16, "kv_rows", 2)
     n_pages, max_pages = 0, 0
     if paged_out is not None:
@@ -150,11 +176,11 @@ def irm_assemble_kv(table: ChunkTable, kv_rows: torch.Tensor, paged_out=None, pa
             _need(t, torch.int32, n, 1)
     if workspace is None:
         workspace = new_workspace(assemble_kv_workspace_size(table.B), kv_rows.device)
-    _check(lib().irm_assemble_kv(
+    _check(lib().irm_assemble_kv_rope(
         _ptr(table.chunks_host), _ptr(table.indptr_host), table.B, _ptr(table.chunks_dev),
         _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]), _ptr(paged_out), n_pages,
         _ptr(page_table), max_pages, _ptr(out_src_row), _ptr(out_delta), _ptr(out_pos_src),
-        _ptr(workspace), workspace.numel(), _stream(stream)))
+        _rope_ptr(rope), _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
 
 
@@ -173,8 +199,9 @@ def prefill_workspace_size(B: int, n_q: int, H: int) -> int:
 
 
 def irm_mla_attn_decode(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,
-                        out=None, lse=None, workspace=None, stream=None):
-    """q_lat [B, H, 512] / q_rope [B, H, 64] bf16 (a [B, 1, H, *] view is accepted)."""
+                        out=None, lse=None, workspace=None, stream=None, rope: Rope | None = None):
+    """q_lat [B, H, 512] / q_rope [B, H, 64] bf16 (a [B, 1, H, *] view is accepted); rope
+    selects the model's RoPE variant (irm_mla_attn_decode_rope), None the default."""
     B, H = int(q_lat.shape[0]), int(q_lat.shape[-2])
     _need(q_lat, torch.bfloat16, "q_lat")
     _need(q_rope, torch.bfloat16, "q_rope")
@@ -186,11 +213,11 @@ def irm_mla_attn_decode(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale
         _need(lse, torch.float32, "lse")
     if workspace is None:
         workspace = new_workspace(decode_workspace_size(table, H), q_lat.device)
-    _check(lib().irm_mla_attn_decode(
+    _check(lib().irm_mla_attn_decode_rope(
         _ptr(q_lat), _ptr(q_rope), B, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
         _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
-        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _stream(stream)))
+        float(softmax_scale), _ptr(out), _ptr(lse), _rope_ptr(rope), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return out, lse, workspace
 
 
@@ -215,8 +242,9 @@ def irm_mla_attn_decode_noalloc(q_lat, q_rope, table: ChunkTable, kv_rows,
 
 
 def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,
-                         out=None, lse=None, workspace=None, stream=None):
-    """q_lat [B, n_q, H, 512] / q_rope [B, n_q, H, 64] bf16, causal over the last n_q rows."""
+                         out=None, lse=None, workspace=None, stream=None, rope: Rope | None = None):
+    """q_lat [B, n_q, H, 512] / q_rope [B, n_q, H, 64] bf16, causal over the last n_q rows;
+    rope selects the model's RoPE variant (irm_mla_attn_prefill_rope), None the default."""
     B, n_q, H = (int(x) for x in q_lat.shape[:3])
     _need(q_lat, torch.bfloat16, "q_lat", 4)
     _need(q_rope, torch.bfloat16, "q_rope", 4)
@@ -228,9 +256,9 @@ def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scal
         _need(lse, torch.float32, "lse")
     if workspace is None:
         workspace = new_workspace(prefill_workspace_size(B, n_q, H), q_lat.device)
-    _check(lib().irm_mla_attn_prefill(
+    _check(lib().irm_mla_attn_prefill_rope(
         _ptr(q_lat), _ptr(q_rope), B, n_q, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
         _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
-        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _stream(stream)))
+        float(softmax_scale), _ptr(out), _ptr(lse), _rope_ptr(rope), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return out, lse, workspace

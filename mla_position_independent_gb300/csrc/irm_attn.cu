@@ -147,7 +147,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int col0 = (int)rank * 256;
-  const int p0 = (int)rank * 16;  // this CTA's NeoX pairs of k_r: p0 .. p0+15
   const int Mv = a.Mv;
   const Layout L = make_layout(Mv, (int)rank);
   const int NS = L.stages;
@@ -232,9 +231,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int rsub = tp >> 3;   // row within a group of kCopyThreads / 8
       const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
       const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
-      // Stored chunk c (0..3) of this CTA's k_r / q_rope half: columns (c < 2 ? 0 : 32) + p0 +
-      // 8 (c & 1) of the 64 rope columns (its pairs' first then second halves).
-      const int kr_col = (chk < 2 ? 0 : 32) + p0 + 8 * (chk & 1);
+      // Stored chunk c (0..3) of this CTA's k_r / q_rope half: the 16-byte chunk
+      // half_chunk(c) of the 64 rope columns (NeoX: its pairs' first then second halves;
+      // interleaved: four contiguous chunks).
+      const int kr_col = chk < 4 ? 8 * half_chunk(a.interleaved, (int)rank, chk) : 0;
       // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
       // lands with the first KV tile (same cp.async group).
       if (ntiles > 0 && chk < 4) {
@@ -311,7 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;  // orders the map's deltas
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          rotate_krope_half_16rows(smem + kr_slab(s), map_delta + s * kBN, phaseF, 32 * pb + 16 * h, p0,
+          rotate_krope_half_16rows(smem + kr_slab(s), map_delta + s * kBN, phaseF, a.interleaved, (int)rank,
+                                   32 * pb + 16 * h,
                                    4 * (s & 1), lane, dprev[h], cs_c[h], cs_s[h]);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));

@@ -52,6 +52,34 @@ __device__ __forceinline__ void rotate_pairs8(uint4& x, uint4& y, const float* c
   }
 }
 
+// Interleaved pairing: rotates the 4 pairs (v[2i], v[2i+1]) held in one 16-byte chunk.
+__device__ __forceinline__ void rotate_pairs4_within(uint4& v, const float* cs_c, const float* cs_s) {
+  __nv_bfloat162* vp = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(vp[q]);
+    const float x = fmaf(f.x, cs_c[q], -f.y * cs_s[q]), y = fmaf(f.x, cs_s[q], f.y * cs_c[q]);
+    vp[q] = __floats2bfloat162_rn(x, y);
+  }
+}
+
+// A lane rotates 8 pairs held in two 16-byte k_r chunks: chunk a (as x) and chunk b (as y).
+// Frequency index of its pair e (0..7): NeoX half split (b = a + 4), pair e = (x[e], y[e]),
+// index 8a + e; interleaved, pairs 0-3 = (x[2i], x[2i+1]), index 4a + i, and pairs 4-7 =
+// (y[2i], y[2i+1]), index 4b + i.
+__device__ __forceinline__ int pair_index(int interleaved, int a, int b, int e) {
+  return interleaved ? (e < 4 ? 4 * a + e : 4 * b + (e - 4)) : 8 * a + e;
+}
+__device__ __forceinline__ void rotate_pairs8_any(uint4& x, uint4& y, const float* cs_c, const float* cs_s,
+                                                  int interleaved) {
+  if (interleaved) {
+    rotate_pairs4_within(x, cs_c, cs_s);
+    rotate_pairs4_within(y, cs_c + 4, cs_s + 4);
+  } else {
+    rotate_pairs8(x, y, cs_c, cs_s);
+  }
+}
+
 __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status != nullptr) atomicOr(status, bits);
 }

@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         const int rs = rot % kKrSlots;
 #pragma unroll
         for (int r0 = 0; r0 < R::kRotRows; r0 += 8)
-          rotate_krope_8rows(smem + L.kr + (uint32_t)rs * kSlab, map_delta + rs * kBN, phaseF, R::kRotRows * pw + r0,
+          rotate_krope_8rows(smem + L.kr + (uint32_t)rs * kSlab, map_delta + rs * kBN, phaseF, a.interleaved,
+                             R::kRotRows * pw + r0,
                              lane, dprev, cs_c, cs_s);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_KR_FULL + rs));

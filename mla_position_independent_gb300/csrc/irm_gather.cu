@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(kGatherThreads) rotate_gather_kernel(const Gat
         for (int u = 0; u < kUnroll; ++u)
           if (d_off[u] >= 0) __stcs(dst + d_off[u], v[u]);
       }
-      // k_r: 4 pair-vectors per row (vector 64+v pairs with 68+v).
+      // k_r: a thread takes 16-byte vectors 64+pv and 68+pv of a row (NeoX: pairs 8pv..8pv+7,
+      // first elements then partners; interleaved: the 4 pairs inside each vector).
       const int n_kr = len * 4;
       for (int it = tid; it < n_kr; it += kGatherThreads) {
         const int row = it >> 2, pv = it & 3;
@@ -132,7 +133,16 @@ __global__ void __launch_bounds__(kGatherThreads) rotate_gather_kernel(const Gat
         if (page < 0 || page >= a.n_pages) continue;  // recorded by the cKV loop
         const uint4* s = src + (int64_t)row * (kDRow / 8) + 64;
         uint4 x = __ldcs(s + pv), y = __ldcs(s + 4 + pv);
-        if (delta != 0) rotate_pairs8(x, y, cs_c + 8 * pv, cs_s + 8 * pv);
+        if (delta != 0) {
+          float c8[8], s8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = pair_index(a.interleaved, pv, pv + 4, e);
+            c8[e] = cs_c[j];
+            s8[e] = cs_s[j];
+          }
+          rotate_pairs8_any(x, y, c8, s8, a.interleaved);
+        }
         uint4* d = dst + ((int64_t)page * kPage + (t % kPage)) * (kDRow / 8) + 64;
         __stcs(d + pv, x);
         __stcs(d + 4 + pv, y);

@@ -35,19 +35,43 @@ irm_status cuda_fail(cudaError_t e, const char* where) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// RoPE phase increments F[j] = theta_j / (2 pi) * 2^64 with theta_j = 10000^(-2j/64),
-// computed once in fp64 on the host; the device turns (delta * F[j]) mod 2^64 into an angle.
+// RoPE phase step of one pair: F = frac(theta / 2pi) * 2^64 (fp64 on the host), so that the
+// device's (delta * F) mod 2^64 is the angle delta * theta reduced to one turn.
+uint64_t phase_step(double theta) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double turns = theta / two_pi;
+  turns -= std::floor(turns);  // [0, 1]
+  const double v = std::ldexp(turns, 64);
+  return v >= 18446744073709551616.0 ? 0ull : (uint64_t)v;
+}
+
+// The default convention: NeoX half split, theta_j = 10000^(-2j/64).
 const irm::RopePhaseHost& rope_phase() {
   static const irm::RopePhaseHost tab = [] {
     irm::RopePhaseHost t{};
-    const double two_pi = 6.283185307179586476925286766559;
-    for (int j = 0; j < 32; ++j) {
-      const double theta = std::pow(10000.0, -2.0 * j / 64.0);
-      t.F[j] = (uint64_t)std::ldexp(theta / two_pi, 64);
-    }
+    for (int j = 0; j < 32; ++j) t.F[j] = phase_step(std::pow(10000.0, -2.0 * j / 64.0));
     return t;
   }();
   return tab;
+}
+
+// Phase steps and pairing of a caller's RoPE variant (NULL: the default).
+irm_status rope_select(const irm_rope* rope, uint64_t* F, int* interleaved) {
+  if (rope == nullptr) {
+    std::memcpy(F, rope_phase().F, 32 * sizeof(uint64_t));
+    *interleaved = 0;
+    return IRM_OK;
+  }
+  if (rope->pairing != IRM_ROPE_NEOX && rope->pairing != IRM_ROPE_INTERLEAVED)
+    return fail(IRM_ERR_INVALID_ARG, "rope pairing %d is neither IRM_ROPE_NEOX nor IRM_ROPE_INTERLEAVED",
+                rope->pairing);
+  if (rope->reserved != 0) return fail(IRM_ERR_INVALID_ARG, "rope reserved field must be 0");
+  for (int j = 0; j < 32; ++j) {
+    if (!std::isfinite(rope->inv_freq[j])) return fail(IRM_ERR_INVALID_ARG, "rope inv_freq[%d] is not finite", j);
+    F[j] = phase_step(rope->inv_freq[j]);
+  }
+  *interleaved = rope->pairing == IRM_ROPE_INTERLEAVED ? 1 : 0;
+  return IRM_OK;
 }
 
 int num_sms() {
@@ -233,11 +257,14 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
 irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                     const irm_chunk* chunks_host, const int32_t* indptr_host,
                     const irm_chunk* chunks_dev, const int32_t* indptr_dev, const void* kv_rows,
-                    int64_t n_rows, float softmax_scale, void* out, float* lse, void* workspace,
-                    size_t workspace_bytes, cudaStream_t stream, bool decode) {
+                    int64_t n_rows, float softmax_scale, void* out, float* lse, const irm_rope* rope,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode) {
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
+  uint64_t phaseF[32];
+  int interleaved = 0;
+  if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
   AttnPlan pl;
   if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
   if (!q_lat || !q_rope || !kv_rows || !out || !chunks_dev || !indptr_dev)
@@ -273,7 +300,8 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     d.out = out;
     d.lse = lse;
     d.status = static_cast<int*>(workspace);
-    std::memcpy(d.phase.F, rope_phase().F, sizeof d.phase.F);
+    std::memcpy(d.phase.F, phaseF, sizeof d.phase.F);
+    d.interleaved = interleaved;
     cudaError_t e = irm::launch_mla_decode(d, stream);
     if (e != cudaSuccess) return cuda_fail(e, "mla decode launch");
     return IRM_OK;
@@ -305,7 +333,8 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     a.lsepart = reinterpret_cast<float*>(ws + partial_o_bytes(B, units));
     a.counters = reinterpret_cast<int*>(ws + partial_o_bytes(B, units) + partial_lse_bytes(B, units));
   }
-  std::memcpy(a.phase.F, rope_phase().F, sizeof a.phase.F);
+  std::memcpy(a.phase.F, phaseF, sizeof a.phase.F);
+  a.interleaved = interleaved;
   cudaError_t e = irm::launch_mla_attn(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "mla attention launch");
   return IRM_OK;
@@ -399,9 +428,24 @@ irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_h
                            const int32_t* page_table, int max_pages, int32_t* out_src_row,
                            int32_t* out_delta, int32_t* out_pos_src, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
+  return irm_assemble_kv_rope(chunks_host, indptr_host, B, chunks_dev, indptr_dev, kv_rows, n_rows,
+                              paged_out, n_pages, page_table, max_pages, out_src_row, out_delta,
+                              out_pos_src, nullptr, workspace, workspace_bytes, stream);
+}
+
+irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                const void* kv_rows, int64_t n_rows, void* paged_out,
+                                int64_t n_pages, const int32_t* page_table, int max_pages,
+                                int32_t* out_src_row, int32_t* out_delta, int32_t* out_pos_src,
+                                const irm_rope* rope, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
+  uint64_t phaseF[32];
+  int interleaved = 0;
+  if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
   const bool plan_out = out_src_row || out_delta || out_pos_src;
   if (plan_out && !(out_src_row && out_delta && out_pos_src))
     return fail(IRM_ERR_INVALID_ARG, "out_src_row, out_delta and out_pos_src go together");
@@ -434,7 +478,8 @@ irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_h
   g.out_src = out_src_row;
   g.out_delta = out_delta;
   g.out_pos_src = out_pos_src;
-  std::memcpy(g.phase.F, rope_phase().F, sizeof g.phase.F);
+  std::memcpy(g.phase.F, phaseF, sizeof g.phase.F);
+  g.interleaved = interleaved;
   if (plan_out) {
     int64_t* row_start = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER);
     g.row_start = row_start;
@@ -466,7 +511,17 @@ irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int
                                float* lse, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
-                  n_rows, softmax_scale, out, lse, workspace, workspace_bytes, stream, true);
+                  n_rows, softmax_scale, out, lse, nullptr, workspace, workspace_bytes, stream, true);
+}
+
+irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B, int H,
+                                    const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                    const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                    const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                    void* out, float* lse, const irm_rope* rope, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+                  n_rows, softmax_scale, out, lse, rope, workspace, workspace_bytes, stream, true);
 }
 
 irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, int B, int H,
@@ -500,7 +555,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   }
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
-                  n_rows, softmax_scale, out, lse, ws, kNoAllocScratchBytes, stream, true);
+                  n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true);
 }
 
 irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes) {
@@ -517,7 +572,17 @@ irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, in
                                 float* lse, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
   return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
-                  n_rows, softmax_scale, out, lse, workspace, workspace_bytes, stream, false);
+                  n_rows, softmax_scale, out, lse, nullptr, workspace, workspace_bytes, stream, false);
+}
+
+irm_status irm_mla_attn_prefill_rope(const void* q_lat, const void* q_rope, int B, int n_q, int H,
+                                     const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                     const irm_chunk* chunks_dev, const int32_t* indptr_dev,
+                                     const void* kv_rows, int64_t n_rows, float softmax_scale,
+                                     void* out, float* lse, const irm_rope* rope, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+                  n_rows, softmax_scale, out, lse, rope, workspace, workspace_bytes, stream, false);
 }
 
 }  // extern "C"

@@ -27,6 +27,7 @@ struct GatherArgs {
   int32_t* out_delta;
   int32_t* out_pos_src;
   int* status;
+  int interleaved;  // RoPE pairing: 0 NeoX (j, j+32), 1 interleaved (2j, 2j+1)
   struct {
     uint64_t F[32];
   } phase;
@@ -53,6 +54,7 @@ struct AttnArgs {
   float* lsepart; // fp32 [2 ranks][B, n_qtiles*S, 128] (S > 1)
   int* counters;  // int [B, n_qtiles, 2] finished-split counters, zero between calls (S > 1)
   int* status;
+  int interleaved;  // RoPE pairing: 0 NeoX (j, j+32), 1 interleaved (2j, 2j+1)
   struct {
     uint64_t F[32];
   } phase;
@@ -79,6 +81,7 @@ struct DecodeArgs {
   float* glse;    // G > 1: fp32 [B, G, H] its log2-sum-exp (scaled scores, log2 units)
   int* counters;  // G > 1: int [B, C] finished clusters per output slice, zero between calls
   int* status;
+  int interleaved;  // RoPE pairing: 0 NeoX (j, j+32), 1 interleaved (2j, 2j+1)
   struct {
     uint64_t F[32];
   } phase;

@@ -99,47 +99,57 @@ struct ChunkWindow {
 };
 
 // Rotate 8 rows [r0, r0 + 8) of a staged k_r slab by R(delta[row]) with one warp: lane =
-// (row of 8, 16-byte chunk v of 4) takes k_r[8v .. 8v+7] and its NeoX partners
-// k_r[32+8v .. 32+8v+7].  dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls
-// (recomputed only when the row's delta changes; chunks are runs of equal delta).
+// (row of 8, 16-byte chunk v of 4) takes chunks v and v + 4 of the row (NeoX: k_r[8v .. 8v+7]
+// and their partners k_r[32+8v .. 32+8v+7]; interleaved: the 4 pairs inside each chunk).
+// dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls (recomputed only when the
+// row's delta changes; chunks are runs of equal delta).
 __device__ __forceinline__ void rotate_krope_8rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
-                                                   int r0, int lane, int& dprev, float (&cs_c)[8],
-                                                   float (&cs_s)[8]) {
+                                                   int interleaved, int r0, int lane, int& dprev,
+                                                   float (&cs_c)[8], float (&cs_s)[8]) {
   const int r = r0 + (lane >> 2), v = lane & 3;
   const int d = delta[r];
   if (d == 0) return;
   if (d != dprev) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[8 * v + e], cs_c[e], cs_s[e]);
+    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[pair_index(interleaved, v, v + 4, e)], cs_c[e], cs_s[e]);
     dprev = d;
   }
   uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)v ^ (uint32_t)(r & 7)) << 4));
   uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(4 + v) ^ (uint32_t)(r & 7)) << 4));
   uint4 x = *px, y = *py;
-  rotate_pairs8(x, y, cs_c, cs_s);
+  rotate_pairs8_any(x, y, cs_c, cs_s, interleaved);
   *px = x;
   *py = y;
 }
 
-// Rotate 16 rows [r0, r0 + 16) of a staged half k_r slab: 16 NeoX pairs j = p0 .. p0+15 per
-// row, stored as chunks cb, cb+1 = k_r[p0 .. p0+15] and chunks cb+2, cb+3 = their partners
-// k_r[32+p0 .. 32+p0+15] (128-byte swizzle; cb = 0 or 4, two stages share a slab).  Lane =
-// (row of 16, chunk c of 2); dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls.
+// The four 16-byte k_r chunks CTA `rank` of a column-split pair holds (stored chunk c =
+// 0..3 of its half slab): NeoX, pairs 16 rank .. 16 rank + 15 as chunks 2 rank, 2 rank + 1
+// (their first elements) and 4 + 2 rank, 5 + 2 rank (their partners); interleaved, the
+// same pairs as the contiguous chunks 4 rank .. 4 rank + 3.
+__device__ __forceinline__ int half_chunk(int interleaved, int rank, int c) {
+  return interleaved ? 4 * rank + c : (c < 2 ? 2 * rank + c : 4 + 2 * rank + (c - 2));
+}
+
+// Rotate 16 rows [r0, r0 + 16) of a staged half k_r slab (a CTA's 16 pairs per row, stored as
+// the chunks half_chunk(., rank, 0..3) at swizzled chunk positions cb .. cb + 3; cb = 0 or 4,
+// two stages share a slab).  Lane = (row of 16, c of 2) takes stored chunks c and c + 2.
+// dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls.
 __device__ __forceinline__ void rotate_krope_half_16rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
-                                                         int r0, int p0, int cb, int lane, int& dprev,
-                                                         float (&cs_c)[8], float (&cs_s)[8]) {
+                                                         int interleaved, int rank, int r0, int cb, int lane,
+                                                         int& dprev, float (&cs_c)[8], float (&cs_s)[8]) {
   const int r = r0 + (lane >> 1), c = lane & 1;
   const int d = delta[r];
   if (d == 0) return;
   if (d != dprev) {
+    const int ga = half_chunk(interleaved, rank, c), gb = half_chunk(interleaved, rank, c + 2);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[p0 + 8 * c + e], cs_c[e], cs_s[e]);
+    for (int e = 0; e < 8; ++e) rope_cos_sin(d, phaseF[pair_index(interleaved, ga, gb, e)], cs_c[e], cs_s[e]);
     dprev = d;
   }
   uint4* px = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(cb + c) ^ (uint32_t)(r & 7)) << 4));
   uint4* py = reinterpret_cast<uint4*>(kr + r * 128 + (((uint32_t)(cb + 2 + c) ^ (uint32_t)(r & 7)) << 4));
   uint4 x = *px, y = *py;
-  rotate_pairs8(x, y, cs_c, cs_s);
+  rotate_pairs8_any(x, y, cs_c, cs_s, interleaved);
   *px = x;
   *py = y;
 }

@@ -136,11 +136,11 @@ def _queries(B, n_q, H, seed, std, device):
     return q_lat, q_rope
 
 
-def tiny_case(seed: int = 0, q_std: float = Q_STD, device="cpu") -> Case:
+def tiny_case(seed: int = 0, q_std: float = Q_STD, device="cpu", H: int = 16) -> Case:
     """1 request, ctx 512: fresh carve-out [0, 32), then 4 reused chunks of 64/96/128/192
     drawn from a pool of 8 chunks with p_src ~ U{32..4096}; 16 causal queries at the tail,
-    16 heads.  k_r of every row is RoPE(position) of a N(0,1) content vector; the caller
-    encodes it (see rope_rows / rope_pos / rope_content)."""
+    H heads (16 in the configured workload).  k_r of every row is RoPE(position) of a N(0,1)
+    content vector; the caller encodes it (see rope_rows / rope_pos / rope_content)."""
     r_tab, r_v = _rngs(seed, 2)
     used = [64, 96, 128, 192]
     pool_lens = used + list(r_tab.choice(used, size=4))
@@ -161,8 +161,8 @@ def tiny_case(seed: int = 0, q_std: float = Q_STD, device="cpu") -> Case:
     for k in range(8):
         rope_pos[offs[k]:offs[k] + pool_lens[k]] = p_src[k] + np.arange(pool_lens[k])
     content = r_v.standard_normal((n_rows, D_ROPE))
-    q_lat, q_rope = _queries(1, 16, 16, seed + 202, q_std, device)
-    return Case("tiny", chunks, indptr, kv, n_q=16, H=16, q_lat=q_lat, q_rope=q_rope,
+    q_lat, q_rope = _queries(1, 16, H, seed + 202, q_std, device)
+    return Case("tiny", chunks, indptr, kv, n_q=16, H=H, q_lat=q_lat, q_rope=q_rope,
                 rope_rows=rope_rows, rope_pos=rope_pos, rope_content=content,
                 meta=dict(pool_lens=pool_lens, p_src=p_src))
 

@@ -52,3 +52,15 @@ def assert_close(out, ref, what, rel=TOL_REL_L2, mx=TOL_MAX_ABS):
     assert np.all(np.isfinite(np.asarray(out, np.float64))), f"{what}: non-finite output"
     assert r <= rel and m <= mx, f"{what}: rel L2 {r:.3e} (<= {rel}), max abs {m:.3e} (<= {mx})"
     return r, m
+
+
+def rope_tables():
+    """Frequency tables used as inputs by the RoPE-variant tests (model configurations, not
+    method arithmetic): the default base 10000, a plain base 500000, and a YaRN-like table
+    whose low-frequency pairs are slowed down by up to 40x with a linear ramp."""
+    j = np.arange(32)
+    base10k = 10000.0 ** (-2.0 * j / 64.0)
+    base500k = 500000.0 ** (-2.0 * j / 64.0)
+    ramp = np.clip((j - 16) / 8.0, 0.0, 1.0)
+    yarn = base10k / (1.0 + 39.0 * ramp)
+    return {"base10k": base10k, "base500k": base500k, "yarn": yarn}

@@ -127,3 +127,37 @@ def test_chunk_struct_layout_matches_header(irm):
     assert synth.CHUNK_DTYPE.itemsize == 24
     assert [synth.CHUNK_DTYPE.fields[k][1] for k in ("pool_offset", "len", "p_src", "p_tgt", "reused")] == \
         [0, 8, 12, 16, 20]
+
+
+def test_rope_struct_layout_matches_header(irm):
+    """irm_rope is 32 doubles + two int32 (264 bytes), as the header declares."""
+    assert ctypes.sizeof(irm.Rope) == 32 * 8 + 8
+    r = irm.Rope.make(np.arange(32) * 0.5, irm.ROPE_INTERLEAVED)
+    assert r.inv_freq[3] == 1.5 and r.pairing == 1 and r.reserved == 0
+
+
+@pytest.mark.parametrize("bad", ["pairing", "nan", "inf", "reserved"])
+def test_rope_entry_points_reject_bad_specs(irm, bad):
+    """The *_rope entry points check the spec on the host, before any pointer or launch."""
+    r = irm.Rope.make(10000.0 ** (-2.0 * np.arange(32) / 64.0))
+    if bad == "pairing":
+        r.pairing = 2
+    elif bad == "nan":
+        r.inv_freq[7] = float("nan")
+    elif bad == "inf":
+        r.inv_freq[0] = float("inf")
+    else:
+        r.reserved = 1
+    chunks, indptr = synth.make_table([[(0, 32, 0, 0), (100, 50, 7, 1)]])
+    L = irm.lib()
+    rp = ctypes.cast(ctypes.pointer(r), ctypes.c_void_p)
+    st = L.irm_assemble_kv_rope(chunks.ctypes.data, indptr.ctypes.data, 1, None, None, None, 1000,
+                                None, 0, None, 0, None, None, None, rp, None, 0, None)
+    assert st == -1, L.irm_last_error()
+    st = L.irm_mla_attn_decode_rope(None, None, 1, 16, chunks.ctypes.data, indptr.ctypes.data, None,
+                                    None, None, 1000, 0.1, None, None, rp, None, 0, None)
+    assert st == -1
+    st = L.irm_mla_attn_prefill_rope(None, None, 1, 4, 16, chunks.ctypes.data, indptr.ctypes.data,
+                                     None, None, None, 1000, 0.1, None, None, rp, None, 0, None)
+    assert st == -1
+    assert "rope" in L.irm_last_error().decode()

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 from mla_position_independent_gb300 import synth
+from helpers import rope_tables
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 SCALE = 1.0 / math.sqrt(192.0)
@@ -355,18 +356,6 @@ def test_rotate_gather_slots(oracle_mod):
 # Walkthrough §11: the delta-rotation must use the model's own rotary class and inv_freq
 # (a plain base-10000 fallback made reuse collapse in the pages' TransMLA case study).  The
 # oracle takes the spec as (theta[32] radians per position, pairing: 0 NeoX, 1 interleaved).
-
-def rope_tables():
-    """Frequency tables used as inputs by the variant tests (model configurations, not
-    method arithmetic): the default base 10000, a plain base 500000, and a YaRN-like table
-    whose low-frequency pairs are slowed down by up to 40x with a linear ramp."""
-    j = np.arange(32)
-    base10k = 10000.0 ** (-2.0 * j / 64.0)
-    base500k = 500000.0 ** (-2.0 * j / 64.0)
-    ramp = np.clip((j - 16) / 8.0, 0.0, 1.0)
-    yarn = base10k / (1.0 + 39.0 * ramp)
-    return {"base10k": base10k, "base500k": base500k, "yarn": yarn}
-
 
 def test_rope_table_of_default_is_the_default(oracle_mod):
     """The spec path with the default table and NeoX pairing is the default rotation, bit
