@@ -345,3 +345,33 @@ def custom_case(reqs, n_rows: int, seed: int = 0, n_q: int = 1, H: int = 16,
             cur += k
         case.page_table, case.n_pages = pt, n_pages
     return case
+
+
+def gear_table(vocab: int, seed: int = 0) -> np.ndarray:
+    """A seeded 64-bit Gear table for content-defined chunking (one random word per token id;
+    the pages do not publish theirs, so it is an input of our own choosing)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x6EA2])))
+    return rng.integers(0, 2**64, size=vocab, dtype=np.uint64)
+
+
+def cdc_streams(n_streams: int, tokens_per_stream: int, vocab: int = 102400, seed: int = 0,
+                doc_len: int = 4096, n_docs: int = 16):
+    """Token streams for content-defined chunking: each stream interleaves random tokens with
+    documents drawn from a shared set, placed at random offsets (agentic prompts that reorder
+    the same documents).  Returns (tokens int32 [sum], offsets int64 [n_streams + 1])."""
+    r_doc, r_mix = _rngs(seed, 2)
+    docs = r_doc.integers(0, vocab, size=(n_docs, doc_len)).astype(np.int32)
+    parts, offs = [], [0]
+    for _ in range(n_streams):
+        cur, stream = 0, []
+        while cur < tokens_per_stream:
+            if r_mix.random() < 0.6:
+                piece = docs[r_mix.integers(0, n_docs)]
+            else:
+                piece = r_mix.integers(0, vocab, size=int(r_mix.integers(16, 1024))).astype(np.int32)
+            piece = piece[: tokens_per_stream - cur]
+            stream.append(piece)
+            cur += piece.shape[0]
+        parts.append(np.concatenate(stream))
+        offs.append(offs[-1] + tokens_per_stream)
+    return np.concatenate(parts).astype(np.int32), np.asarray(offs, np.int64)

@@ -21,6 +21,9 @@ Functions and the passages they follow:
   attn         absorbed MLA softmax attention in fp64       [walkthrough §4]
   mla_attention  plan + assemble + attn per request, all or sampled (b, i, h) rows
   rotate_gather  expected paged rows for a set of target rows
+  gear_hash    64-token-window Gear hash of a token stream   [summary §2.2], [walkthrough §6]
+  cdc          content-defined chunks (7-bit test, [32, 512] clip) of a token stream
+  xxh64, chunk_fingerprint   xxHash64 of bytes / of a chunk's token ids [summary §2.2]
 
 Pins (tests/test_oracle.py): composition R(delta)R(p_src) = R(p_tgt), the worked example of
 [walkthrough §15] (tests/golden/worked_example.json), delta = 0 identity, norm preservation,
@@ -74,6 +77,14 @@ def _load():
             lib.oracle_attn.argtypes = [P, P, I, P, I, ctypes.c_double, P, P]
             lib.oracle_widen.argtypes = [P, I, P]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_gear_hash.argtypes = [P, I, P, P]
+            lib.oracle_cdc.argtypes = [P, I, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, P, P]
+            lib.oracle_cdc.restype = I
+            lib.oracle_xxh64.argtypes = [P, I, ctypes.c_uint64]
+            lib.oracle_xxh64.restype = ctypes.c_uint64
+            lib.oracle_chunk_fingerprint.argtypes = [P, I, I, ctypes.c_uint64]
+            lib.oracle_chunk_fingerprint.restype = ctypes.c_uint64
             _lib = lib
     return _lib
 
@@ -246,3 +257,41 @@ def rotate_gather(kv_rows_bits, chunks, indptr, page_table, rows=None, rope=None
     slot = page_table[b_of, t_of // 64].astype(np.int64) * 64 + t_of % 64
     vals = assemble(kv_rows_bits, pl["src_row"][flat], pl["delta"][flat], rope)
     return slot, vals
+
+
+# ------------------------------------------------------------------- content-defined chunking
+
+def gear_hash(tokens, gear) -> np.ndarray:
+    """h_i = sum_{k<64, k<=i} gear[tokens[i-k]] * 2^k mod 2^64 for every position (uint64)."""
+    tokens = _c(tokens, np.int32)
+    gear = _c(gear, np.uint64)
+    if tokens.size and (tokens.min() < 0 or tokens.max() >= gear.shape[0]):
+        raise ValueError("token id outside the Gear table")
+    out = np.empty(tokens.shape[0], np.uint64)
+    _load().oracle_gear_hash(_p(tokens), tokens.shape[0], _p(gear), _p(out))
+    return out
+
+
+def cdc(tokens, gear, min_len=32, max_len=512, bits=7, mode=0):
+    """Content-defined chunks of one stream: (starts, lens) int64 arrays."""
+    tokens = _c(tokens, np.int32)
+    gear = _c(gear, np.uint64)
+    if tokens.size and (tokens.min() < 0 or tokens.max() >= gear.shape[0]):
+        raise ValueError("token id outside the Gear table")
+    n = tokens.shape[0]
+    starts = np.empty(max(n, 1), np.int64)
+    lens = np.empty(max(n, 1), np.int64)
+    c = _load().oracle_cdc(_p(tokens), n, _p(gear), int(min_len), int(max_len), int(bits),
+                           int(mode), _p(starts), _p(lens))
+    return starts[:c], lens[:c]
+
+
+def xxh64(data: bytes, seed: int = 0) -> int:
+    buf = np.frombuffer(bytes(data) + b"\0", np.uint8)
+    return int(_load().oracle_xxh64(_p(buf), len(data), ctypes.c_uint64(seed)))
+
+
+def chunk_fingerprint(tokens, start, length, seed: int = 0) -> int:
+    tokens = _c(tokens, np.int32)
+    return int(_load().oracle_chunk_fingerprint(_p(tokens), int(start), int(length),
+                                                ctypes.c_uint64(seed)))

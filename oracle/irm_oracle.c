@@ -226,3 +226,134 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------------------
+ * Content-defined chunking of a token stream [summary §2.2, walkthrough §6].
+ *   Gear hash over a 64-token window: h_i = sum_{k=0}^{min(i,63)} G[x_{i-k}] * 2^k
+ *   (mod 2^64), G a 64-bit table indexed by token id (an input).
+ *   A position i is a boundary candidate when the hash passes the 7-bit test:
+ *     mode 0 (threshold): h_i < 2^(64 - bits)    (reading: "falls below a threshold")
+ *     mode 1 (low bits):  h_i mod 2^bits == 0    (the walkthrough's "low 7 bits" wording)
+ *   A chunk starting at s ends at the first candidate i with i - s + 1 >= min_len, or at
+ *   i = s + max_len - 1, or at the end of the stream; the next chunk starts at i + 1.
+ * ------------------------------------------------------------------------------------ */
+
+/* Window sum, written out term by term. */
+void oracle_gear_hash(const int32_t *tokens, i64 n, const uint64_t *gear, uint64_t *h) {
+  for (i64 i = 0; i < n; ++i) {
+    uint64_t acc = 0;
+    for (int k = 0; k < 64 && k <= i; ++k) acc += gear[tokens[i - k]] << k;
+    h[i] = acc;
+  }
+}
+
+static int cdc_candidate(uint64_t h, int bits, int mode) {
+  if (mode == 1) return (h & ((1ull << bits) - 1ull)) == 0ull;
+  return (h >> (64 - bits)) == 0ull;
+}
+
+/* Chunks of one stream; returns their count (starts / lens must hold n entries). */
+i64 oracle_cdc(const int32_t *tokens, i64 n, const uint64_t *gear, int min_len, int max_len,
+               int bits, int mode, i64 *starts, i64 *lens) {
+  uint64_t *h = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
+  oracle_gear_hash(tokens, n, gear, h);
+  i64 count = 0, s = 0;
+  for (i64 i = 0; i < n; ++i) {
+    i64 len = i - s + 1;
+    int end = (len >= min_len && cdc_candidate(h[i], bits, mode)) || len == max_len || i == n - 1;
+    if (end) {
+      starts[count] = s;
+      lens[count] = len;
+      ++count;
+      s = i + 1;
+    }
+  }
+  free(h);
+  return count;
+}
+
+/* ------------------------------------------------------------------------------------
+ * xxHash64 of a byte string (Y. Collet's XXH64: four 64-bit lanes over 32-byte stripes,
+ * lane merge, then 8-, 4- and 1-byte tails and the final avalanche), used as the chunk
+ * fingerprint [summary §2.2].  The chunk's token ids are hashed as little-endian int32.
+ * ------------------------------------------------------------------------------------ */
+static const uint64_t XP1 = 11400714785074694791ull, XP2 = 14029467366897019727ull,
+                      XP3 = 1609587929392839161ull, XP4 = 9650029242287828579ull,
+                      XP5 = 2870177450012600261ull;
+
+static uint64_t rotl64(uint64_t x, int r) { return (x << r) | (x >> (64 - r)); }
+static uint64_t rd64(const uint8_t *p) {
+  uint64_t v = 0;
+  for (int i = 7; i >= 0; --i) v = (v << 8) | p[i];
+  return v;
+}
+static uint32_t rd32(const uint8_t *p) {
+  uint32_t v = 0;
+  for (int i = 3; i >= 0; --i) v = (v << 8) | p[i];
+  return v;
+}
+static uint64_t xround(uint64_t acc, uint64_t input) {
+  acc += input * XP2;
+  acc = rotl64(acc, 31);
+  return acc * XP1;
+}
+static uint64_t xmerge(uint64_t acc, uint64_t v) {
+  acc ^= xround(0, v);
+  return acc * XP1 + XP4;
+}
+
+uint64_t oracle_xxh64(const uint8_t *p, i64 len, uint64_t seed) {
+  const uint8_t *end = p + len;
+  uint64_t h;
+  if (len >= 32) {
+    uint64_t v1 = seed + XP1 + XP2, v2 = seed + XP2, v3 = seed, v4 = seed - XP1;
+    while (p + 32 <= end) {
+      v1 = xround(v1, rd64(p));
+      v2 = xround(v2, rd64(p + 8));
+      v3 = xround(v3, rd64(p + 16));
+      v4 = xround(v4, rd64(p + 24));
+      p += 32;
+    }
+    h = rotl64(v1, 1) + rotl64(v2, 7) + rotl64(v3, 12) + rotl64(v4, 18);
+    h = xmerge(h, v1);
+    h = xmerge(h, v2);
+    h = xmerge(h, v3);
+    h = xmerge(h, v4);
+  } else {
+    h = seed + XP5;
+  }
+  h += (uint64_t)len;
+  while (p + 8 <= end) {
+    h ^= xround(0, rd64(p));
+    h = rotl64(h, 27) * XP1 + XP4;
+    p += 8;
+  }
+  if (p + 4 <= end) {
+    h ^= (uint64_t)rd32(p) * XP1;
+    h = rotl64(h, 23) * XP2 + XP3;
+    p += 4;
+  }
+  while (p < end) {
+    h ^= (uint64_t)(*p) * XP5;
+    h = rotl64(h, 11) * XP1;
+    ++p;
+  }
+  h ^= h >> 33;
+  h *= XP2;
+  h ^= h >> 29;
+  h *= XP3;
+  h ^= h >> 32;
+  return h;
+}
+
+/* Fingerprint of tokens[start .. start + len): xxHash64 of their little-endian int32 bytes. */
+uint64_t oracle_chunk_fingerprint(const int32_t *tokens, i64 start, i64 len, uint64_t seed) {
+  uint8_t *buf = (uint8_t *)malloc((size_t)(4 * len + 1));
+  for (i64 i = 0; i < len; ++i) {
+    uint32_t v = (uint32_t)tokens[start + i];
+    for (int b = 0; b < 4; ++b) buf[4 * i + b] = (uint8_t)(v >> (8 * b));
+  }
+  uint64_t h = oracle_xxh64(buf, 4 * len, seed);
+  free(buf);
+  return h;
+}
