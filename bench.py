@@ -142,7 +142,15 @@ def _prep_case(name, seed):
     if name.startswith("rotate_gather_"):
         n = int(name.split("_")[-1].rstrip("M")) << 20
         return synth.rotate_gather_case(n, seed, device="cuda", fill_kv=False)
+    if name.startswith("cdc_"):
+        S, per = CDC_SHAPES[name]
+        return synth.cdc_streams(S, per, seed=seed)
     raise ValueError(name)
+
+
+# content-defined chunking workloads: (streams, tokens per stream)
+CDC_SHAPES = {"cdc_4M": (64, 1 << 16), "cdc_16M": (256, 1 << 16)}
+CDC_VOCAB = 102400
 
 
 DESCR = {
@@ -154,6 +162,10 @@ DESCR = {
                        "16384-token prefix (4096 exact-prefix delta=0, 12288 moved delta ~ U[-8192,8192])",
     "chunked_prefill_256": "profiling-size slice of the chunked prefill: the same prefix, 256 new "
                            "causal queries per request",
+    "cdc_4M": "content-defined chunking of 64 token streams x 65536 tokens (shared documents at "
+              "shifting offsets, vocab 102400): Gear hash (SplitMix64 Gear words), [32,512] "
+              "chunks, xxHash64 fingerprints",
+    "cdc_16M": "content-defined chunking of 256 token streams x 65536 tokens (as cdc_4M)",
 }
 
 
@@ -172,6 +184,29 @@ class Workload:
         import mla_position_independent_gb300 as irm
         self.irm = irm
         self.name = name
+        if name.startswith("cdc_"):
+            from mla_position_independent_gb300 import synth
+            tokens, offsets = _prep_case(name, seed)
+            self.kind = "cdc"
+            self.tokens = torch.from_numpy(tokens).cuda()
+            self.offsets = offsets
+            self.offsets_dev = torch.from_numpy(offsets.copy()).cuda()
+            self.gear = None  # Gear words generated from SplitMix64 (no table lookups)
+            nbytes, slots = irm.cdc_sizes(offsets)
+            self.ws = irm.new_workspace(nbytes)
+            S = offsets.shape[0] - 1
+            self.cdc_out = (torch.empty(S, dtype=torch.int32, device="cuda"),
+                            torch.empty(slots, dtype=torch.int32, device="cuda"),
+                            torch.empty(slots, dtype=torch.int32, device="cuda"),
+                            torch.empty(slots, dtype=torch.int64, device="cuda"))
+            self.ctx_total = int(offsets[-1])
+            self.n_tokens = self.ctx_total
+            # algorithmic bytes: every token id read once (4 B); the chunk records written
+            # (start, len, fingerprint: 16 B) for ~n/156 chunks
+            self.bytes = 4 * self.n_tokens + 16 * (self.n_tokens // 156)
+            self.flops = 0.0
+            self.table = None
+            return
         case = _prep_case(name, seed)
         if name.startswith("rotate_gather_"):
             _fill_large(case.kv_rows, seed)
@@ -211,6 +246,11 @@ class Workload:
 
     def step(self, stream=None):
         irm = self.irm
+        if self.kind == "cdc":
+            irm.irm_cdc_chunk(self.tokens, self.offsets, self.gear, out=self.cdc_out,
+                              workspace=self.ws, stream=stream, offsets_dev=self.offsets_dev,
+                              vocab=CDC_VOCAB)
+            return
         if self.kind == "decode":
             irm.irm_mla_attn_decode(self.q_lat, self.q_rope, self.table, self.case.kv_rows,
                                     out=self.out, lse=self.lse, workspace=self.ws, stream=stream)
@@ -222,9 +262,13 @@ class Workload:
                                 workspace=self.ws, stream=stream)
 
     def launches_per_step(self):
+        if self.kind == "cdc":
+            return 4  # slot bases, hash + candidate bits, boundary walk, fingerprints
         return 1  # one fused kernel per call (the split-KV merge runs inside it)
 
     def kernel_name(self):
+        if self.kind == "cdc":
+            return "cdc (4 kernels: base, hash, walk, fingerprint)"
         if self.kind == "gather":
             return "rotate_gather_kernel"
         if self.kind == "decode" and self.H in (16, 32):
@@ -461,7 +505,8 @@ def main():
                 warmup=args.warmup, ms_per_step=round(ms, 5), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
                 config=dict(workload=args.workload, description=DESCR.get(args.workload),
-                            requests=wl.table.B, ctx_total=wl.ctx_total,
+                            requests=(wl.table.B if wl.table is not None else len(wl.offsets) - 1),
+                            ctx_total=wl.ctx_total,
                             l2=L2_NOTE,
                             parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
                 roofline=rf, e2e=e2e, gpu_launches=args.steps * wl.launches_per_step(),
@@ -475,13 +520,13 @@ def main():
                                            f"{secs:.1f} s; bytes counted as ctx*1152/H per unit")
     if not args.no_extras and world == 1:
         extras = {}
-        for name in ("v3_decode", "chunked_prefill", "rotate_gather_4M"):
+        for name in ("v3_decode", "chunked_prefill", "rotate_gather_4M", "cdc_4M"):
             if name == args.workload:
                 continue
             del wl
             torch.cuda.empty_cache()
             wl = Workload(name, seed=rank)
-            st = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_4M": 50}[name]
+            st = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_4M": 50, "cdc_4M": 50}[name]
             t = statistics.mean(time_steps(wl, st, 3))
             r = roofline(wl, t, pk)
             r["kernel"] = wl.kernel_name()
@@ -489,6 +534,8 @@ def main():
             if wl.kind == "gather":
                 ent["rows_per_s"] = round(wl.ctx_total / (t * 1e-3), 1)
                 ent["GB_per_s_moved"] = r["achieved"]
+            elif wl.kind == "cdc":
+                ent["tokens_per_s"] = round(wl.n_tokens / (t * 1e-3), 1)
             elif wl.kind == "decode":
                 ent["logical_KV_GB_per_s"] = r["achieved"]
             else:

@@ -253,6 +253,67 @@ irm_status irm_mla_attn_prefill_rope(const void* q_lat, const void* q_rope, int 
                                      void* out, float* lse, const irm_rope* rope, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Content-defined chunking of token streams, the step that cuts a request's unmatched tail
+ * into content-addressed chunks before the registry lookup ["Irminsul: MLA-Native
+ * Position-Independent Caching for Agentic LLM Serving" technical summary §2.2: rolling Gear
+ * hash over 64-token windows, xxHash64 fingerprints; "Irminsul论文详解" §6: 7-bit boundary
+ * test, chunk length clipped to [32, 512]].
+ *   h_i = sum_{k=0}^{min(i,63)} gear[x_{i-k}] * 2^k mod 2^64, gear either a caller table or,
+ *   when gear == NULL, generated: gear[t] = the (t+1)-th output of SplitMix64 seeded with
+ *   params->gear_seed (a published counter-based generator; no table lookups on the GPU)
+ *   position i is a boundary candidate when the 7-bit test passes:
+ *     IRM_CDC_THRESHOLD: h_i < 2^(64 - bits) (the hash "falls below a threshold"; this test
+ *                        reads bits that depend on the whole 64-token window)
+ *     IRM_CDC_LOW_BITS:  h_i mod 2^bits == 0 (the "low 7 bits" wording; with this hash those
+ *                        bits depend only on the last `bits` tokens)
+ *   a chunk starting at s ends at the first candidate i >= s + min_len - 1, else at
+ *   s + max_len - 1, else at the end of the stream (the last chunk may be shorter);
+ *   its fingerprint is xxHash64 (seed `seed`) of its token ids as little-endian int32 bytes.
+ * params NULL: min_len 32, max_len 512, bits 7, IRM_CDC_THRESHOLD, seed 0, gear_seed 0.
+ */
+#define IRM_CDC_THRESHOLD 0
+#define IRM_CDC_LOW_BITS 1
+typedef struct irm_cdc_params {
+  int32_t min_len; /* >= 1 */
+  int32_t max_len; /* >= min_len, <= 65536 */
+  int32_t bits;    /* 1 .. 63 */
+  int32_t mode;    /* IRM_CDC_THRESHOLD or IRM_CDC_LOW_BITS */
+  uint64_t seed;      /* xxHash64 seed of the fingerprints */
+  uint64_t gear_seed; /* SplitMix64 seed of the generated Gear words (gear == NULL) */
+} irm_cdc_params;
+
+/*
+ * Sizes for irm_cdc_chunk:
+ *   offsets_host  [n_streams + 1] int64, offsets_host[0] == 0, non-decreasing; stream s is
+ *                 tokens[offsets[s] .. offsets[s+1]), at most INT32_MAX tokens long
+ *   bytes         workspace bytes
+ *   slots         output slots: stream s owns slots [base_s, base_s + len_s / min_len + 1),
+ *                 base_s = sum over earlier streams of (len / min_len + 1)
+ */
+irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
+                         size_t* bytes, int64_t* slots);
+
+/*
+ *   tokens       device int32 [offsets[n_streams]], ids in [0, vocab) (an id outside is
+ *                read as gear = 0 and recorded as IRM_ERR_DEVICE_BOUNDS in the status word)
+ *   offsets_host / offsets_dev   the stream offsets, host copy (validated, sizes) and a
+ *                byte-identical device copy (read by the kernels)
+ *   gear         device uint64 [vocab], the Gear table, or NULL for generated Gear words
+ *   vocab        token ids lie in [0, vocab)
+ *   n_chunks     device int32 [n_streams]: chunks of each stream
+ *   chunk_start  device int32 [slots]: stream-relative first token of each chunk (see
+ *                irm_cdc_sizes for the slot layout)
+ *   chunk_len    device int32 [slots]
+ *   chunk_hash   device uint64 [slots] or NULL (no fingerprints)
+ * Workspace: irm_cdc_sizes bytes, 256-byte aligned (its status word as for the other calls).
+ */
+irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, const int64_t* offsets_dev,
+                         int n_streams, const uint64_t* gear, int32_t vocab,
+                         const irm_cdc_params* params, int32_t* n_chunks, int32_t* chunk_start,
+                         int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,8 @@ EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_c
            "irm_device_status", "irm_assemble_kv_workspace_size", "irm_assemble_kv",
            "irm_assemble_kv_rope", "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
            "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc",
-           "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope"]
+           "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope",
+           "irm_cdc_sizes", "irm_cdc_chunk"]
 
 ROPE_NEOX, ROPE_INTERLEAVED = 0, 1
 
@@ -40,6 +41,19 @@ class Rope(ctypes.Structure):
     def make(cls, inv_freq, pairing=ROPE_NEOX):
         f = np.asarray(inv_freq, np.float64).reshape(32)
         return cls((ctypes.c_double * 32)(*f.tolist()), int(pairing), 0)
+
+
+CDC_THRESHOLD, CDC_LOW_BITS = 0, 1
+
+
+class CdcParams(ctypes.Structure):
+    """irm_cdc_params: chunk length clip, boundary test and fingerprint seed."""
+    _fields_ = [("min_len", ctypes.c_int32), ("max_len", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("seed", ctypes.c_uint64), ("gear_seed", ctypes.c_uint64)]
+
+    @classmethod
+    def make(cls, min_len=32, max_len=512, bits=7, mode=CDC_THRESHOLD, seed=0, gear_seed=0):
+        return cls(int(min_len), int(max_len), int(bits), int(mode), int(seed), int(gear_seed))
 
 
 def _rope_ptr(rope):
@@ -81,6 +95,8 @@ def lib():
                                                P, P, P, SZ, P]
         L.irm_mla_attn_prefill_rope.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float,
                                                 P, P, P, P, SZ, P]
+        L.irm_cdc_sizes.argtypes = [P, I, P, P, P]
+        L.irm_cdc_chunk.argtypes = [P, P, P, I, P, ctypes.c_int32, P, P, P, P, P, P, SZ, P]
         for name in EXPORTS:
             if name not in ("irm_status_string", "irm_last_error", "irm_version"):
                 getattr(L, name).restype = I
@@ -262,3 +278,54 @@ def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scal
         float(softmax_scale), _ptr(out), _ptr(lse), _rope_ptr(rope), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return out, lse, workspace
+
+
+def cdc_sizes(offsets: np.ndarray, params: CdcParams | None = None):
+    """(workspace bytes, output slots) of irm_cdc_chunk for these stream offsets."""
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    nb, sl = ctypes.c_size_t(0), ctypes.c_int64(0)
+    pp = None if params is None else ctypes.cast(ctypes.pointer(params), ctypes.c_void_p)
+    _check(lib().irm_cdc_sizes(_ptr(offsets), int(offsets.shape[0] - 1), pp, ctypes.byref(nb),
+                               ctypes.byref(sl)))
+    return nb.value, sl.value
+
+
+def cdc_slot_base(offsets: np.ndarray, min_len: int = 32) -> np.ndarray:
+    """First output slot of each stream (the layout irm_cdc_sizes documents)."""
+    lens = np.diff(np.asarray(offsets, np.int64))
+    return np.concatenate([[0], np.cumsum(lens // min_len + 1)])[:-1]
+
+
+def irm_cdc_chunk(tokens: torch.Tensor, offsets: np.ndarray, gear: torch.Tensor | None,
+                  params: CdcParams | None = None, fingerprints=True, out=None, workspace=None,
+                  stream=None, offsets_dev=None, vocab: int | None = None):
+    """Content-defined chunks of token streams (tokens int32 on the GPU, streams at host
+    offsets; gear: the 64-bit Gear table as an int64 tensor on the GPU, or None for Gear
+    words generated from params.gear_seed, with token ids in [0, vocab)).  Returns
+    (n_chunks [S], chunk_start [slots], chunk_len [slots], chunk_hash [slots] or None,
+    workspace); stream s's chunks sit at slots cdc_slot_base(offsets)[s] onwards."""
+    _need(tokens, torch.int32, "tokens", 1)
+    if gear is not None:
+        _need(gear, torch.int64, "gear", 1)
+        vocab = int(gear.shape[0])
+    elif vocab is None:
+        raise ValueError("generated Gear words need the vocab size")
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    S = int(offsets.shape[0] - 1)
+    nbytes, slots = cdc_sizes(offsets, params)
+    dev = tokens.device
+    if out is None:
+        out = (torch.empty(S, dtype=torch.int32, device=dev),
+               torch.empty(max(slots, 1), dtype=torch.int32, device=dev),
+               torch.empty(max(slots, 1), dtype=torch.int32, device=dev),
+               torch.empty(max(slots, 1), dtype=torch.int64, device=dev) if fingerprints else None)
+    n_chunks, c_start, c_len, c_hash = out
+    if offsets_dev is None:
+        offsets_dev = torch.from_numpy(offsets.copy()).to(dev)
+    if workspace is None:
+        workspace = new_workspace(nbytes, dev)
+    pp = None if params is None else ctypes.cast(ctypes.pointer(params), ctypes.c_void_p)
+    _check(lib().irm_cdc_chunk(_ptr(tokens), _ptr(offsets), _ptr(offsets_dev), S, _ptr(gear),
+                               int(vocab), pp, _ptr(n_chunks), _ptr(c_start), _ptr(c_len),
+                               _ptr(c_hash), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return n_chunks, c_start, c_len, c_hash, workspace

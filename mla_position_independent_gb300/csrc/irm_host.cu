@@ -368,6 +368,49 @@ irm_status noalloc_scratch(void** out) {
   return IRM_OK;
 }
 
+// Workspace of irm_cdc_chunk: status header, slot and segment bases [S + 1] each, the
+// candidate bitmask, then per speculative segment its chunk ends [spec_cap] and count.
+struct CdcLayout {
+  size_t base, seg_base, words, spec_ends, spec_count, total;
+  int64_t n_segs, spec_cap;
+};
+irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
+                     irm_cdc_params* p, int64_t* slots, int64_t* max_len, size_t* bytes,
+                     CdcLayout* lay = nullptr) {
+  if (n_streams <= 0 || offsets_host == nullptr) return fail(IRM_ERR_INVALID_ARG, "need n_streams > 0 and offsets");
+  *p = params ? *params : irm_cdc_params{32, 512, 7, IRM_CDC_THRESHOLD, 0, 0};
+  if (p->min_len < 1 || p->max_len < p->min_len || p->max_len > 65536)
+    return fail(IRM_ERR_INVALID_ARG, "need 1 <= min_len <= max_len <= 65536 (got %d, %d)", p->min_len, p->max_len);
+  if (p->bits < 1 || p->bits > 63) return fail(IRM_ERR_INVALID_ARG, "bits must lie in [1, 63]");
+  if (p->mode != IRM_CDC_THRESHOLD && p->mode != IRM_CDC_LOW_BITS)
+    return fail(IRM_ERR_INVALID_ARG, "mode must be IRM_CDC_THRESHOLD or IRM_CDC_LOW_BITS");
+  if (offsets_host[0] != 0) return fail(IRM_ERR_INVALID_ARG, "offsets[0] must be 0");
+  int64_t sl = 0, mx = 0;
+  for (int s = 0; s < n_streams; ++s) {
+    const int64_t len = offsets_host[s + 1] - offsets_host[s];
+    if (len < 0 || len > INT32_MAX) return fail(IRM_ERR_INVALID_ARG, "stream %d has length %lld", s, (long long)len);
+    sl += len / p->min_len + 1;
+    mx = std::max(mx, len);
+  }
+  *slots = sl;
+  *max_len = mx;
+  CdcLayout L{};
+  const int64_t seg = irm::cdc_segment_len();
+  for (int s = 0; s < n_streams; ++s) L.n_segs += (offsets_host[s + 1] - offsets_host[s] + seg - 1) / seg;
+  L.spec_cap = (seg + p->max_len) / p->min_len + 2;  // chunk ends in [seg start, seg end + max_len)
+  const size_t words = (size_t)(offsets_host[n_streams] >> 5) + (size_t)n_streams + 1;
+  const size_t bases = align_up((size_t)(n_streams + 1) * sizeof(int64_t), 256);
+  L.base = IRM_WORKSPACE_HEADER;
+  L.seg_base = L.base + bases;
+  L.words = L.seg_base + bases;
+  L.spec_ends = L.words + align_up(words * sizeof(uint32_t), 256);
+  L.spec_count = L.spec_ends + align_up((size_t)L.n_segs * (size_t)L.spec_cap * sizeof(int32_t), 256);
+  L.total = L.spec_count + align_up((size_t)(L.n_segs + 1) * sizeof(int32_t), 256);
+  *bytes = L.total;
+  if (lay) *lay = L;
+  return IRM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -556,6 +599,63 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
                   n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true);
+}
+
+
+irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
+                         size_t* bytes, int64_t* slots) {
+  if (bytes == nullptr || slots == nullptr) return fail(IRM_ERR_INVALID_ARG, "null output");
+  irm_cdc_params p;
+  int64_t mx;
+  return cdc_check(offsets_host, n_streams, params, &p, slots, &mx, bytes);
+}
+
+irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, const int64_t* offsets_dev,
+                         int n_streams, const uint64_t* gear, int32_t vocab,
+                         const irm_cdc_params* params, int32_t* n_chunks, int32_t* chunk_start,
+                         int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  irm_cdc_params p;
+  int64_t slots = 0, max_len = 0;
+  size_t need = 0;
+  CdcLayout lay;
+  irm_status st = cdc_check(offsets_host, n_streams, params, &p, &slots, &max_len, &need, &lay);
+  if (st != IRM_OK) return st;
+  if (vocab <= 0) return fail(IRM_ERR_INVALID_ARG, "vocab must be positive");
+  if (!offsets_dev || !n_chunks || !chunk_start || !chunk_len ||
+      (!tokens && offsets_host[n_streams] > 0))
+    return fail(IRM_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned(tokens, 4) || !aligned(offsets_dev, 8) || !aligned(gear, 8) || !aligned(chunk_hash, 8))
+    return fail(IRM_ERR_INVALID_ARG, "misaligned device pointer");
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+  irm::CdcArgs a{};
+  a.tokens = tokens;
+  a.offsets = offsets_dev;
+  a.S = n_streams;
+  a.gear = gear;
+  a.gear_seed = p.gear_seed;
+  a.vocab = vocab;
+  a.min_len = p.min_len;
+  a.max_len = p.max_len;
+  a.bits = p.bits;
+  a.mode = p.mode;
+  a.seed = p.seed;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<int*>(ws);
+  a.base = reinterpret_cast<int64_t*>(ws + lay.base);
+  a.seg_base = reinterpret_cast<int64_t*>(ws + lay.seg_base);
+  a.words = reinterpret_cast<uint32_t*>(ws + lay.words);
+  a.spec_ends = reinterpret_cast<int32_t*>(ws + lay.spec_ends);
+  a.spec_count = reinterpret_cast<int32_t*>(ws + lay.spec_count);
+  a.spec_cap = lay.spec_cap;
+  a.n_chunks = n_chunks;
+  a.chunk_start = chunk_start;
+  a.chunk_len = chunk_len;
+  a.chunk_hash = chunk_hash;
+  cudaError_t e = irm::launch_cdc(a, max_len, slots, lay.n_segs, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "content-defined chunking launch");
+  return IRM_OK;
 }
 
 irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes) {

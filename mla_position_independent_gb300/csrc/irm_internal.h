@@ -87,6 +87,32 @@ struct DecodeArgs {
   } phase;
 };
 
+// Content-defined chunking of a batch of token streams.
+struct CdcArgs {
+  const int32_t* tokens;    // [offsets[S]] token ids, streams concatenated
+  const int64_t* offsets;   // device [S + 1]
+  int S;
+  const uint64_t* gear;     // device [vocab], or nullptr: SplitMix64 words from gear_seed
+  uint64_t gear_seed;
+  int vocab;
+  int min_len, max_len, bits, mode;
+  uint64_t seed;
+  int64_t* base;            // workspace [S + 1]: first output slot of each stream
+  int64_t* seg_base;        // workspace [S + 1]: first speculative segment of each stream
+  uint32_t* words;          // workspace: candidate bitmask, stream s from word (offsets[s] >> 5) + s
+  int32_t* spec_ends;       // workspace [segments][spec_cap]: speculative chunk ends
+  int32_t* spec_count;      // workspace [segments]
+  int64_t spec_cap;
+  int32_t* n_chunks;        // [S]
+  int32_t* chunk_start;     // [slots] stream-relative start of each chunk
+  int32_t* chunk_len;       // [slots]
+  uint64_t* chunk_hash;     // [slots] or nullptr
+  int* status;
+};
+int cdc_segment_len();
+cudaError_t launch_cdc(const CdcArgs& a, int64_t max_stream_len, int64_t slots, int64_t n_segs,
+                       cudaStream_t stream);
+
 cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int B,
                              int64_t* row_start, cudaStream_t stream);
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);

@@ -24,6 +24,7 @@ Functions and the passages they follow:
   gear_hash    64-token-window Gear hash of a token stream   [summary §2.2], [walkthrough §6]
   cdc          content-defined chunks (7-bit test, [32, 512] clip) of a token stream
   xxh64, chunk_fingerprint   xxHash64 of bytes / of a chunk's token ids [summary §2.2]
+  splitmix_gear  Gear words from SplitMix64 (G[t] = its (t+1)-th output), instead of a table
 
 Pins (tests/test_oracle.py): composition R(delta)R(p_src) = R(p_tgt), the worked example of
 [walkthrough §15] (tests/golden/worked_example.json), delta = 0 identity, norm preservation,
@@ -85,6 +86,7 @@ def _load():
             lib.oracle_xxh64.restype = ctypes.c_uint64
             lib.oracle_chunk_fingerprint.argtypes = [P, I, I, ctypes.c_uint64]
             lib.oracle_chunk_fingerprint.restype = ctypes.c_uint64
+            lib.oracle_splitmix_gear.argtypes = [I, ctypes.c_uint64, P]
             _lib = lib
     return _lib
 
@@ -295,3 +297,10 @@ def chunk_fingerprint(tokens, start, length, seed: int = 0) -> int:
     tokens = _c(tokens, np.int32)
     return int(_load().oracle_chunk_fingerprint(_p(tokens), int(start), int(length),
                                                 ctypes.c_uint64(seed)))
+
+
+def splitmix_gear(vocab: int, seed: int = 0) -> np.ndarray:
+    """Gear table whose word t is the (t+1)-th SplitMix64 output for `seed`."""
+    out = np.empty(int(vocab), np.uint64)
+    _load().oracle_splitmix_gear(int(vocab), ctypes.c_uint64(seed), _p(out))
+    return out

@@ -357,3 +357,16 @@ uint64_t oracle_chunk_fingerprint(const int32_t *tokens, i64 start, i64 len, uin
   free(buf);
   return h;
 }
+
+/* Gear words from SplitMix64 (Steele, Lea, Flood 2014): G[t] is the (t+1)-th output of the
+ * generator seeded with `seed`, i.e. mix(seed + (t + 1) * gamma) with the generator's output
+ * mix.  An alternative to a stored Gear table. */
+void oracle_splitmix_gear(i64 vocab, uint64_t seed, uint64_t *out) {
+  const uint64_t gamma = 0x9e3779b97f4a7c15ull;
+  for (i64 t = 0; t < vocab; ++t) {
+    uint64_t z = seed + (uint64_t)(t + 1) * gamma;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    out[t] = z ^ (z >> 31);
+  }
+}

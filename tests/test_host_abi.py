@@ -161,3 +161,25 @@ def test_rope_entry_points_reject_bad_specs(irm, bad):
                                      None, None, None, 1000, 0.1, None, None, rp, None, 0, None)
     assert st == -1
     assert "rope" in L.irm_last_error().decode()
+
+
+def test_cdc_sizes_and_slot_layout(irm):
+    nb, slots = irm.cdc_sizes(np.array([0, 100, 100, 1100]))
+    assert slots == (100 // 32 + 1) + 1 + (1000 // 32 + 1)
+    assert list(irm.cdc_slot_base(np.array([0, 100, 100, 1100]))) == [0, 4, 5]
+    assert nb >= 256
+
+
+@pytest.mark.parametrize("bad", [dict(min_len=0), dict(min_len=64, max_len=32), dict(bits=64),
+                                 dict(mode=2), dict(max_len=70000)])
+def test_cdc_rejects_bad_params(irm, bad):
+    with pytest.raises(irm.IrmError) as e:
+        irm.cdc_sizes(np.array([0, 100]), irm.CdcParams.make(**bad))
+    assert e.value.status == -1
+
+
+def test_cdc_rejects_bad_offsets(irm):
+    for offs in ([1, 100], [0, 100, 50]):
+        with pytest.raises(irm.IrmError) as e:
+            irm.cdc_sizes(np.array(offs))
+        assert e.value.status == -1

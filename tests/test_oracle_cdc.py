@@ -137,3 +137,11 @@ def test_cdc_boundaries_follow_content_after_a_shift(oracle_mod):
     tail_a = {x for x in ra if x >= 2048}
     tail_b = {x for x in rb if x >= 2048}
     assert tail_a and tail_a == tail_b
+
+
+def test_splitmix_gear_reference_values(oracle_mod):
+    """Gear words from SplitMix64: word t is the generator's (t+1)-th output."""
+    g = json.load(open(os.path.join(GOLDEN, "splitmix64_reference.json")))
+    for c in g["cases"]:
+        got = oracle_mod.splitmix_gear(len(c["outputs"]), c["seed"])
+        assert [int(x) for x in got] == [int(h, 16) for h in c["outputs"]]
