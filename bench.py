@@ -263,12 +263,12 @@ class Workload:
 
     def launches_per_step(self):
         if self.kind == "cdc":
-            return 4  # slot bases, hash + candidate bits, boundary walk, fingerprints
+            return 5  # base scans, hash + candidate bits, speculative walks, fix-up, fingerprints
         return 1  # one fused kernel per call (the split-KV merge runs inside it)
 
     def kernel_name(self):
         if self.kind == "cdc":
-            return "cdc (4 kernels: base, hash, walk, fingerprint)"
+            return "cdc (5 kernels: base, hash, spec walk, fix-up, fingerprint)"
         if self.kind == "gather":
             return "rotate_gather_kernel"
         if self.kind == "decode" and self.H in (16, 32):
@@ -373,23 +373,34 @@ def roofline(wl: Workload, ms: float, pk):
                 frac=round(ach / pk["hbm"], 4))
 
 
-def kernel_digest():
+KERNEL_SOURCES = {
+    "mla_decode_kernel": ["irm_decode.cu", "irm_pipeline.cuh", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
+    "mla_attn_kernel": ["irm_attn.cu", "irm_pipeline.cuh", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
+    "rotate_gather_kernel": ["irm_gather.cu", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
+}
+
+
+def kernel_digest(kernel=None):
+    """Digest of the sources a kernel is built from (all of csrc/ when kernel is None)."""
+    csrc = os.path.join(ROOT, "mla_position_independent_gb300", "csrc")
+    files = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(csrc))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "mla_position_independent_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "mla_position_independent_gb300", "csrc", f), "rb") as fh:
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(name):
-    """DRAM bytes per launch from the committed ncu summary, if it matches these sources."""
+    """DRAM bytes per launch from the committed ncu summary, if its kernel's sources have not
+    changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(name)
-    if not ent or ent.get("kernel_digest") != kernel_digest():
+    if not ent or ent.get("kernel_digest") != kernel_digest(ent.get("kernel")):
         return None
     return ent.get("dram_bytes_per_launch")
 
