@@ -314,6 +314,51 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, con
                          int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Content-addressed chunk registry and chunk-table assembler (host side): the step that turns a
+ * request into the chunk table the kernels above consume ["Irminsul论文详解" §5: exact prefix
+ * first; then per CDC segment of the tail at target position p: p < 32 is prefilled (first-chunk
+ * carve-out), a registry hit on the segment's fingerprint is reused with delta = p - p_src, a
+ * miss is prefilled and registered at p; §6: the S1 fallback looks a missed chunk up again as
+ * fixed 128-token sub-windows].
+ *   The registry keys chunks by (xxHash64 fingerprint, length) and keeps their rows in a ring of
+ *   pool_rows rows starting at row pool_base of the row store: a newly prefilled chunk takes the
+ *   next rows of the ring (a chunk never wraps around the ring's end), and an entry becomes stale
+ *   once the ring has moved a full turn past its first row (eviction by age).  capacity is the
+ *   expected number of live entries (the table grows when needed).  All calls on one registry are
+ *   serialized by a mutex; the registry is host memory only.
+ */
+typedef struct irm_registry irm_registry;
+irm_status irm_registry_create(int64_t pool_base, int64_t pool_rows, int64_t capacity, irm_registry** out);
+void irm_registry_destroy(irm_registry* reg);
+/* Live (not stale) entries and rows allocated so far. */
+irm_status irm_registry_stats(irm_registry* reg, int64_t* live_entries, int64_t* rows_allocated);
+
+#define IRM_ASSEMBLE_S1 1 /* flags: look missed chunks up again as 128-token sub-windows */
+/*
+ * Chunk table of one request.
+ *   tokens_host   the request's n_tokens token ids (needed with IRM_ASSEMBLE_S1, else may be NULL)
+ *   prefix_len    tokens matched exactly by a prefix cache; they are reused in place from row
+ *                 prefix_row on (one chunk, delta 0, not prefilled)
+ *   seg_*         the n_seg CDC segments of the tail (tokens prefix_len ..), in order: start
+ *                 relative to the tail, length, fingerprint (e.g. irm_cdc_chunk's outputs)
+ *   flags, seed   IRM_ASSEMBLE_S1 or 0; xxHash64 seed of the S1 sub-window fingerprints
+ *   chunks_out    [chunks_cap] the chunk table (irm_chunk, target order, tiling [0, n_tokens));
+ *                 1 + n_seg entries suffice, 1 + sum ceil(len / 128) with IRM_ASSEMBLE_S1
+ *   prefill_out   [chunks_cap] 1 where the caller must prefill the chunk's rows (pool_offset ..
+ *                 pool_offset + len - 1 of the row store, at positions p_tgt ..) before the next
+ *                 request can reuse them; 0 for reused and prefix chunks
+ *   n_chunks_out  entries written
+ * A chunk registered while assembling a request is not reused by later segments of the same
+ * request.  Errors: IRM_ERR_INVALID_ARG for segments that do not tile the tail, a segment longer
+ * than the pool or too small a capacity (nothing is changed then).
+ */
+irm_status irm_registry_assemble(irm_registry* reg, const int32_t* tokens_host, int64_t n_tokens,
+                                 int64_t prefix_len, int64_t prefix_row, const int32_t* seg_start,
+                                 const int32_t* seg_len, const uint64_t* seg_hash, int32_t n_seg,
+                                 int32_t flags, uint64_t seed, irm_chunk* chunks_out,
+                                 uint8_t* prefill_out, int32_t chunks_cap, int32_t* n_chunks_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_c
            "irm_assemble_kv_rope", "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
            "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc",
            "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope",
-           "irm_cdc_sizes", "irm_cdc_chunk"]
+           "irm_cdc_sizes", "irm_cdc_chunk", "irm_registry_create", "irm_registry_stats",
+           "irm_registry_assemble"]
 
 ROPE_NEOX, ROPE_INTERLEAVED = 0, 1
 
@@ -97,6 +98,12 @@ def lib():
                                                 P, P, P, P, SZ, P]
         L.irm_cdc_sizes.argtypes = [P, I, P, P, P]
         L.irm_cdc_chunk.argtypes = [P, P, P, I, P, ctypes.c_int32, P, P, P, P, P, P, SZ, P]
+        L.irm_registry_create.argtypes = [I64, I64, I64, P]
+        L.irm_registry_destroy.argtypes = [P]
+        L.irm_registry_destroy.restype = None
+        L.irm_registry_stats.argtypes = [P, P, P]
+        L.irm_registry_assemble.argtypes = [P, P, I64, I64, I64, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_uint64, P, P, ctypes.c_int32, P]
         for name in EXPORTS:
             if name not in ("irm_status_string", "irm_last_error", "irm_version"):
                 getattr(L, name).restype = I
@@ -329,3 +336,49 @@ def irm_cdc_chunk(tokens: torch.Tensor, offsets: np.ndarray, gear: torch.Tensor 
                                int(vocab), pp, _ptr(n_chunks), _ptr(c_start), _ptr(c_len),
                                _ptr(c_hash), _ptr(workspace), workspace.numel(), _stream(stream)))
     return n_chunks, c_start, c_len, c_hash, workspace
+
+
+ASSEMBLE_S1 = 1
+
+
+class Registry:
+    """Content-addressed chunk registry (host side, libirm's irm_registry): keeps cached chunks'
+    rows in a ring of pool rows and turns a request's CDC segments into a chunk table."""
+
+    def __init__(self, pool_rows: int, pool_base: int = 0, capacity: int = 1 << 16):
+        h = ctypes.c_void_p()
+        _check(lib().irm_registry_create(int(pool_base), int(pool_rows), int(capacity), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().irm_registry_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def stats(self):
+        live, rows = ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(lib().irm_registry_stats(self._h, ctypes.byref(live), ctypes.byref(rows)))
+        return live.value, rows.value
+
+    def assemble(self, tokens, prefix_len, prefix_row, seg_start, seg_len, seg_hash, s1=False,
+                 seed=0):
+        """(chunk table as a CHUNK_DTYPE array, prefill flags uint8) of one request."""
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        st = np.ascontiguousarray(seg_start, dtype=np.int32)
+        ln = np.ascontiguousarray(seg_len, dtype=np.int32)
+        hs = np.ascontiguousarray(np.asarray(seg_hash, dtype=np.uint64))
+        cap = 1 + (int(((ln.astype(np.int64) + 127) // 128).sum()) if s1 else len(ln))
+        out = np.zeros(cap, CHUNK_DTYPE)
+        pre = np.zeros(cap, np.uint8)
+        n = ctypes.c_int32(0)
+        _check(lib().irm_registry_assemble(self._h, _ptr(tokens), int(tokens.shape[0]), int(prefix_len),
+                                           int(prefix_row), _ptr(st), _ptr(ln), _ptr(hs), int(len(st)),
+                                           ASSEMBLE_S1 if s1 else 0, ctypes.c_uint64(seed), _ptr(out),
+                                           _ptr(pre), cap, ctypes.byref(n)))
+        return out[:n.value], pre[:n.value]

@@ -413,6 +413,11 @@ irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_p
 
 }  // namespace
 
+namespace irm {
+// Sets the calling thread's last-error text (used by the registry's translation unit).
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace irm
+
 extern "C" {
 
 const char* irm_status_string(int status) {
