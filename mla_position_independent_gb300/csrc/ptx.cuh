@@ -84,18 +84,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait.  Returns false once kWaitLimitNs has elapsed or *abort_flag != 0.  Between
-// polls the thread sleeps briefly, so waiting warps leave issue slots to working ones.
+// Bounded wait.  Returns false once kWaitLimitNs has elapsed or *abort_flag != 0.  try_wait
+// itself suspends the thread until the phase completes or a hardware time limit passes, so the
+// loop needs no sleep of its own (a sleep only delays the wake-up).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 8; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-      __nanosleep(20);
-    }
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
