@@ -108,3 +108,20 @@ def test_cdc_generated_gear_words(oracle_mod, gear_seed):
     gear = oracle_mod.splitmix_gear(102400, gear_seed)
     _run_and_check(oracle_mod, tokens, offsets, gear, irm.CdcParams.make(gear_seed=gear_seed, seed=5),
                    generated=True)
+
+
+def test_cdc_one_long_stream(oracle_mod):
+    """One stream of 1M tokens: 256 speculative segments whose true starts the fix-up resolves
+    in order; every boundary and sampled fingerprints."""
+    tokens, offsets = synth.cdc_streams(1, 1 << 20, seed=3)
+    gear = oracle_mod.splitmix_gear(102400, 11)
+    n = _run_and_check(oracle_mod, tokens, offsets, gear, irm.CdcParams.make(gear_seed=11), generated=True)
+    assert n > 5000
+
+
+def test_cdc_long_chunks_cross_segments(oracle_mod):
+    """max_len larger than a walk segment (chunks spanning several segments) and a sparse test."""
+    tokens, offsets = synth.cdc_streams(3, 100000, seed=4)
+    gear = oracle_mod.splitmix_gear(102400, 5)
+    _run_and_check(oracle_mod, tokens, offsets, gear,
+                   irm.CdcParams.make(min_len=3000, max_len=20000, bits=12, gear_seed=5), generated=True)

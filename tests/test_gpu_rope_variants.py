@@ -33,7 +33,8 @@ def _spec(name, pairing):
 
 
 def _encode(case, oracle_mod, rope_o):
-    """Cached rows carry RoPE(position) of their content under the variant (bf16)."""
+    """Cached rows carry RoPE(position) of their content under the variant (bf16; rope_o None:
+    the default convention)."""
     if case.rope_rows is None:
         return case
     enc = oracle_mod.rotate(case.rope_content, case.rope_pos, rope=rope_o)
@@ -121,3 +122,61 @@ def test_wrong_rotary_class_changes_the_result(oracle_mod):
                                     case.indptr, kv, SCALE, rope=rope_o)
     assert_close(_attn(case, rope_c, prefill=True), O, "matching class")
     assert rel_l2(_attn(case, None, prefill=True), O) > 2e-2
+
+
+def test_v3_decode_variant_sampled(oracle_mod):
+    """The V3-shaped decode (tile kernel, split-KV) with an interleaved YaRN-like variant on
+    request-private rows encoded by the oracle; sampled (request, head) outputs."""
+    rope_c, rope_o = _spec("yarn", irm.ROPE_INTERLEAVED)
+    case = synth.v3_decode(0, q_std=1.0, device="cuda")
+    rng = np.random.default_rng(8)
+    sel = np.array([[b, 0, h] for b in (0, 31, 63) for h in rng.choice(128, 6, replace=False)])
+    kv = synth.bits(case.kv_rows)
+    O, _ = oracle_mod.mla_attention(synth.bits(case.q_lat), synth.bits(case.q_rope), case.chunks,
+                                    case.indptr, kv, SCALE, select=sel, rope=rope_o)
+    got = _attn(case, rope_c, prefill=False)[sel[:, 0], sel[:, 1], sel[:, 2]]
+    assert_close(got, O, "v3 decode yarn-il")
+
+
+def test_chunked_prefill_variant_sampled(oracle_mod):
+    rope_c, rope_o = _spec("base500k", irm.ROPE_INTERLEAVED)
+    case = synth.chunked_prefill(0, device="cuda", n_q=256)
+    sel = np.array([[b, i, h] for b in (0, 3) for i in (0, 128, 255) for h in (0, 77, 127)])
+    kv = synth.bits(case.kv_rows)
+    O, _ = oracle_mod.mla_attention(synth.bits(case.q_lat), synth.bits(case.q_rope), case.chunks,
+                                    case.indptr, kv, SCALE, select=sel, rope=rope_o)
+    got = _attn(case, rope_c, prefill=True)[sel[:, 0], sel[:, 1], sel[:, 2]]
+    assert_close(got, O, "chunked prefill base500k-il")
+
+
+def test_plain_entry_points_equal_the_default_variant(oracle_mod):
+    """The entry points without a RoPE argument give bit-identical results to the *_rope ones
+    called with NULL (they are the default convention)."""
+    import ctypes
+    case = to_device(_encode(synth.tiny_case(0, q_std=1.0), oracle_mod, None))
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    L = irm.lib()
+    ql, qr = case.q_lat[:, -1].contiguous(), case.q_rope[:, -1].contiguous()
+    ref, _, _ = irm.irm_mla_attn_decode(ql, qr, table, case.kv_rows, SCALE)
+    out = torch.empty_like(ref)
+    ws = irm.new_workspace(irm.decode_workspace_size(table, 16))
+    st = L.irm_mla_attn_decode(ql.data_ptr(), qr.data_ptr(), 1, 16, table.chunks_host.ctypes.data,
+                               table.indptr_host.ctypes.data, table.chunks_dev.data_ptr(),
+                               table.indptr_dev.data_ptr(), case.kv_rows.data_ptr(), case.kv_rows.shape[0],
+                               ctypes.c_float(SCALE), out.data_ptr(), None, ws.data_ptr(), ws.numel(),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    pref, _, _ = irm.irm_mla_attn_prefill(case.q_lat, case.q_rope, table, case.kv_rows, SCALE)
+    out2 = torch.empty_like(pref)
+    ws2 = irm.new_workspace(irm.prefill_workspace_size(1, 16, 16))
+    st = L.irm_mla_attn_prefill(case.q_lat.data_ptr(), case.q_rope.data_ptr(), 1, 16, 16,
+                                table.chunks_host.ctypes.data, table.indptr_host.ctypes.data,
+                                table.chunks_dev.data_ptr(), table.indptr_dev.data_ptr(),
+                                case.kv_rows.data_ptr(), case.kv_rows.shape[0], ctypes.c_float(SCALE),
+                                out2.data_ptr(), None, ws2.data_ptr(), ws2.numel(),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out2, pref)

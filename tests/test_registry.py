@@ -71,3 +71,16 @@ def test_registry_rejects_bad_segments(irm):
         reg.assemble(np.zeros(100, np.int32), 0, 0, [0], [90], [1])             # does not cover
     with pytest.raises(irm.IrmError):
         reg.assemble(np.zeros(2000, np.int32), 0, 0, [0], [2000], [1])         # longer than the pool
+
+
+def test_registry_heavy_eviction_with_s1(irm, oracle_mod):
+    """A pool of 2500 rows (a fraction of one request) with S1: entries go stale all the time;
+    the library and the reference still agree request by request."""
+    from oracle.assembler import Registry as RefRegistry
+    gear = synth.gear_table(20000, seed=10)
+    reg = irm.Registry(pool_rows=2500, capacity=16)
+    ref = RefRegistry(pool_rows=2500)
+    for i, tok in enumerate(_requests(81, 20)):
+        segs = _segments(oracle_mod, tok, gear, 0)
+        got, pre = reg.assemble(tok, 0, 0, *segs, s1=True)
+        assert _as_tuples(got, pre) == ref.assemble(tok, 0, 0, *segs, s1=True), f"request {i}"
