@@ -19,20 +19,25 @@
 //     is bit-identical in both CTAs.
 //   - The output is split the same way: CTA r accumulates O[:, 256r:256r+256) += P V_r
 //     (tcgen05, M=128, N=256) in TMEM, with V_r = the cKV columns it already holds.
-//   - TMEM holds O (256 columns), two score buffers (64 columns each) and the CTA's four
-//     cKV slabs of Q as bf16 pairs (128 columns); the softmax writes P as bf16 pairs over
-//     the score buffer it just read, and both Q.K^T and P.V take their A operand from
-//     TMEM.  Both issuers build their operand descriptors once per tile and step them by
-//     constants (a thread issues one UMMA per ~50 cycles at best, so small UMMAs are
-//     issue-bound).  Only the CTA's half of q_rope sits in shared memory, so nearly all of
-//     shared memory is KV pipeline stages.
+//   - TMEM holds O (256 columns), one score buffer (64 columns), a double buffer for P
+//     (2 x 32 columns of bf16 pairs) and the CTA's four cKV slabs of Q as bf16 pairs (128
+//     columns); both Q.K^T and P.V take their A operand from TMEM.  The softmax warps load
+//     a tile's scores into registers and release the score buffer at once, so the next
+//     Q.K^T never waits for a P.V.  Both issuers build their operand descriptors once per
+//     tile and step them by constants (a thread issues one UMMA per ~50 cycles at best, so
+//     small UMMAs are issue-bound).  Only the CTA's half of q_rope sits in shared memory,
+//     so nearly all of shared memory is KV pipeline stages.
+//   - The softmax is software-pipelined: iteration j combines tile j's own and peer
+//     partials, loads tile j+1's scores, ships them to the peer once the peer has read tile
+//     j's, and then runs tile j's exponentials, so the exchange of one tile overlaps the
+//     softmax of the previous one.
 //   - Warp roles: 0-7 softmax, two warps per TMEM lane quadrant (thread = TMEM lane = query
 //     row; warps 0-3 take keys 0-31 of every tile, warps 4-7 keys 32-63, and the two halves
 //     agree on the row's running max through one barrier reduction per tile); 8-9 gather KV
-//     rows with cp.async following the chunk table (completion tracked by an mbarrier, so
-//     they run ahead across stages); 10-11 rotate each landed tile's k_r by R(delta) and
-//     publish it; 12 allocates TMEM and issues Q.K^T, 13 issues P.V (one issuing thread per
-//     product).
+//     rows with cp.async (completion tracked by an mbarrier, so they run ahead across
+//     stages); 10-11 rotate each landed tile's k_r by R(delta) and publish it; 12 allocates
+//     TMEM and issues Q.K^T, 13 issues P.V (one issuing thread per product); 14 turns the
+//     chunk table into per-tile row maps, up to the stage count ahead of the copies.
 //   - Only the first Mv rows (valid query rows rounded up to 8) of the q_rope slab and the
 //     score exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
 //     whatever follows in shared memory (or TMEM lanes nobody wrote).  Those rows only
@@ -58,7 +63,10 @@ constexpr int kCopyThreads = kCopyWarps * 32;
 constexpr int kPubWarps = kLoaderWarps - kCopyWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 12: TMEM allocation, Q.K^T issue
 constexpr int kPvWarp = kMmaWarp + 1;                    // 13: P.V issue
-constexpr int kThreads = (kPvWarp + 1) * 32;             // 448
+constexpr int kMapWarp = kPvWarp + 1;                    // 14: row maps, ahead of the copies
+constexpr int kThreads = (kMapWarp + 1) * 32;            // 480
+constexpr int kCopyRowsPerPass = kCopyThreads / 8;       // rows one pass of the copy warps covers
+constexpr int kCopyPasses = (kBN + kCopyRowsPerPass - 1) / kCopyRowsPerPass;
 constexpr int kMaxStages = 6;
 constexpr uint32_t kSlabKV = kBN * 128;  // one 64-column slab of a KV tile
 constexpr uint32_t kSmemLimit = 232448 - 128;  // opt-in maximum, less room for static shared memory
@@ -86,9 +94,10 @@ enum : int {
   BAR_KV_EMPTY = BAR_KV_FULL + kMaxStages,  // [kMaxStages] UMMA commit after P.V of the stage
   BAR_LANDED = BAR_KV_EMPTY + kMaxStages,   // [kMaxStages] every copy thread's copies landed
   BAR_MAP = BAR_LANDED + kMaxStages,        // [kMaxStages] row map of the stage published
-  BAR_S_FULL = BAR_MAP + kMaxStages,        // [2] UMMA commit after Q.K^T into S buffer
-  BAR_PV_DONE = BAR_S_FULL + 2,             // [2] UMMA commit after P.V of the P in S buffer
-  BAR_P_FULL = BAR_PV_DONE + 2,             // [2] softmax wrote P over S buffer (and rescaled O) (count 8)
+  BAR_S_FULL = BAR_MAP + kMaxStages,        // UMMA commit after Q.K^T into the score buffer
+  BAR_S_EMPTY = BAR_S_FULL + 1,             // softmax warps loaded the score buffer (count 8)
+  BAR_PV_DONE = BAR_S_EMPTY + 1,            // [2] UMMA commit after P.V of P buffer
+  BAR_P_FULL = BAR_PV_DONE + 2,             // [2] softmax wrote P buffer (and rescaled O) (count 8)
   BAR_Q_FULL = BAR_P_FULL + 2,              // softmax warps stored Q in TMEM (count 8)
   BAR_X_FULL = BAR_Q_FULL + 1,              // peer's partial scores landed (1 arrive + tx)
   BAR_X_EMPTY = BAR_X_FULL + 1,             // peer's 8 softmax warps consumed our scores (remote)
@@ -98,7 +107,8 @@ enum : int {
 static_assert(NUM_BARS <= 64, "barrier area");
 
 constexpr uint32_t kTmemO = 0;    // O half: 256 fp32 columns
-constexpr uint32_t kTmemS = 256;  // S double buffer: 2 x 64 columns (P overwrites the first 32)
+constexpr uint32_t kTmemS = 256;  // score buffer: 64 fp32 columns
+constexpr uint32_t kTmemP = 320;  // P double buffer: 2 x 32 columns of bf16 pairs
 constexpr uint32_t kTmemQ = 384;  // Q, cKV slabs 0-3: 4 x 32 columns of bf16 pairs
 constexpr uint32_t kTmemCols = 512;
 
@@ -190,8 +200,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_LANDED + s), kCopyThreads);
       mbar_init(bar(BAR_MAP + s), 1);
     }
+    mbar_init(bar(BAR_S_FULL), 1);
+    mbar_init(bar(BAR_S_EMPTY), kSoftmaxWarps);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(BAR_S_FULL + s), 1);
       mbar_init(bar(BAR_PV_DONE + s), 1);
       mbar_init(bar(BAR_P_FULL + s), kSoftmaxWarps);
     }
@@ -217,8 +228,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ======================= loaders =====================================================
-    // Warps 8-9 gather KV rows with cp.async following the chunk table (warp 8 also builds the
-    // row maps); warps 10-11 wait for each tile's bytes to land, rotate this CTA's k_r pairs by
+    // Warps 8-9 gather KV rows with cp.async following the row maps that warp 14 builds from
+    // the chunk table; warps 10-11 wait for each tile's bytes to land, rotate this CTA's k_r pairs by
     // R(delta) in shared memory and publish the tile.  Every role blocks in mbarrier waits, so
     // no loader warp spins for issue slots the softmax warps need, and the copies run up to NS
     // tiles ahead.  The Q.K^T issuer fences the bytes for the async proxy after acquiring
@@ -249,32 +260,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
         }
       }
-      // Copy warp 0 keeps a window of 32 chunk records (one per lane) and turns it into
-      // per-tile row maps: source row (-1 = outside the context, zero filled) and delta.
-      ChunkWindow cw;
-      cw.chunks = a.chunks;
-      cw.c_end = c_end;
-      cw.win = c_begin;
-      if (lw == 0 && ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
       int s = 0;
       uint32_t ph = 0;
       for (int j = 0; j < ntiles; ++j) {
-        if (lw == 0) {
-          // the map slot is free once tile j-NS was published; build the map now, while stage
-          // s may still be in use by the P.V of tile j-NS
-          if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
-          cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + s * kBN, map_delta + s * kBN, a.status, lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
-        }
         // stage s is free once the P.V of tile j-NS completed
         if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
         if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
         const uint32_t stage = sb + L.kv + (uint32_t)s * L.stage;
-#pragma unroll 2
-        for (int rr = 0; rr < kBN; rr += kCopyThreads / 8) {
-          const int row = rr + rsub;
-          const int sr = map_src[s * kBN + row];
+        // all of this thread's source rows first, then every copy of the tile back to back
+        int srs[kCopyPasses];
+#pragma unroll
+        for (int p = 0; p < kCopyPasses; ++p) {
+          const int row = p * kCopyRowsPerPass + rsub;
+          srs[p] = row < kBN ? map_src[s * kBN + row] : -1;
+        }
+#pragma unroll
+        for (int p = 0; p < kCopyPasses; ++p) {
+          const int row = p * kCopyRowsPerPass + rsub;
+          if (row >= kBN) break;
+          const int sr = srs[p];
           const __nv_bfloat16* kvrow = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow;
           const __nv_bfloat16* rowp = kvrow + col0 + chk * 8;
           const uint32_t dst = stage + sw128_offset(row, chk);
@@ -336,14 +340,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t aq = sdesc_sw128(sb + L.qr, 16, 1024);  // the q_rope half (A, K-major)
       for (int ns = 0; ns < ntiles && ok; ++ns) {
         if (!(ok = mbar_wait(bar(BAR_KV_FULL + ss), phs, abort_flag))) break;
-        // score buffer ns&1 holds P of tile ns-2 until that tile's P.V has completed
-        if (ns >= 2 && !(ok = mbar_wait(bar(BAR_PV_DONE + (ns & 1)), ((ns >> 1) - 1) & 1, abort_flag))) break;
+        // the score buffer is free once the softmax warps have loaded tile ns-1's scores
+        if (ns >= 1 && !(ok = mbar_wait(bar(BAR_S_EMPTY), (ns - 1) & 1, abort_flag))) break;
         // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads
         tc_fence_after();
         fence_proxy_async_smem();
         const uint64_t bd = sdesc_sw128(sb + L.kv + (uint32_t)ss * L.stage, 16, 1024);
         const uint64_t bk = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64, 16, 1024);
-        const uint32_t tS = tmem + kTmemS + 64u * (uint32_t)(ns & 1);
+        const uint32_t tS = tmem + kTmemS;
 #pragma unroll
         for (int slab = 0; slab < 4; ++slab) {
 #pragma unroll
@@ -354,7 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)  // the half k_r slab: 32 columns, 2 K-steps
           umma_bf16(tS, sdesc_add(aq, kk * 32), sdesc_add(bk, kk * 32), kIdescS, 1u);
-        umma_commit(bar(BAR_S_FULL + (ns & 1)));
+        umma_commit(bar(BAR_S_FULL));
         if (++ss == NS) {
           ss = 0;
           phs ^= 1u;
@@ -368,6 +372,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(BAR_DRAIN), 0, nullptr)) set_status(a.status, kDevErrTimeout);
     }
     __syncwarp();
+  } else if (warp == kMapWarp) {
+    // ======================= row maps ====================================================
+    // A window of 32 chunk records (one per lane) turned into each tile's row map: source
+    // row (-1 = outside the context, zero filled) and delta.  The map of tile j goes into
+    // slot j % NS once tile j-NS has been published (its copies issued and its k_r rotated),
+    // so maps are ready up to NS tiles ahead of the copies.
+    ChunkWindow cw;
+    cw.chunks = a.chunks;
+    cw.c_end = c_end;
+    cw.win = c_begin;
+    bool ok = true;
+    if (ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
+      cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + s * kBN, map_delta + s * kBN, a.status, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.status, kDevErrTimeout);
+    }
   } else if (warp == kPvWarp) {
     // ======================= P.V issuer (one thread) =====================================
     if (lane == 0 && ntiles > 0) {
@@ -378,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t bv = sdesc_sw128(sb + L.kv + (uint32_t)sp * L.stage, kSlabKV, 1024);
-        const uint32_t tP = tmem + kTmemS + 64u * (uint32_t)(np & 1);
+        const uint32_t tP = tmem + kTmemP + 32u * (uint32_t)(np & 1);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16_ts(tO, tP + 8u * kk, sdesc_add(bv, kk * 2048), kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
@@ -445,57 +477,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(BAR_Q_FULL));
+    // This half's partial scores of one tile (the CTA's share of the contraction), loaded from
+    // the score buffer, which is released at once, and rounded to fp16 pairs exactly as the
+    // peer receives them.
+    auto load_scores = [&](int t, uint32_t (&w)[16]) -> bool {
+      if (!warp_wait(bar(BAR_S_FULL), (uint32_t)t & 1u, abort_flag)) return false;
+      tc_fence_after();
+      uint32_t r[32];
+      if (warp_live) {
+        tmem_ld32(tmem + kTmemS + 32u * (uint32_t)half + lane_base, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      return true;
+    };
+    // Ship them to the peer's exchange buffer (transposed: word (4 half + i) of row m).
+    auto send_scores = [&](const uint32_t (&w)[16]) {
+      if (row_live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_async_v4_b32(rX + (uint32_t)((4 * half + i) * Mv + m) * 16u,
+                          make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]), rXfull);
+      }
+    };
+    // Software pipeline: iteration j combines tile j's own and peer partials, loads tile
+    // j+1's scores (freeing the score buffer for the next Q.K^T), ships them once the peer
+    // has read tile j's (normally long since), and runs tile j's softmax.  P goes to its own
+    // double buffer, so the score buffer never waits for a P.V.
+    uint32_t own[16];  // this half's partial scores of the tile in flight (fp16 pairs)
+    if (ntiles > 0) {
+      if (m == 0 && half == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
+      ok = load_scores(0, own);
+      if (ok) send_scores(own);
+    }
     // Every softmax warp runs every iteration up to the tile's barrier reduction, also after a
     // failed wait (it then skips its work): the reduction tells all 256 threads of a failure,
     // and they leave the loop together, so no warp is left waiting at a named barrier.
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
       const int T = (kb + j) * kBN + 32 * half;  // position of this half's first key
+      const bool more = j + 1 < ntiles;
+      // the peer's partial scores of tile j
+      if (ok) ok = warp_wait_cluster(bar(BAR_X_FULL), (uint32_t)j & 1u, abort_flag);
       float sv[32];
-      if (ok) ok = warp_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        if (warp_live) {
-          uint32_t r[32];
-          tmem_ld32(tmem + kTmemS + 64u * (uint32_t)s + 32u * (uint32_t)half + lane_base, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-        }
-        // exchange partial scores with the peer (each side owns part of the contraction)
-        if (j >= 1) ok = warp_wait_cluster(bar(BAR_X_EMPTY), (j - 1) & 1, abort_flag);
-      }
-      if (ok) {
-        if (m == 0 && half == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
-        if (row_live) {
-          // own partial rounded to fp16 exactly as the peer receives it, packed 8 per 16 bytes
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            __half2 h;
-            h = __floats2half2_rn(sv[8 * i], sv[8 * i + 1]);
-            w.x = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(sv[8 * i + 2], sv[8 * i + 3]);
-            w.y = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(sv[8 * i + 4], sv[8 * i + 5]);
-            w.z = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(sv[8 * i + 6], sv[8 * i + 7]);
-            w.w = *reinterpret_cast<uint32_t*>(&h);
-            st_async_v4_b32(rX + (uint32_t)((4 * half + i) * Mv + m) * 16u, w, rXfull);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
-              sv[8 * i + 2 * k] = f.x;
-              sv[8 * i + 2 * k + 1] = f.y;
-            }
-          }
-        }
-        ok = warp_wait_cluster(bar(BAR_X_FULL), j & 1, abort_flag);
-      }
       float lmx = -INFINITY;
       bool need = false;
       if (ok) {
+        // the barrier's next phase expects the peer's tile j+1 bytes
+        if (more && m == 0 && half == 0) mbar_arrive_expect_tx(bar(BAR_X_FULL), (uint32_t)Mv * kBN * 2u);
         if (row_live) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -503,9 +541,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
-              sv[8 * i + 2 * k] += f.x;
-              sv[8 * i + 2 * k + 1] += f.y;
+              const float2 f = add_f16x2_f16x2_f32(own[4 * i + k], vv[k]);
+              sv[8 * i + 2 * k] = f.x;
+              sv[8 * i + 2 * k + 1] = f.y;
             }
           }
         }
@@ -513,6 +551,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this warp is done with the peer's scores (the values are in registers and used, so
         // a relaxed arrive suffices; a release would stall on this lane's outstanding st.async)
         if (lane == 0) mbar_arrive_remote_relaxed(rXempty);
+        // tile j+1's scores (own[] is free again)
+        if (more) ok = load_scores(j + 1, own);
+      }
+      if (ok) {
         if (row_live) {
           // causal mask t <= pos_m, only on tiles that reach past the tile's first query
           if (T + 31 > pos_first) {
@@ -534,10 +576,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           need = (m < rows_valid) && (lmx > m_run + 8.f);
         }
       }
-      // One reduction per tile over both halves (and a fence pair around it): it orders both
-      // halves' reads of the score buffer before either writes P over it, and flags the rare
-      // tile where a row's max moves or a wait failed.
-      tc_fence_before();
+      // One reduction per tile over both halves: it flags the rare tile where a row's max
+      // moves or a wait failed (and a second one agrees on the new max or on leaving).
       if (named_bar_red_or(kBarSmRed, kSoftmaxThreads, need || !ok)) {
         half_max[half * kBM + m] = lmx;
         if (named_bar_red_or(kBarSmRed2, kSoftmaxThreads, !ok)) {
@@ -546,7 +586,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         lmx = fmaxf(lmx, half_max[(half ^ 1) * kBM + m]);  // the row's max over both halves
       }
-      tc_fence_after();
       const bool want = (m < rows_valid) && (lmx > m_run + 8.f);  // same in both halves
       const float corr = want ? fast_exp2(m_run - lmx) : 1.f;
       if (j > 0 && __any_sync(FULL, want)) {
@@ -571,6 +610,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_run *= corr;
         m_run = lmx;
       }
+      // tile j+1's partials to the peer, once the peer's warps have read tile j's
+      if (ok && more) {
+        ok = warp_wait_cluster(bar(BAR_X_EMPTY), (uint32_t)j & 1u, abort_flag);
+        if (ok) send_scores(own);
+      }
       uint32_t pk[16];
       if (row_live) {
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
@@ -589,15 +633,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
       }
-      // P over the first 32 columns of the score buffer just read (bf16 pairs): this half's
-      // 32 keys are columns 16 * half .. 16 * half + 15
-      if (warp_live) {
-        tmem_st16(tmem + kTmemS + 64u * (uint32_t)s + 16u * (uint32_t)half + lane_base, pk);
+      // P buffer j&1 is free once the P.V of tile j-2 has completed; this half's 32 keys are
+      // its columns 16 * half .. 16 * half + 15 (bf16 pairs)
+      if (ok && j >= 2) ok = warp_wait(bar(BAR_PV_DONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag);
+      if (ok && warp_live) {
+        tc_fence_after();
+        tmem_st16(tmem + kTmemP + 32u * (uint32_t)(j & 1) + 16u * (uint32_t)half + lane_base, pk);
         tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + s));
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (j & 1)));
     }
     if (ok && ntiles > 0)
       ok = warp_wait(bar(BAR_PV_DONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, abort_flag);
