@@ -32,8 +32,9 @@
 //     j's, and then runs tile j's exponentials, so the exchange of one tile overlaps the
 //     softmax of the previous one.
 //   - Warp roles: 0-7 softmax, two warps per TMEM lane quadrant (thread = TMEM lane = query
-//     row; warps 0-3 take keys 0-31 of every tile, warps 4-7 keys 32-63, and the two halves
-//     agree on the row's running max through one barrier reduction per tile); 8-9 gather KV
+//     row; warps 0-3 take keys 0-31 of every tile, warps 4-7 keys 32-63, and the two warps
+//     of a quadrant agree on their rows' running max through one 64-thread barrier
+//     reduction per tile); 8-9 gather KV
 //     rows with cp.async (completion tracked by an mbarrier, so they run ahead across
 //     stages); 10-11 rotate each landed tile's k_r by R(delta) and publish it; 12 allocates
 //     TMEM and issues Q.K^T, 13 issues P.V (one issuing thread per product); 14 turns the
@@ -83,11 +84,13 @@ constexpr uint32_t kOffHalfL = kOffHalfMax + 2 * 128 * 4;   // float [2 halves][
 constexpr uint32_t kFixedBytes = 6144;
 static_assert(kOffHalfL + 2 * 128 * 4 <= kFixedBytes, "fixed area overflow");
 
-// Named barriers (0 is __syncthreads): the softmax warps' per-tile reduction and the rare
-// second round of it, and the split-KV completion count.
-constexpr int kBarSmRed = 2;
-constexpr int kBarSmRed2 = 3;
+// Named barriers (0 is __syncthreads): the split-KV completion count, the softmax warps'
+// final row sums, and per TMEM lane quadrant (the two warps that share its rows) the per-tile
+// reduction and the rare second round of it.
 constexpr int kBarSmMerge = 1;
+constexpr int kBarSmRed2 = 3;
+constexpr int kBarPairRed = 4;   // 4 .. 7
+constexpr int kBarPairRed2 = 8;  // 8 .. 11
 
 enum : int {
   BAR_KV_FULL = 0,                      // [kMaxStages] publishers published the tile (count 2)
@@ -521,8 +524,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (ok) send_scores(own);
     }
     // Every softmax warp runs every iteration up to the tile's barrier reduction, also after a
-    // failed wait (it then skips its work): the reduction tells all 256 threads of a failure,
-    // and they leave the loop together, so no warp is left waiting at a named barrier.
+    // failed wait (it then skips its work): the reduction tells both warps of a quadrant of a
+    // failure, and they leave the loop together, so no warp is left waiting at a named
+    // barrier; the abort flag they raise makes the other quadrants' waits give up as well.
     for (int j = 0; j < ntiles; ++j) {
       const int T = (kb + j) * kBN + 32 * half;  // position of this half's first key
       const bool more = j + 1 < ntiles;
@@ -551,8 +555,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this warp is done with the peer's scores (the values are in registers and used, so
         // a relaxed arrive suffices; a release would stall on this lane's outstanding st.async)
         if (lane == 0) mbar_arrive_remote_relaxed(rXempty);
-        // tile j+1's scores (own[] is free again)
-        if (more) ok = load_scores(j + 1, own);
+        // tile j+1's scores (own[] is free again), shipped once the peer has read tile j's
+        if (more) {
+          ok = load_scores(j + 1, own);
+          if (ok) ok = warp_wait_cluster(bar(BAR_X_EMPTY), (uint32_t)j & 1u, abort_flag);
+          if (ok) send_scores(own);
+        }
       }
       if (ok) {
         if (row_live) {
@@ -576,12 +584,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           need = (m < rows_valid) && (lmx > m_run + 8.f);
         }
       }
-      // One reduction per tile over both halves: it flags the rare tile where a row's max
-      // moves or a wait failed (and a second one agrees on the new max or on leaving).
-      if (named_bar_red_or(kBarSmRed, kSoftmaxThreads, need || !ok)) {
+      // One reduction per tile over the quadrant's two warps (both halves of its rows): it
+      // flags the rare tile where a row's max moves or a wait failed (and a second one agrees
+      // on the new max or on leaving).
+      if (named_bar_red_or(kBarPairRed + wq, 64, need || !ok)) {
         half_max[half * kBM + m] = lmx;
-        if (named_bar_red_or(kBarSmRed2, kSoftmaxThreads, !ok)) {
+        if (named_bar_red_or(kBarPairRed2 + wq, 64, !ok)) {
           ok = false;
+          *abort_flag = 1;  // the other quadrants' waits give up too
           break;
         }
         lmx = fmaxf(lmx, half_max[(half ^ 1) * kBM + m]);  // the row's max over both halves
@@ -609,11 +619,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (want) {
         l_run *= corr;
         m_run = lmx;
-      }
-      // tile j+1's partials to the peer, once the peer's warps have read tile j's
-      if (ok && more) {
-        ok = warp_wait_cluster(bar(BAR_X_EMPTY), (uint32_t)j & 1u, abort_flag);
-        if (ok) send_scores(own);
       }
       uint32_t pk[16];
       if (row_live) {
