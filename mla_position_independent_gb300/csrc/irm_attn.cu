@@ -37,8 +37,8 @@
 //     reduction per tile); 8-9 gather KV
 //     rows with cp.async (completion tracked by an mbarrier, so they run ahead across
 //     stages); 10-11 rotate each landed tile's k_r by R(delta) and publish it; 12 allocates
-//     TMEM and issues Q.K^T, 13 issues P.V (one issuing thread per product); 14 turns the
-//     chunk table into per-tile row maps, up to the stage count ahead of the copies.
+//     TMEM; 13 issues P.V and 15 Q.K^T (one issuing thread per product); 14 turns the chunk
+//     table into per-tile row maps, up to the stage count ahead of the copies.
 //   - Only the first Mv rows (valid query rows rounded up to 8) of the q_rope slab and the
 //     score exchange are stored: the UMMA still reads 128 rows, and the rows past Mv read
 //     whatever follows in shared memory (or TMEM lanes nobody wrote).  Those rows only
@@ -62,10 +62,11 @@ constexpr int kLoaderWarps = 4;   // 2 copy warps + 2 publishers
 constexpr int kCopyWarps = 2;
 constexpr int kCopyThreads = kCopyWarps * 32;
 constexpr int kPubWarps = kLoaderWarps - kCopyWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 12: TMEM allocation, Q.K^T issue
+constexpr int kMmaWarp = kSoftmaxWarps + kLoaderWarps;  // 12: TMEM allocation
 constexpr int kPvWarp = kMmaWarp + 1;                    // 13: P.V issue
 constexpr int kMapWarp = kPvWarp + 1;                    // 14: row maps, ahead of the copies
-constexpr int kThreads = (kMapWarp + 1) * 32;            // 480
+constexpr int kSWarp = kMapWarp + 1;                     // 15: Q.K^T issue
+constexpr int kThreads = (kSWarp + 1) * 32;              // 512
 constexpr int kCopyRowsPerPass = kCopyThreads / 8;       // rows one pass of the copy warps covers
 constexpr int kCopyPasses = (kBN + kCopyRowsPerPass - 1) / kCopyRowsPerPass;
 constexpr int kMaxStages = 6;
@@ -333,8 +334,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       set_status(a.status, kDevErrTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kSWarp) {
     // ======================= Q.K^T issuer (one thread) ===================================
+    // (warp 15, the only one of its SM sub-partition besides two softmax warps and a
+    // publisher: its issue slots are the least contended)
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(bar(BAR_Q_FULL), 0, abort_flag);
       tc_fence_after();
@@ -375,6 +378,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(BAR_DRAIN), 0, nullptr)) set_status(a.status, kDevErrTimeout);
     }
     __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // TMEM allocation and release only
   } else if (warp == kMapWarp) {
     // ======================= row maps ====================================================
     // A window of 32 chunk records (one per lane) turned into each tile's row map: source

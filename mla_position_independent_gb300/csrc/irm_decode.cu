@@ -193,14 +193,27 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   const int crank = split % C, g = split / C;
   const int b = blockIdx.y;
 
-  int c_begin = a.indptr[b], c_end = a.indptr[b + 1];
-  int ctx = 0;
-  const bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks;
+  int c_begin, c_end, ctx = 0, c_first = -1;
+  if (a.n_hints > 0) {
+    const DecodeHint hint = a.hint[b * C * G + split];
+    c_begin = hint.c_begin;
+    c_end = hint.c_end;
+    ctx = hint.ctx;
+    c_first = hint.c_first;
+  } else {
+    c_begin = a.indptr[b];
+    c_end = a.indptr[b + 1];
+  }
+  const bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks &&
+                        (c_first < 0 || (c_first >= c_begin && c_first < c_end));
   if (table_ok) {
-    const irm_chunk last = a.chunks[c_end - 1];
-    ctx = last.p_tgt + last.len;
+    if (a.n_hints == 0) {
+      const irm_chunk last = a.chunks[c_end - 1];
+      ctx = last.p_tgt + last.len;
+    }
   } else {
     c_begin = c_end = 0;
+    c_first = -1;
   }
   const int kv_tiles = (table_ok && ctx > 0) ? (ctx + kBN - 1) / kBN : 0;
   const int kb = (int)((int64_t)split * kv_tiles / (C * G));
@@ -357,7 +370,14 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     cw.c_end = c_end;
     cw.win = c_begin;
     bool ok = true;
-    if (ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
+    if (ntiles > 0) {
+      if (c_first >= 0) {
+        cw.win = c_first;  // the chunk holding the split's first row (launch hint)
+        cw.load(lane);
+      } else {
+        cw.seek(c_begin, kb * kBN, lane);
+      }
+    }
     for (int t = 0; t < ntiles && ok; ++t) {
       const int ks = t % kKrSlots;
       if (t >= kKrSlots &&
@@ -430,19 +450,19 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         tc_fence_after();
         const uint32_t pb = sb + L.p + (uint32_t)(np & 1) * H * 128u;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = sdesc_sw128(pb + kk * 32, 16, 1024);
+        for (int blk = 0; blk < 4; ++blk) {
+          // V^T block = slab pair blk: M atoms (64 columns) 1024 B apart, 8-row K groups
+          // 2048 B apart, 16 KV rows per K-step; the unit is released as soon as its own
+          // four UMMAs complete
+          const uint32_t ub = sb + L.ring + (uint32_t)((4 * np + blk) % L.units) * kPairBytes;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            // V^T block = slab pair blk: M atoms (64 columns) 1024 B apart, 8-row K groups
-            // 2048 B apart, 16 KV rows per K-step
-            const uint32_t ub = sb + L.ring + (uint32_t)((4 * np + blk) % L.units) * kPairBytes;
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc_sw128(pb + kk * 32, 16, 1024);
             const uint64_t ad = sdesc_sw128(ub + kk * 4096, 1024, 2048);
             umma_bf16(tmem + kTmemO + (uint32_t)(blk * H), ad, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
           }
+          umma_commit(bar(BAR_PAIR_EMPTY + (4 * np + blk) % L.units));
         }
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) umma_commit(bar(BAR_PAIR_EMPTY + (4 * np + blk) % L.units));
         umma_commit(bar(BAR_PV_DONE + (np & 1)));
       }
       if (!ok) {

@@ -302,6 +302,23 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     d.status = static_cast<int*>(workspace);
     std::memcpy(d.phase.F, phaseF, sizeof d.phase.F);
     d.interleaved = interleaved;
+    const int splits = pl.C * pl.G;
+    if ((int64_t)B * splits <= irm::kDecodeHints) {
+      // each split's start, from the validated host table (the kernels use the same split
+      // boundaries: split sp of a request starts at tile sp * tiles / splits)
+      d.n_hints = B * splits;
+      for (int b = 0; b < B; ++b) {
+        const int cb = indptr_host[b], ce = indptr_host[b + 1];
+        const int64_t ctx = info.ctx[b];
+        const int64_t tiles = (ctx + kBN - 1) / kBN;
+        int c = cb;
+        for (int sp = 0; sp < splits; ++sp) {
+          const int64_t t0 = (int64_t)sp * tiles / splits * kBN;
+          while (c + 1 < ce && chunks_host[c + 1].p_tgt <= t0) ++c;
+          d.hint[b * splits + sp] = irm::DecodeHint{cb, ce, (int32_t)ctx, c};
+        }
+      }
+    }
     cudaError_t e = irm::launch_mla_decode(d, stream);
     if (e != cudaSuccess) return cuda_fail(e, "mla decode launch");
     return IRM_OK;

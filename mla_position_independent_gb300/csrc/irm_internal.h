@@ -63,6 +63,14 @@ struct AttnArgs {
 // Split-KV decode for a few heads (one query token per request): one CTA per (request,
 // split), the C splits of a request in one cluster that merges them in shared memory.
 constexpr int kMaxDecodeCluster = 16;
+// Where a decode split starts, taken from the validated host copy of the chunk table when
+// the launch has at most kDecodeHints splits: its request's chunk range [c_begin, c_end) and
+// context, and the chunk that holds the split's first row.  The kernel then starts without
+// the dependent reads of indptr, the last chunk and the search for its first chunk.
+struct DecodeHint {
+  int32_t c_begin, c_end, ctx, c_first;
+};
+constexpr int kDecodeHints = 256;
 struct DecodeArgs {
   const void* q_lat;    // bf16 [B, H, 512]
   const void* q_rope;   // bf16 [B, H, 64]
@@ -85,6 +93,8 @@ struct DecodeArgs {
   struct {
     uint64_t F[32];
   } phase;
+  int n_hints;      // B * C * G when the hints below are filled in, else 0
+  DecodeHint hint[kDecodeHints];  // [b * C * G + split]
 };
 
 // Content-defined chunking of a batch of token streams.
