@@ -237,6 +237,16 @@ def test_decode_many_requests(oracle_mod):
     _check_attn(case, oracle_mod, prefill=False, select=sel, what="decode 40 requests")
 
 
+@pytest.mark.parametrize("H", [16, 32])
+def test_decode_beyond_launch_hints(oracle_mod, H):
+    """300 short requests: more decode splits than the launch arguments carry start hints for,
+    so every CTA finds its request's chunk range and first chunk from the device table."""
+    ctxs = [40 + (7 * b) % 170 for b in range(300)]
+    case = _ragged_decode_case(ctxs, H, seed=11 + H)
+    sel = np.array([[b, 0, h] for b in (0, 1, 150, 257, 299) for h in (0, H // 2, H - 1)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel, what=f"decode 300 requests H={H}")
+
+
 def test_device_table_mismatch_is_recorded_not_faulted(oracle_mod):
     """A device chunk table whose rows leave the row store (the host copy is valid) is caught
     by the kernels' bounds check: rows are zero filled and the status word is set."""
