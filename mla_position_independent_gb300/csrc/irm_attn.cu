@@ -119,6 +119,29 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);   // A, B K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 256, 0, 1);  // B (cKV tile) MN-major
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Two fp32 values in one 64-bit register pair, and the paired fp32 FMA / add of sm_100 and
+// later (each lane rounds exactly as fmaf / + would).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 constexpr uint32_t FULL = kFullMask;
 
 // Shared-memory layout for a given number of stored query rows (Mv, multiple of 8), the same
@@ -628,17 +651,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pk[16];
       if (row_live) {
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        const float c = a.scale_log2;
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2), m2 = f2_pack(-m_use, -m_use);
+        uint64_t part[2] = {0ull, 0ull};  // paired partial sums
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = fast_exp2(fmaf(sv[i], c, -m_use));
-          const float p1 = fast_exp2(fmaf(sv[i + 1], c, -m_use));
-          part[(i >> 1) & 3] += p0 + p1;
+          const float2 x = f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), c2, m2));
+          const float p0 = fast_exp2(x.x);
+          const float p1 = fast_exp2(x.y);
+          part[(i >> 1) & 1] = f2_add(part[(i >> 1) & 1], f2_pack(p0, p1));
           const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
           pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        l_run += (part[0] + part[1]) + (part[2] + part[3]);
+        const float2 s01 = f2_unpack(f2_add(part[0], part[1]));
+        l_run += s01.x + s01.y;
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
