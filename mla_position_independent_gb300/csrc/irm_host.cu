@@ -139,18 +139,21 @@ constexpr int kBM = 128;
 constexpr int kBN = 64;
 
 // Decode split-KV factor: the attention runs one 2-CTA cluster per (request, split); pick the
-// split count that minimises waves x (tiles per split + fixed cost), charging each split
-// for the merge its query tile then needs (in tile-equivalents, grows with the head count).
+// split count that minimises waves x (tiles per split + the fixed cost of a split) plus the
+// merge of the splits' partials.  In tile times (measured on the V3-shaped decode): a split's
+// pipeline fill and epilogue cost ~12 tiles, and the merge reads each split's fp32 partial,
+// ~3.6 tiles per split for 128 query rows (fewer rows, proportionally less).
 int choose_splits(int B, int64_t max_ctx, int H, int sms) {
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles = (max_ctx + kBN - 1) / kBN;
-  const double merge_per_split = 0.25 + 0.02 * H;
+  const double split_cost = 12.0;
+  const double merge_per_split = 3.6 * std::min(H, kBM) / kBM;
   int best = 1;
   double best_cost = 1e30;
   for (int S = 1; S <= 64 && S <= tiles; ++S) {
     const int64_t units = (int64_t)B * S;
     const int64_t waves = (units + pairs - 1) / pairs;
-    const double cost = (double)waves * ((double)((tiles + S - 1) / S) + 3.0) +
+    const double cost = (double)waves * ((double)((tiles + S - 1) / S) + split_cost) +
                         (S > 1 ? merge_per_split * S : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;

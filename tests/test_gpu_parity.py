@@ -237,6 +237,16 @@ def test_decode_many_requests(oracle_mod):
     _check_attn(case, oracle_mod, prefill=False, select=sel, what="decode 40 requests")
 
 
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("ctxs", [[8192], [8192, 3000]])
+def test_decode_split_kv(oracle_mod, H, ctxs):
+    """One or two long requests with many heads: the tile kernel splits each request's KV
+    over several clusters and merges their partials (the last cluster of a query tile)."""
+    case = _ragged_decode_case(ctxs, H, seed=7 + H)
+    sel = np.array([[b, 0, h] for b in range(len(ctxs)) for h in (0, 1, H // 2, H - 1)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel, what=f"split-KV decode H={H} ctxs={ctxs}")
+
+
 @pytest.mark.parametrize("H", [16, 32])
 def test_decode_beyond_launch_hints(oracle_mod, H):
     """300 short requests: more decode splits than the launch arguments carry start hints for,

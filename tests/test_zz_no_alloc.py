@@ -57,17 +57,21 @@ def test_noalloc_rejects_decode_larger_than_its_scratch():
         pytest.skip("no GPU")
     import mla_position_independent_gb300 as irm
     L = irm.lib()
-    # 64 requests x 128 heads x 32768 rows needs more split-KV scratch than the array holds
-    reqs = [[(0, 32, 0, 0), (32, 32736, 0, 0)] for _ in range(64)]
-    chunks, indptr = synth.make_table(reqs)
+    # a batch of long 128-head requests whose split-KV scratch is more than the array holds
+    # (how far a decode is split depends on the device, so a few batch sizes are tried)
     need = ctypes.c_size_t(0)
-    assert L.irm_mla_attn_decode_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 64, 128,
-                                                ctypes.byref(need)) == 0
-    if need.value <= 32 << 20:
-        pytest.skip("this device splits the decode too little to exceed the scratch")
+    for B in (48, 64, 96, 128, 192):
+        reqs = [[(0, 32, 0, 0), (32, 32736, 0, 0)] for _ in range(B)]
+        chunks, indptr = synth.make_table(reqs)
+        assert L.irm_mla_attn_decode_workspace_size(chunks.ctypes.data, indptr.ctypes.data, B, 128,
+                                                    ctypes.byref(need)) == 0
+        if need.value > 32 << 20:
+            break
+    else:
+        pytest.skip("this device splits these decodes too little to exceed the scratch")
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: rejected first
     st = L.irm_mla_attn_decode_noalloc(
-        dummy.data_ptr(), dummy.data_ptr(), 64, 128, chunks.ctypes.data, indptr.ctypes.data,
+        dummy.data_ptr(), dummy.data_ptr(), B, 128, chunks.ctypes.data, indptr.ctypes.data,
         dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), 40000, ctypes.c_float(SCALE),
         dummy.data_ptr(), None, None)
     assert st == -8 and b"no-allocation" in L.irm_last_error()
