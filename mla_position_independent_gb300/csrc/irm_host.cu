@@ -268,7 +268,7 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   uint64_t phaseF[32];
   int interleaved = 0;
   if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
-  AttnPlan pl;
+  AttnPlan pl{};
   if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
   if (!q_lat || !q_rope || !kv_rows || !out || !chunks_dev || !indptr_dev)
     return fail(IRM_ERR_INVALID_ARG, "null device pointer");
@@ -566,7 +566,7 @@ irm_status irm_mla_attn_decode_workspace_size(const irm_chunk* chunks_host, cons
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, INT32_MAX, &info);
   if (st != IRM_OK) return st;
-  AttnPlan pl;
+  AttnPlan pl{};
   if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
   *bytes = pl.ws_bytes;
   return IRM_OK;
@@ -600,7 +600,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
-  AttnPlan pl;
+  AttnPlan pl{};
   if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
   if (pl.ws_bytes > kNoAllocScratchBytes)
     return fail(IRM_ERR_WORKSPACE,
@@ -630,7 +630,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
 irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
                          size_t* bytes, int64_t* slots) {
   if (bytes == nullptr || slots == nullptr) return fail(IRM_ERR_INVALID_ARG, "null output");
-  irm_cdc_params p;
+  irm_cdc_params p{};
   int64_t mx;
   return cdc_check(offsets_host, n_streams, params, &p, slots, &mx, bytes);
 }
@@ -640,10 +640,10 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, con
                          const irm_cdc_params* params, int32_t* n_chunks, int32_t* chunk_start,
                          int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream) {
-  irm_cdc_params p;
+  irm_cdc_params p{};
   int64_t slots = 0, max_len = 0;
   size_t need = 0;
-  CdcLayout lay;
+  CdcLayout lay{};
   irm_status st = cdc_check(offsets_host, n_streams, params, &p, &slots, &max_len, &need, &lay);
   if (st != IRM_OK) return st;
   if (vocab <= 0) return fail(IRM_ERR_INVALID_ARG, "vocab must be positive");
