@@ -566,13 +566,23 @@ def main():
                                            f"{secs:.1f} s; bytes counted as ctx*1152/H per unit")
     if not args.no_extras and world == 1:
         extras = {}
-        for name in ("v3_decode", "chunked_prefill", "rotate_gather_4M", "cdc_4M"):
+        steps_of = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_1M": 50,
+                    "rotate_gather_4M": 50, "rotate_gather_16M": 20, "rotate_gather_64M": 10,
+                    "cdc_4M": 50}
+        for name, st in steps_of.items():
             if name == args.workload:
                 continue
             del wl
+            wl = None
             torch.cuda.empty_cache()
+            if name.startswith("rotate_gather_"):
+                # row store + pages (2 x 1152 B per row), plus room for the L2 flush buffers
+                n = int(name.split("_")[-1].rstrip("M")) << 20
+                need = 2 * n * ROW_BYTES + (2 << 30)
+                if torch.cuda.mem_get_info()[0] < need:
+                    extras[name] = dict(skipped=f"needs {need / 1e9:.1f} GB of free device memory")
+                    continue
             wl = Workload(name, seed=rank)
-            st = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_4M": 50, "cdc_4M": 50}[name]
             t = statistics.mean(time_steps(wl, st, 3))
             r = roofline(wl, t, pk)
             r["kernel"] = wl.kernel_name()

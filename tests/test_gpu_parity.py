@@ -90,10 +90,10 @@ def test_rotate_gather_64k_rows_full(oracle_mod):
     assert r < 2.5e-3
 
 
-@pytest.mark.parametrize("n_rows", [1 << 20, 1 << 22])
-def test_rotate_gather_full_size_sampled(oracle_mod, n_rows):
-    """The configured sizes, checked on sampled target rows plus every chunk's endpoints."""
-    case = synth.rotate_gather_case(n_rows, seed=0, device="cuda")
+def _check_gather_sampled(case, oracle_mod, n_rows):
+    """Rotate+gather of a workload, checked on sampled target rows plus every chunk's
+    endpoints (the first 20000 of each kind): cKV and unrotated k_r bit-exact, rotated k_r
+    within the pages' bf16 error."""
     table = irm.ChunkTable(case.chunks, case.indptr)
     paged = torch.empty((case.n_pages, 64, 576), dtype=torch.bfloat16, device="cuda")
     pt = torch.from_numpy(case.page_table).cuda()
@@ -101,8 +101,7 @@ def test_rotate_gather_full_size_sampled(oracle_mod, n_rows):
     irm.device_status(ws)
     rng = np.random.default_rng(1)
     ends = np.concatenate([case.chunks["p_tgt"], case.chunks["p_tgt"] + case.chunks["len"] - 1])
-    t = np.unique(np.concatenate([rng.integers(0, n_rows, 20000), ends[:20000]]))
-    rows = np.stack([np.zeros_like(t), t], 1)
+    t = np.unique(np.concatenate([rng.integers(0, n_rows, 20000), ends[:20000], ends[-2000:]]))
     # only the rows the oracle needs are copied to the host
     pl = oracle_mod.plan(case.chunks, case.indptr)
     src = pl["src_row"][t]
@@ -114,6 +113,35 @@ def test_rotate_gather_full_size_sampled(oracle_mod, n_rows):
     nz = pl["delta"][t] != 0
     assert np.array_equal(got[~nz, 512:], kv_sub[~nz, 512:])
     assert rel_l2(oracle_mod.widen(got[nz, 512:]), ref[nz, 512:]) <= TOL_KR_REL_L2
+
+
+@pytest.mark.parametrize("n_rows", [1 << 20, 1 << 22])
+def test_rotate_gather_full_size_sampled(oracle_mod, n_rows):
+    """The configured sizes, checked on sampled target rows plus every chunk's endpoints."""
+    case = synth.rotate_gather_case(n_rows, seed=0, device="cuda")
+    _check_gather_sampled(case, oracle_mod, n_rows)
+
+
+@pytest.mark.parametrize("n_rows", [1 << 24, 1 << 26])
+def test_rotate_gather_largest_sizes_sampled(oracle_mod, n_rows):
+    """The sweep's 16M- and 64M-row sizes (38.6 and 154.6 GB of row store plus pages), when
+    the device has the memory free; the row store is filled 1M rows at a time."""
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    if free < 2 * n_rows * 1152 + (2 << 30):
+        pytest.skip(f"needs {2 * n_rows * 1152 / 1e9:.1f} GB of free device memory")
+    case = synth.rotate_gather_case(n_rows, seed=0, device="cuda", fill_kv=False)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(123)
+    step = 1 << 20
+    for i in range(0, n_rows, step):
+        case.kv_rows[i:i + step] = torch.randn((min(step, n_rows - i), 576), generator=g,
+                                               device="cuda").to(torch.bfloat16)
+    try:
+        _check_gather_sampled(case, oracle_mod, n_rows)
+    finally:
+        del case
+        torch.cuda.empty_cache()
 
 
 # ----------------------------------------------------------------------------- attention
