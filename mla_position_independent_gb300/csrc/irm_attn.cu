@@ -220,7 +220,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     last_sh = 0;
-    if (!table_ok) set_status(a.status, kDevErrBounds);
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), kPubWarps);
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
@@ -252,6 +251,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_arrive();  // the peer's barriers exist before any remote traffic
   cluster_wait();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
+  // (checked only now, so that the set-up above does not wait for the chunk-table reads)
+  if (tid == 0 && !table_ok) set_status(a.status, kDevErrBounds);
 
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ======================= loaders =====================================================
@@ -276,13 +277,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
       // lands with the first KV tile (same cp.async group).
       if (ntiles > 0 && chk < 4) {
+        // tile row m is (query q0 + m / H, head m % H): global row (b n_q + q0) H + m
+        const int64_t row0 = ((int64_t)b * a.n_q + q0) * a.H;
         for (int m = rsub; m < Mv; m += kCopyThreads / 8) {
           const bool valid = m < rows_valid;
-          int64_t row = 0;
-          if (valid) {
-            const int qi = q0 + m / a.H, h = m % a.H;
-            row = ((int64_t)b * a.n_q + qi) * a.H + h;
-          }
+          const int64_t row = valid ? row0 + m : 0;
           const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
           cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
         }
@@ -414,7 +413,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cw.c_end = c_end;
     cw.win = c_begin;
     bool ok = true;
-    if (ntiles > 0) cw.seek(c_begin, kb * kBN, lane);
+    if (ntiles > 0) {
+      if (kb == 0) {
+        cw.load(lane);  // the request's first chunk starts at position 0
+      } else {
+        cw.seek(c_begin, kb * kBN, lane);
+      }
+    }
     int s = 0;
     uint32_t ph = 0;
     for (int j = 0; j < ntiles; ++j) {
@@ -486,8 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // lanes)
     if (ntiles > 0 && warp_live) {
       const bool valid = m < rows_valid;
-      int64_t row = 0;
-      if (valid) row = ((int64_t)b * a.n_q + (q0 + m / a.H)) * a.H + (m % a.H);
+      const int64_t row = valid ? ((int64_t)b * a.n_q + q0) * a.H + m : 0;
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_lat) +
                                                          row * kDLat + col0);
 #pragma unroll 1
