@@ -232,6 +232,28 @@ def test_attention_edge_cases(oracle_mod, H, lens):
             _check_attn(case, oracle_mod, prefill=False, what=f"decode H={H} lens={lens}")
 
 
+@pytest.mark.parametrize("H", [3, 40, 100])
+def test_attention_head_counts_not_dividing_the_tile(oracle_mod, H):
+    """A query tile holds floor(128 / H) queries of H heads (rows past them unused); prefill
+    over several query tiles and decode, with ragged chunks and large deltas."""
+    rng = np.random.default_rng(H)
+    n_rows = 4096
+    reqs = []
+    for b in range(2):
+        p, req = 0, []
+        for k, n in enumerate([32, 200, 128, 3, 77]):
+            reused = p >= 32 and k % 2 == 1
+            d = [1, -1, 65536, -65536, 0, 777][k % 6] if reused else 0
+            req.append((int(rng.integers(0, n_rows - n)), n, p - d, reused))
+            p += n
+        reqs.append(req)
+    for n_q in (1, 70):
+        case = to_device(synth.custom_case(reqs, n_rows=n_rows, n_q=n_q, H=H, q_std=1.0, seed=n_q + H))
+        _check_attn(case, oracle_mod, prefill=True, what=f"H={H} n_q={n_q}")
+        if n_q == 1:
+            _check_attn(case, oracle_mod, prefill=False, what=f"decode H={H}")
+
+
 def _ragged_decode_case(ctxs, H, seed):
     """Requests of very different context lengths in one decode batch: with the splits of a
     request sized for the longest one, short requests leave whole splits without tiles."""
