@@ -135,6 +135,17 @@ irm_status irm_validate_chunks(const irm_chunk* chunks_host, const int32_t* indp
 irm_status irm_device_status(void* workspace, cudaStream_t stream);
 
 /*
+ * Self-test of the bounded pipeline wait (the pages have no counterpart; for tests).  Launches
+ * one warp on `stream` that waits on a barrier nothing ever arrives on; the wait gives up after
+ * its time limit (2 s), exactly as a stalled pipeline wait of the other kernels would, and sets
+ * the timeout bit of the workspace status word.  irm_device_status() then returns
+ * IRM_ERR_DEVICE_TIMEOUT, and the context stays usable.
+ *   workspace  device, 256-byte aligned, >= IRM_WORKSPACE_HEADER bytes (its status word is used)
+ * Returns IRM_OK (launched), IRM_ERR_WORKSPACE or IRM_ERR_CUDA.
+ */
+irm_status irm_selftest_wait_timeout(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Rotate+gather into a paged KV layout, and/or the per-row assembly plan.
  * [walkthrough §5 assembly loop: reused chunks contribute (cKV, R(delta) k_r,base)]
  *

@@ -9,9 +9,10 @@ from .binding import (CDC_LOW_BITS, CDC_THRESHOLD, ROPE_INTERLEAVED, ROPE_NEOX, 
                       ChunkTable, IrmError, Registry, Rope, cdc_sizes, cdc_slot_base, irm_cdc_chunk,
                       assemble_kv_workspace_size, decode_workspace_size, device_status,
                       irm_assemble_kv, irm_mla_attn_decode, irm_mla_attn_prefill, lib,
-                      new_workspace, prefill_workspace_size, validate_chunks)
+                      new_workspace, prefill_workspace_size, selftest_wait_timeout,
+                      validate_chunks)
 
 __all__ = ["Registry", "CDC_LOW_BITS", "CDC_THRESHOLD", "CdcParams", "cdc_sizes", "cdc_slot_base",
            "irm_cdc_chunk", "ROPE_INTERLEAVED", "ROPE_NEOX", "Rope", "ChunkTable", "IrmError",
            "assemble_kv_workspace_size", "decode_workspace_size", "device_status", "irm_assemble_kv", "irm_mla_attn_decode", "irm_mla_attn_prefill",
-           "lib", "new_workspace", "prefill_workspace_size", "validate_chunks"]
+           "lib", "new_workspace", "prefill_workspace_size", "selftest_wait_timeout", "validate_chunks"]

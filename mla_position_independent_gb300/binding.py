@@ -27,7 +27,7 @@ EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_c
            "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc",
            "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope",
            "irm_cdc_sizes", "irm_cdc_chunk", "irm_registry_create", "irm_registry_stats",
-           "irm_registry_assemble"]
+           "irm_registry_assemble", "irm_selftest_wait_timeout"]
 
 ROPE_NEOX, ROPE_INTERLEAVED = 0, 1
 
@@ -81,6 +81,7 @@ def lib():
         L.irm_version.restype = ctypes.c_char_p
         L.irm_validate_chunks.argtypes = [P, P, I, I64, P]
         L.irm_device_status.argtypes = [P, P]
+        L.irm_selftest_wait_timeout.argtypes = [P, SZ, P]
         L.irm_assemble_kv_workspace_size.argtypes = [I, P]
         L.irm_assemble_kv.argtypes = [P, P, I, P, P, P, I64, P, I64, P, I, P, P, P, P, SZ, P]
         L.irm_mla_attn_decode_workspace_size.argtypes = [P, P, I, I, P]
@@ -175,6 +176,12 @@ def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 def device_status(workspace: torch.Tensor, stream=None):
     """Raises IrmError if a kernel recorded a timeout or an out-of-range row (and clears it)."""
     _check(lib().irm_device_status(_ptr(workspace), _stream(stream)))
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, stream=None):
+    """Launches the bounded-wait self-test (a wait nothing ever completes); after it,
+    device_status(workspace) raises the timeout it recorded."""
+    _check(lib().irm_selftest_wait_timeout(_ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def assemble_kv_workspace_size(B: int) -> int:
