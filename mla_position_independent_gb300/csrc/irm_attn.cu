@@ -254,215 +254,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // (checked only now, so that the set-up above does not wait for the chunk-table reads)
   if (tid == 0 && !table_ok) set_status(a.status, kDevErrBounds);
 
-  if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-    // ======================= loaders =====================================================
-    // Warps 8-9 gather KV rows with cp.async following the row maps that warp 14 builds from
-    // the chunk table; warps 10-11 wait for each tile's bytes to land, rotate this CTA's k_r pairs by
-    // R(delta) in shared memory and publish the tile.  Every role blocks in mbarrier waits, so
-    // no loader warp spins for issue slots the softmax warps need, and the copies run up to NS
-    // tiles ahead.  The Q.K^T issuer fences the bytes for the async proxy after acquiring
-    // KV_FULL (a writer's own fence would also wait for its copies of later tiles in flight).
-    const int lw = warp - kSoftmaxWarps;  // 0-1 copy warps, 2-3 publishers
-    bool ok = true;
-    if (lw < kCopyWarps) {
-      const int tp = tid - kSoftmaxWarps * 32;  // 0 .. kCopyThreads - 1
-      const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
-      const int rsub = tp >> 3;   // row within a group of kCopyThreads / 8
-      const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
-      const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
-      // Stored chunk c (0..3) of this CTA's k_r / q_rope half: the 16-byte chunk
-      // half_chunk(c) of the 64 rope columns (NeoX: its pairs' first then second halves;
-      // interleaved: four contiguous chunks).
-      const int kr_col = chk < 4 ? 8 * half_chunk(a.interleaved, (int)rank, chk) : 0;
-      // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
-      // lands with the first KV tile (same cp.async group).
-      if (ntiles > 0 && chk < 4) {
-        // tile row m is (query q0 + m / H, head m % H): global row (b n_q + q0) H + m
-        const int64_t row0 = ((int64_t)b * a.n_q + q0) * a.H;
-        for (int m = rsub; m < Mv; m += kCopyThreads / 8) {
-          const bool valid = m < rows_valid;
-          const int64_t row = valid ? row0 + m : 0;
-          const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
-          cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
-        }
-      }
-      int s = 0;
-      uint32_t ph = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        // stage s is free once the P.V of tile j-NS completed
-        if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
-        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
-        const uint32_t stage = sb + L.kv + (uint32_t)s * L.stage;
-        // all of this thread's source rows first, then every copy of the tile back to back
-        int srs[kCopyPasses];
-#pragma unroll
-        for (int p = 0; p < kCopyPasses; ++p) {
-          const int row = p * kCopyRowsPerPass + rsub;
-          srs[p] = row < kBN ? map_src[s * kBN + row] : -1;
-        }
-#pragma unroll
-        for (int p = 0; p < kCopyPasses; ++p) {
-          const int row = p * kCopyRowsPerPass + rsub;
-          if (row >= kBN) break;
-          const int sr = srs[p];
-          const __nv_bfloat16* kvrow = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow;
-          const __nv_bfloat16* rowp = kvrow + col0 + chk * 8;
-          const uint32_t dst = stage + sw128_offset(row, chk);
-          const uint32_t nb = sr >= 0 ? 16u : 0u;
-#pragma unroll
-          for (int slab = 0; slab < 4; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
-          if (chk < 4)
-            cp_async_16(sb + kr_slab(s) + sw128_offset(row, chk + 4 * (s & 1)), kvrow + kDLat + kr_col, nb);
-        }
-        cp_async_arrive_noinc(bar(BAR_LANDED + s));
-        if (++s == NS) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-      cp_async_wait_all();
-    } else {
-      // publisher pb owns rows 32 pb .. 32 pb + 31 of every tile; each 16-row half keeps its
-      // lane's last (cos, sin) (recomputed only when the row's delta changes)
-      const int pb = lw - kCopyWarps;
-      int dprev[2] = {0, 0};
-      float cs_c[2][8], cs_s[2][8];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          cs_c[h][e] = 1.f;
-          cs_s[h][e] = 0.f;
-        }
-      int s = 0;
-      uint32_t ph = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
-        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;  // orders the map's deltas
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          rotate_krope_half_16rows(smem + kr_slab(s), map_delta + s * kBN, phaseF, a.interleaved, (int)rank,
-                                   32 * pb + 16 * h,
-                                   4 * (s & 1), lane, dprev[h], cs_c[h], cs_s[h]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));
-        if (++s == NS) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      set_status(a.status, kDevErrTimeout);
-    }
-  } else if (warp == kSWarp) {
-    // ======================= Q.K^T issuer (one thread) ===================================
-    // (warp 15, the only one of its SM sub-partition besides two softmax warps and a
-    // publisher: its issue slots are the least contended)
-    if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(bar(BAR_Q_FULL), 0, abort_flag);
-      tc_fence_after();
-      int ss = 0;
-      uint32_t phs = 0;  // kv_full parity of stage ss
-      const uint64_t aq = sdesc_sw128(sb + L.qr, 16, 1024);  // the q_rope half (A, K-major)
-      for (int ns = 0; ns < ntiles && ok; ++ns) {
-        if (!(ok = mbar_wait(bar(BAR_KV_FULL + ss), phs, abort_flag))) break;
-        // the score buffer is free once the softmax warps have loaded tile ns-1's scores
-        if (ns >= 1 && !(ok = mbar_wait(bar(BAR_S_EMPTY), (ns - 1) & 1, abort_flag))) break;
-        // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads
-        tc_fence_after();
-        fence_proxy_async_smem();
-        const uint64_t bd = sdesc_sw128(sb + L.kv + (uint32_t)ss * L.stage, 16, 1024);
-        const uint64_t bk = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64, 16, 1024);
-        const uint32_t tS = tmem + kTmemS;
-#pragma unroll
-        for (int slab = 0; slab < 4; ++slab) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, sdesc_add(bd, slab * kSlabKV + kk * 32),
-                         kIdescS, (slab | kk) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)  // the half k_r slab: 32 columns, 2 K-steps
-          umma_bf16(tS, sdesc_add(aq, kk * 32), sdesc_add(bk, kk * 32), kIdescS, 1u);
-        umma_commit(bar(BAR_S_FULL));
-        if (++ss == NS) {
-          ss = 0;
-          phs ^= 1u;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(a.status, kDevErrTimeout);
-      }
-      umma_commit(bar(BAR_DRAIN));
-      if (!mbar_wait(bar(BAR_DRAIN), 0, nullptr)) set_status(a.status, kDevErrTimeout);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // TMEM allocation and release only
-  } else if (warp == kMapWarp) {
-    // ======================= row maps ====================================================
-    // A window of 32 chunk records (one per lane) turned into each tile's row map: source
-    // row (-1 = outside the context, zero filled) and delta.  The map of tile j goes into
-    // slot j % NS once tile j-NS has been published (its copies issued and its k_r rotated),
-    // so maps are ready up to NS tiles ahead of the copies.
-    ChunkWindow cw;
-    cw.chunks = a.chunks;
-    cw.c_end = c_end;
-    cw.win = c_begin;
-    bool ok = true;
-    if (ntiles > 0) {
-      if (kb == 0) {
-        cw.load(lane);  // the request's first chunk starts at position 0
-      } else {
-        cw.seek(c_begin, kb * kBN, lane);
-      }
-    }
-    int s = 0;
-    uint32_t ph = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
-      cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + s * kBN, map_delta + s * kBN, a.status, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
-      if (++s == NS) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      set_status(a.status, kDevErrTimeout);
-    }
-  } else if (warp == kPvWarp) {
-    // ======================= P.V issuer (one thread) =====================================
-    if (lane == 0 && ntiles > 0) {
-      const uint32_t tO = tmem + kTmemO;
-      bool ok = true;
-      int sp = 0;
-      for (int np = 0; np < ntiles && ok; ++np) {
-        if (!(ok = mbar_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint64_t bv = sdesc_sw128(sb + L.kv + (uint32_t)sp * L.stage, kSlabKV, 1024);
-        const uint32_t tP = tmem + kTmemP + 32u * (uint32_t)(np & 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ts(tO, tP + 8u * kk, sdesc_add(bv, kk * 2048), kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(BAR_KV_EMPTY + sp));
-        umma_commit(bar(BAR_PV_DONE + (np & 1)));
-        if (++sp == NS) sp = 0;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(a.status, kDevErrTimeout);
-      }
-      umma_commit(bar(BAR_DRAIN + 1));
-      if (!mbar_wait(bar(BAR_DRAIN + 1), 0, nullptr)) set_status(a.status, kDevErrTimeout);
-    }
-    __syncwarp();
-  } else {
+  // The softmax branch comes first: its loop is the hottest code of the kernel, and its place
+  // in the binary measurably matters (instruction fetch is a top stall reason).
+  if (warp < kSoftmaxWarps) {
     // ======================= softmax + epilogue (thread = query row) ===================
     // Warps w and w + 4 share TMEM lane quadrant w & 3; `half` 0 takes keys 0-31 of every
     // tile and O columns [0, 128) of this CTA's 256, half 1 keys 32-63 and columns [128, 256).
@@ -756,6 +550,215 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         last_sh = (atomicAdd(cnt, 1) == a.S - 1) ? 1 : 0;
       }
     }
+  
+  } else if (warp < kMmaWarp) {
+    // ======================= loaders =====================================================
+    // Warps 8-9 gather KV rows with cp.async following the row maps that warp 14 builds from
+    // the chunk table; warps 10-11 wait for each tile's bytes to land, rotate this CTA's k_r pairs by
+    // R(delta) in shared memory and publish the tile.  Every role blocks in mbarrier waits, so
+    // no loader warp spins for issue slots the softmax warps need, and the copies run up to NS
+    // tiles ahead.  The Q.K^T issuer fences the bytes for the async proxy after acquiring
+    // KV_FULL (a writer's own fence would also wait for its copies of later tiles in flight).
+    const int lw = warp - kSoftmaxWarps;  // 0-1 copy warps, 2-3 publishers
+    bool ok = true;
+    if (lw < kCopyWarps) {
+      const int tp = tid - kSoftmaxWarps * 32;  // 0 .. kCopyThreads - 1
+      const int chk = tp & 7;     // 16-byte chunk of a 128-byte slab row
+      const int rsub = tp >> 3;   // row within a group of kCopyThreads / 8
+      const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
+      const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
+      // Stored chunk c (0..3) of this CTA's k_r / q_rope half: the 16-byte chunk
+      // half_chunk(c) of the 64 rope columns (NeoX: its pairs' first then second halves;
+      // interleaved: four contiguous chunks).
+      const int kr_col = chk < 4 ? 8 * half_chunk(a.interleaved, (int)rank, chk) : 0;
+      // The CTA's q_rope half: Mv rows (rows past the tile's valid rows are zero filled); it
+      // lands with the first KV tile (same cp.async group).
+      if (ntiles > 0 && chk < 4) {
+        // tile row m is (query q0 + m / H, head m % H): global row (b n_q + q0) H + m
+        const int64_t row0 = ((int64_t)b * a.n_q + q0) * a.H;
+        for (int m = rsub; m < Mv; m += kCopyThreads / 8) {
+          const bool valid = m < rows_valid;
+          const int64_t row = valid ? row0 + m : 0;
+          const void* src = valid ? (const void*)(qr + row * kDRope + kr_col) : a.q_rope;
+          cp_async_16(sb + L.qr + sw128_offset(m, chk), src, valid ? 16u : 0u);
+        }
+      }
+      int s = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        // stage s is free once the P.V of tile j-NS completed
+        if (j >= NS && !(ok = warp_wait(bar(BAR_KV_EMPTY + s), ph ^ 1u, abort_flag))) break;
+        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;
+        const uint32_t stage = sb + L.kv + (uint32_t)s * L.stage;
+        // all of this thread's source rows first, then every copy of the tile back to back
+        int srs[kCopyPasses];
+#pragma unroll
+        for (int p = 0; p < kCopyPasses; ++p) {
+          const int row = p * kCopyRowsPerPass + rsub;
+          srs[p] = row < kBN ? map_src[s * kBN + row] : -1;
+        }
+#pragma unroll
+        for (int p = 0; p < kCopyPasses; ++p) {
+          const int row = p * kCopyRowsPerPass + rsub;
+          if (row >= kBN) break;
+          const int sr = srs[p];
+          const __nv_bfloat16* kvrow = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow;
+          const __nv_bfloat16* rowp = kvrow + col0 + chk * 8;
+          const uint32_t dst = stage + sw128_offset(row, chk);
+          const uint32_t nb = sr >= 0 ? 16u : 0u;
+#pragma unroll
+          for (int slab = 0; slab < 4; ++slab) cp_async_16(dst + slab * kSlabKV, rowp + slab * 64, nb);
+          if (chk < 4)
+            cp_async_16(sb + kr_slab(s) + sw128_offset(row, chk + 4 * (s & 1)), kvrow + kDLat + kr_col, nb);
+        }
+        cp_async_arrive_noinc(bar(BAR_LANDED + s));
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      cp_async_wait_all();
+    } else {
+      // publisher pb owns rows 32 pb .. 32 pb + 31 of every tile; each 16-row half keeps its
+      // lane's last (cos, sin) (recomputed only when the row's delta changes)
+      const int pb = lw - kCopyWarps;
+      int dprev[2] = {0, 0};
+      float cs_c[2][8], cs_s[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cs_c[h][e] = 1.f;
+          cs_s[h][e] = 0.f;
+        }
+      int s = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        if (!(ok = warp_wait(bar(BAR_LANDED + s), ph, abort_flag))) break;
+        if (!(ok = warp_wait(bar(BAR_MAP + s), ph, abort_flag))) break;  // orders the map's deltas
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          rotate_krope_half_16rows(smem + kr_slab(s), map_delta + s * kBN, phaseF, a.interleaved, (int)rank,
+                                   32 * pb + 16 * h,
+                                   4 * (s & 1), lane, dprev[h], cs_c[h], cs_s[h]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_KV_FULL + s));
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.status, kDevErrTimeout);
+    }
+  } else if (warp == kSWarp) {
+    // ======================= Q.K^T issuer (one thread) ===================================
+    // (warp 15, the only one of its SM sub-partition besides two softmax warps and a
+    // publisher: its issue slots are the least contended)
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(bar(BAR_Q_FULL), 0, abort_flag);
+      tc_fence_after();
+      int ss = 0;
+      uint32_t phs = 0;  // kv_full parity of stage ss
+      const uint64_t aq = sdesc_sw128(sb + L.qr, 16, 1024);  // the q_rope half (A, K-major)
+      for (int ns = 0; ns < ntiles && ok; ++ns) {
+        if (!(ok = mbar_wait(bar(BAR_KV_FULL + ss), phs, abort_flag))) break;
+        // the score buffer is free once the softmax warps have loaded tile ns-1's scores
+        if (ns >= 1 && !(ok = mbar_wait(bar(BAR_S_EMPTY), (ns - 1) & 1, abort_flag))) break;
+        // the tile's bytes (cp.async-written and rotated) -> async proxy before the UMMA reads
+        tc_fence_after();
+        fence_proxy_async_smem();
+        const uint64_t bd = sdesc_sw128(sb + L.kv + (uint32_t)ss * L.stage, 16, 1024);
+        const uint64_t bk = sdesc_sw128(sb + kr_slab(ss) + (ss & 1) * 64, 16, 1024);
+        const uint32_t tS = tmem + kTmemS;
+#pragma unroll
+        for (int slab = 0; slab < 4; ++slab) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ts(tS, tmem + kTmemQ + 32u * slab + 8u * kk, sdesc_add(bd, slab * kSlabKV + kk * 32),
+                         kIdescS, (slab | kk) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)  // the half k_r slab: 32 columns, 2 K-steps
+          umma_bf16(tS, sdesc_add(aq, kk * 32), sdesc_add(bk, kk * 32), kIdescS, 1u);
+        umma_commit(bar(BAR_S_FULL));
+        if (++ss == NS) {
+          ss = 0;
+          phs ^= 1u;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, kDevErrTimeout);
+      }
+      umma_commit(bar(BAR_DRAIN));
+      if (!mbar_wait(bar(BAR_DRAIN), 0, nullptr)) set_status(a.status, kDevErrTimeout);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // TMEM allocation and release only
+  } else if (warp == kMapWarp) {
+    // ======================= row maps ====================================================
+    // A window of 32 chunk records (one per lane) turned into each tile's row map: source
+    // row (-1 = outside the context, zero filled) and delta.  The map of tile j goes into
+    // slot j % NS once tile j-NS has been published (its copies issued and its k_r rotated),
+    // so maps are ready up to NS tiles ahead of the copies.
+    ChunkWindow cw;
+    cw.chunks = a.chunks;
+    cw.c_end = c_end;
+    cw.win = c_begin;
+    bool ok = true;
+    if (ntiles > 0) {
+      if (kb == 0) {
+        cw.load(lane);  // the request's first chunk starts at position 0
+      } else {
+        cw.seek(c_begin, kb * kBN, lane);
+      }
+    }
+    int s = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      if (j >= NS && !(ok = warp_wait(bar(BAR_KV_FULL + s), ph ^ 1u, abort_flag))) break;
+      cw.build_map((kb + j) * kBN, ctx, a.n_rows, map_src + s * kBN, map_delta + s * kBN, a.status, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_MAP + s));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.status, kDevErrTimeout);
+    }
+  } else if (warp == kPvWarp) {
+    // ======================= P.V issuer (one thread) =====================================
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t tO = tmem + kTmemO;
+      bool ok = true;
+      int sp = 0;
+      for (int np = 0; np < ntiles && ok; ++np) {
+        if (!(ok = mbar_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t bv = sdesc_sw128(sb + L.kv + (uint32_t)sp * L.stage, kSlabKV, 1024);
+        const uint32_t tP = tmem + kTmemP + 32u * (uint32_t)(np & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts(tO, tP + 8u * kk, sdesc_add(bv, kk * 2048), kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(BAR_KV_EMPTY + sp));
+        umma_commit(bar(BAR_PV_DONE + (np & 1)));
+        if (++sp == NS) sp = 0;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, kDevErrTimeout);
+      }
+      umma_commit(bar(BAR_DRAIN + 1));
+      if (!mbar_wait(bar(BAR_DRAIN + 1), 0, nullptr)) set_status(a.status, kDevErrTimeout);
+    }
+    __syncwarp();
   }
   // ---- teardown ---------------------------------------------------------------------
   __syncthreads();
