@@ -6,12 +6,15 @@ the other workloads (V3-shaped decode, chunked prefill, rotate+gather) in "workl
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-A step is one pass of the whole hot path over one batch: chunk-table walk, per-chunk
-rotation angles, gather of [cKV | k_r] rows, delta-rotation in shared memory, Q.K^T,
-online softmax, P.cKV (and the split-KV merge for decode) -- one call of the C ABI.
+A step is one pass of the whole hot path over one batch -- one call of the C ABI: the
+copy of the validated host chunk table into the workspace, then the fused kernel
+(chunk-table walk, per-chunk rotation angles, gather of [cKV | k_r] rows, delta-rotation
+in shared memory, Q.K^T, online softmax, P.cKV, and the split-KV merge for decode).
 Steps are timed with CUDA events on the launching stream, each step replayed from a CUDA
-graph, with L2 flushed (256 MiB write then 256 MiB read, untimed) between steps.  The oracle arm
-(--impl reference) times the fp64 CPU oracle on a bounded sample of the same workload.
+graph, with L2 flushed (256 MiB write then 256 MiB read, untimed) between steps.  Every
+workload also gets an end-to-end figure (host buffers in, result back), its own clock
+record, and the fp64 oracle timed on the host cores on a bounded sample of it.  The oracle
+arm (--impl reference) times the oracle alone on the selected workload.
 Under torchrun every rank runs its own replica (weak scaling); rank 0 prints one JSON line.
 """
 from __future__ import annotations
@@ -131,6 +134,8 @@ class ClockSampler:
 
 def _prep_case(name, seed):
     from mla_position_independent_gb300 import synth
+    if name == "tiny":
+        return synth.tiny_case(seed, device="cuda")
     if name == "v2lite_decode":
         return synth.v2lite_decode(seed, device="cuda")
     if name == "v3_decode":
@@ -154,6 +159,8 @@ CDC_VOCAB = 102400
 
 
 DESCR = {
+    "tiny": "tiny correctness case: 1 request, ctx 512 (carve-out + 4 reused chunks of 64/96/128/192 "
+            "from a pool of 8), 16 causal queries x 16 heads",
     "v2lite_decode": "DeepSeek-V2-Lite-shaped decode: 16 heads, batch 8, ctx 8192, 1 query/request, "
                      "chunks geometric mean 128 in [32,512], 75% reused, delta ~ U[-4096,4096]",
     "v3_decode": "DeepSeek-V3-shaped decode: 128 heads, batch 64, ctx 32768, 256 shared pool "
@@ -167,6 +174,10 @@ DESCR = {
               "chunks, xxHash64 fingerprints",
     "cdc_16M": "content-defined chunking of 256 token streams x 65536 tokens (as cdc_4M)",
 }
+for _n in ("1M", "4M", "16M", "64M"):
+    DESCR[f"rotate_gather_{_n}"] = (f"rotate+gather of {_n} rows of [cKV 512 | k_r 64] bf16 from a chunk "
+                                    "pool (geometric chunks, mean 128, [32,512]) into 64-row pages in "
+                                    "random physical order, delta ~ U[-65536,65536] per chunk")
 
 
 def _fill_large(kv, seed):
@@ -178,21 +189,23 @@ def _fill_large(kv, seed):
 
 
 class Workload:
-    """Device-resident inputs and the C-ABI call of one step."""
+    """Device-resident inputs and the C-ABI call of one step.  The chunk table is the
+    library's input in page-locked host memory: every call validates it and copies it into
+    the workspace (inside the timed step)."""
 
     def __init__(self, name, seed=0):
         import mla_position_independent_gb300 as irm
         self.irm = irm
         self.name = name
         if name.startswith("cdc_"):
-            from mla_position_independent_gb300 import synth
             tokens, offsets = _prep_case(name, seed)
             self.kind = "cdc"
             self.tokens = torch.from_numpy(tokens).cuda()
-            self.offsets = offsets
-            self.offsets_dev = torch.from_numpy(offsets.copy()).cuda()
+            # page-locked, so the library's copy of the offsets can be captured into the graph
+            self._offsets_pinned = torch.from_numpy(offsets.copy()).pin_memory()
+            self.offsets = self._offsets_pinned.numpy()
             self.gear = None  # Gear words generated from SplitMix64 (no table lookups)
-            nbytes, slots = irm.cdc_sizes(offsets)
+            nbytes, slots = irm.cdc_sizes(self.offsets)
             self.ws = irm.new_workspace(nbytes)
             S = offsets.shape[0] - 1
             self.cdc_out = (torch.empty(S, dtype=torch.int32, device="cuda"),
@@ -224,15 +237,15 @@ class Workload:
             self.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
             self.lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
             self.ws = irm.new_workspace(irm.decode_workspace_size(self.table, H))
-            self.S_split = None
             self.bytes = self.ctx_total * ROW_BYTES
             self.flops = float(self.ctx_total) * H * PAIR_FLOPS
         elif self.kind == "prefill":
             self.q_lat, self.q_rope = case.q_lat, case.q_rope
             B, n_q, H = self.q_lat.shape[:3]
+            self.H = H
             self.out = torch.empty((B, n_q, H, 512), dtype=torch.bfloat16, device="cuda")
             self.lse = torch.empty((B, n_q, H), dtype=torch.float32, device="cuda")
-            self.ws = irm.new_workspace(irm.prefill_workspace_size(B, n_q, H))
+            self.ws = irm.new_workspace(irm.prefill_workspace_size(self.table, n_q, H))
             # causal pairs: query i at ctx-n_q+i sees ctx-n_q+i+1 keys
             pairs = sum(H * (n_q * (c - n_q) + n_q * (n_q + 1) // 2) for c in ctx)
             self.flops = float(pairs) * PAIR_FLOPS
@@ -240,16 +253,16 @@ class Workload:
         else:
             self.paged = torch.empty((case.n_pages, 64, 576), dtype=torch.bfloat16, device="cuda")
             self.page_table = torch.from_numpy(case.page_table).cuda()
-            self.ws = irm.new_workspace(irm.assemble_kv_workspace_size(self.table.B))
+            self.ws = irm.new_workspace(irm.assemble_kv_workspace_size(self.table))
             self.bytes = 2 * self.ctx_total * ROW_BYTES
             self.flops = 0.0
+        self.table_bytes = int(self.table._buf.numel())
 
     def step(self, stream=None):
         irm = self.irm
         if self.kind == "cdc":
             irm.irm_cdc_chunk(self.tokens, self.offsets, self.gear, out=self.cdc_out,
-                              workspace=self.ws, stream=stream, offsets_dev=self.offsets_dev,
-                              vocab=CDC_VOCAB)
+                              workspace=self.ws, stream=stream, vocab=CDC_VOCAB)
             return
         if self.kind == "decode":
             irm.irm_mla_attn_decode(self.q_lat, self.q_rope, self.table, self.case.kv_rows,
@@ -300,10 +313,12 @@ L2_NOTE = ("flushed between steps (untimed): 256 MiB write, then 256 MiB read so
 
 
 def time_steps(wl: Workload, steps: int, warmup: int, use_graph=True):
-    """Per-step CUDA-event time (ms) of `steps` steps, L2 flushed before each (untimed)."""
+    """Per-step CUDA-event time (ms) of `steps` steps, L2 flushed before each (untimed).  A
+    step (the C-ABI call: the chunk-table copy into the workspace and the kernel launch) is
+    captured once into a CUDA graph and replayed."""
     stream = torch.cuda.current_stream()
     flush = L2Flush()
-    for _ in range(max(warmup, 1)):
+    for _ in range(max(warmup, 3)):
         wl.step()
     torch.cuda.synchronize()
     wl.check_status()
@@ -334,33 +349,88 @@ def time_steps(wl: Workload, steps: int, warmup: int, use_graph=True):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def e2e_decode(wl: Workload, steps: int):
-    """Decode through the public API from pinned host buffers: per step H2D of the queries
-    and the chunk table, the call, D2H of the output; wall clock per step."""
-    assert wl.kind == "decode"
+def timed(wl: Workload, steps: int, warmup: int, device_index: int):
+    """time_steps with nvidia-smi clock samples taken during the timed region."""
+    clk = ClockSampler(device_index)
+    per_step = time_steps(wl, steps, warmup)
+    clocks = clk.stop()
+    return per_step, dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"],
+                          reasons=clocks["reasons"], samples=clocks["samples"])
+
+
+def e2e(wl: Workload, steps: int):
+    """The step end to end through the C ABI with host buffers, wall clock per step: H2D of
+    the step's inputs from page-locked host memory (queries; the page table for
+    rotate+gather), the C-ABI call (which validates the host chunk table and copies it into
+    the workspace), and the read-back of the step's result (the attention output; for
+    rotate+gather, whose output stays on the device as the paged cache, its status word),
+    then a synchronize.  L2 is flushed (untimed) before each step.  Returns (ms per step,
+    H2D bytes, D2H bytes)."""
+    import ctypes
     irm = wl.irm
-    ql_h = wl.q_lat.cpu().pin_memory()
-    qr_h = wl.q_rope.cpu().pin_memory()
-    ch_h = torch.from_numpy(wl.table.chunks_host.view(np.uint8).copy()).pin_memory()
-    out_h = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
+    L = irm.lib()
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    t = wl.table
+    ch, ip = t.chunks_host.ctypes.data, t.indptr_host.ctypes.data
+    ws = wl.ws
+    if wl.kind in ("decode", "prefill"):
+        nl, nr = wl.q_lat.numel(), wl.q_rope.numel()
+        dq = torch.empty(nl + nr, dtype=torch.bfloat16, device="cuda")  # [q_lat | q_rope]
+        hq = torch.empty(nl + nr, dtype=torch.bfloat16).pin_memory()
+        hq[:nl].copy_(wl.q_lat.reshape(-1).cpu())
+        hq[nl:].copy_(wl.q_rope.reshape(-1).cpu())
+        hout = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
+        ql, qr = dq.data_ptr(), dq.data_ptr() + 2 * nl
+        scale = ctypes.c_float(1.0 / math.sqrt(192.0))
+        kv, n_rows = wl.case.kv_rows.data_ptr(), int(wl.case.kv_rows.shape[0])
+        if wl.kind == "decode":
+            B, H = wl.q_lat.shape[:2]
+            args = (ql, qr, B, H, ch, ip, kv, n_rows, scale, wl.out.data_ptr(), None, ws.data_ptr(),
+                    ws.numel(), sp)
+            call = L.irm_mla_attn_decode
+        else:
+            B, n_q, H = wl.q_lat.shape[:3]
+            args = (ql, qr, B, n_q, H, ch, ip, kv, n_rows, scale, wl.out.data_ptr(), None,
+                    ws.data_ptr(), ws.numel(), sp)
+            call = L.irm_mla_attn_prefill
+
+        def one():
+            dq.copy_(hq, non_blocking=True)
+            st = call(*args)
+            if st != 0:
+                raise RuntimeError(L.irm_last_error().decode())
+            hout.copy_(wl.out, non_blocking=True)
+            stream.synchronize()
+        h2d = hq.numel() * 2 + wl.table_bytes
+        d2h = hout.numel() * 2
+    else:
+        hpt = torch.from_numpy(wl.case.page_table.copy()).pin_memory()
+        kv = wl.case.kv_rows
+        args = (ch, ip, t.B, kv.data_ptr(), int(kv.shape[0]), wl.paged.data_ptr(),
+                int(wl.paged.shape[0]), wl.page_table.data_ptr(), int(wl.page_table.shape[1]),
+                None, None, None, ws.data_ptr(), ws.numel(), sp)
+
+        def one():
+            wl.page_table.copy_(hpt, non_blocking=True)
+            st = L.irm_assemble_kv(*args)
+            if st != 0:
+                raise RuntimeError(L.irm_last_error().decode())
+            if L.irm_device_status(ws.data_ptr(), sp) != 0:  # reads the status word, synchronizes
+                raise RuntimeError(L.irm_last_error().decode())
+        h2d = hpt.numel() * 4 + wl.table_bytes
+        d2h = 4
     flush = L2Flush()
     times = []
     for i in range(steps + 3):
         flush(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        wl.q_lat.copy_(ql_h, non_blocking=True)
-        wl.q_rope.copy_(qr_h, non_blocking=True)
-        wl.table.chunks_dev.copy_(ch_h, non_blocking=True)
-        irm.irm_mla_attn_decode(wl.q_lat, wl.q_rope, wl.table, wl.case.kv_rows, out=wl.out,
-                                lse=wl.lse, workspace=wl.ws)
-        out_h.copy_(wl.out, non_blocking=True)
-        torch.cuda.synchronize()
+        one()
         if i >= 3:
             times.append(time.perf_counter() - t0)
-    h2d = ql_h.numel() * 2 + qr_h.numel() * 2 + ch_h.numel()
-    d2h = out_h.numel() * 2
-    return statistics.mean(times) * 1e3, h2d, d2h
+    wl.check_status()
+    return statistics.median(times) * 1e3, int(h2d), int(d2h)
 
 
 def assemble_host(wl: Workload, rounds: int = 3):
@@ -404,8 +474,15 @@ def roofline(wl: Workload, ms: float, pk):
         return dict(bound="tensor", achieved=round(ach, 2), peak=pk["bf16"], unit="TFLOP/s",
                     frac=round(ach / pk["bf16"], 4))
     ach = wl.bytes / (ms * 1e-3) / 1e9
-    return dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm"], unit="GB/s",
-                frac=round(ach / pk["hbm"], 4))
+    r = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm"], unit="GB/s",
+             frac=round(ach / pk["hbm"], 4))
+    if wl.kind == "decode":
+        # decode also runs the two contractions on the tensor cores (2176 flop per (head, key));
+        # with shared pool chunks served from L2 (V3-shaped decode) that can be the tighter bound
+        tf = wl.flops / (ms * 1e-3) / 1e12
+        r["tensor"] = dict(achieved=round(tf, 2), peak=pk["bf16"], unit="TFLOP/s",
+                           frac=round(tf / pk["bf16"], 4))
+    return r
 
 
 KERNEL_SOURCES = {
@@ -442,44 +519,216 @@ def traffic_for(name):
 
 # --------------------------------------------------------------------------- oracle arm
 
-def oracle_sample(name, budget_s=None, steps=None, warmup=0):
-    """Times the fp64 oracle on (request, head) units of the workload; each unit assembles
-    the request's rows and computes one head's attention.  Returns (GB/s-equivalent,
-    seconds, units, threads) where one unit counts ctx*1152/H bytes (the GPU reads the KV
-    once for all H heads)."""
+def _host_cores():
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except AttributeError:
+        aff = os.cpu_count()
+    return os.cpu_count(), aff
+
+
+_ORACLE_CASES = {}
+
+
+def _oracle_case(name):
+    """Inputs of a workload on the host (generated once per process)."""
+    key = "rotate_gather" if name.startswith("rotate_gather_") else name
+    if key not in _ORACLE_CASES:
+        _ORACLE_CASES.clear()
+        _ORACLE_CASES[key] = _make_oracle_case(name)
+    return _ORACLE_CASES[key]
+
+
+def _make_oracle_case(name):
+    from mla_position_independent_gb300 import synth
+    import oracle
+    if name == "tiny":
+        case = synth.tiny_case(0)
+        enc = oracle.rotate(case.rope_content, case.rope_pos)
+        case.kv_rows[torch.as_tensor(case.rope_rows), 512:] = torch.from_numpy(enc).to(torch.bfloat16)
+    elif name.startswith("rotate_gather_"):
+        case = synth.rotate_gather_case(1 << 20, 0)
+    else:
+        case = {"v2lite_decode": synth.v2lite_decode, "v3_decode": synth.v3_decode,
+                "chunked_prefill": synth.chunked_prefill,
+                "chunked_prefill_256": lambda seed: synth.chunked_prefill(seed, n_q=256)}[name](0)
+    kv = synth.bits(case.kv_rows)
+    ql = qr = None
+    if case.q_lat is not None:
+        ql, qr = synth.bits(case.q_lat), synth.bits(case.q_rope)
+    return case, kv, ql, qr
+
+
+def _oracle_units(name, case):
+    """The oracle's units of work on a workload and the algorithmic amount each stands for
+    (the GPU metric's unit: KV bytes for decode, flops for prefill, bytes moved for
+    rotate+gather).  Decode: one request with all its heads in one call (the oracle
+    assembles the request once and runs its H query rows in parallel).  Prefill: one
+    request with 8 query positions (always the first and the last) x 16 heads.  Tiny: the
+    whole case.  Rotate+gather: the whole 1M-row table."""
+    rng = np.random.default_rng(0)
+    if name.startswith("rotate_gather_"):
+        return [("gather", None, 2.0 * int(case.ctx.sum()) * ROW_BYTES)], "GB/s", 1e9
+    B, n_q, H = case.q_lat.shape[:3]
+    ctx = case.ctx
+    if name == "tiny":
+        sel = np.stack(np.meshgrid([0], np.arange(n_q), np.arange(H), indexing="ij"), -1).reshape(-1, 3)
+        return [("attn", sel, _attn_amount(case, sel))], "TFLOP/s", 1e12
+    if n_q == 1:
+        units = []
+        for b in rng.permutation(B):
+            sel = np.array([[b, 0, h] for h in range(H)])
+            units.append(("attn", sel, _attn_amount(case, sel)))
+        return units, "GB/s", 1e9
+    units = []
+    for b in rng.permutation(B):
+        qs = np.unique(np.concatenate([[0, n_q - 1], rng.choice(n_q, 6, replace=False)]))
+        hs = rng.choice(H, 16, replace=False)
+        sel = np.array([[b, i, h] for i in qs for h in hs])
+        units.append(("attn", sel, _attn_amount(case, sel)))
+    return units, "TFLOP/s", 1e12
+
+
+def _attn_amount(case, sel):
+    """What the selected (b, i, h) rows stand for in the GPU metric: decode reads each KV row
+    once for all H heads, so a row counts ctx_b * 1152 / H bytes; prefill counts the flops of
+    its visible keys."""
+    B, n_q, H = case.q_lat.shape[:3]
+    ctx = case.ctx
+    if n_q == 1:
+        return float(sum(ctx[b] for b in sel[:, 0])) * ROW_BYTES / H
+    return float(sum(ctx[b] - n_q + i + 1 for b, i in sel[:, :2])) * PAIR_FLOPS
+
+
+def oracle_sample(name, budget_s=10.0, max_units=None, threads=None):
+    """Times the fp64 oracle, as it stands, on units of a workload (see _oracle_units), until
+    `budget_s` seconds or `max_units` units.  Returns dict(value, unit, seconds, units,
+    threads, sample)."""
     import oracle
     from mla_position_independent_gb300 import synth
-    case = {"v2lite_decode": synth.v2lite_decode, "v3_decode": synth.v3_decode,
-            "chunked_prefill": synth.chunked_prefill,
-            "chunked_prefill_256": lambda seed: synth.chunked_prefill(seed, n_q=256)}[name](0)
-    kv = synth.bits(case.kv_rows)
-    ql, qr = synth.bits(case.q_lat), synth.bits(case.q_rope)
-    B, n_q, H = ql.shape[:3]
-    ctx = case.ctx
-    rng = np.random.default_rng(0)
-    units = [(b, n_q - 1, h) for b in range(B) for h in range(H)]
-    rng.shuffle(units)
-    done_bytes, t_total, n = 0.0, 0.0, 0
-    i = 0
+    oracle.build()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    case, kv, ql, qr = _oracle_case(name)
+    units, unit, div = _oracle_units(name, case)
+    if threads == 1:
+        if name.startswith("rotate_gather_"):
+            # one thread: the first 65536 target rows (the whole table would take minutes)
+            rows = np.stack([np.zeros(1 << 16, np.int64), np.arange(1 << 16)], 1)
+            units = [("gather_rows", rows, 2.0 * (1 << 16) * ROW_BYTES)]
+        elif name != "tiny":
+            # one thread: 16 rows of the first unit
+            sel = units[0][1][:16]
+            units = [("attn", sel, _attn_amount(case, sel))]
+    done, secs, n, i = 0.0, 0.0, 0, 0
     while True:
-        b, qi, h = units[i % len(units)]
+        kind, sel, amount = units[i % len(units)]
         t0 = time.perf_counter()
-        oracle.mla_attention(ql, qr, case.chunks, case.indptr, kv, 1 / math.sqrt(192),
-                             select=np.array([[b, qi, h]]))
-        dt = time.perf_counter() - t0
-        if i >= warmup:
-            t_total += dt
-            done_bytes += ctx[b] * ROW_BYTES / H
-            n += 1
+        if kind == "gather":
+            oracle.rotate_gather(kv, case.chunks, case.indptr, case.page_table)
+        elif kind == "gather_rows":
+            oracle.rotate_gather(kv, case.chunks, case.indptr, case.page_table, rows=sel)
+        else:
+            oracle.mla_attention(ql, qr, case.chunks, case.indptr, kv, 1 / math.sqrt(192), select=sel)
+        secs += time.perf_counter() - t0
+        done += amount
+        n += 1
         i += 1
-        if steps is not None and n >= steps:
+        if max_units is not None and n >= max_units:
             break
-        if budget_s is not None and t_total >= budget_s:
+        if secs >= budget_s or (name == "tiny" and n >= 1) or kind.startswith("gather"):
             break
-    return done_bytes / t_total / 1e9, t_total, n, oracle.num_threads()
+    thr = oracle.num_threads()
+    return dict(value=done / secs / div, unit=unit, seconds=secs, units=n, threads=thr)
+
+
+def cpu_baseline(name, budget_s=8.0, one_thread_budget_s=3.0):
+    """The oracle on the host cores (all of them, then one thread) on a bounded sample of a
+    workload; the figures are per unit of the GPU metric, extrapolated where the sample is
+    a subset."""
+    import oracle
+    ncpu, aff = _host_cores()
+    full = oracle_sample(name, budget_s=budget_s, threads=aff)
+    one = oracle_sample(name, budget_s=one_thread_budget_s, max_units=1, threads=1)
+    oracle.set_num_threads(aff)
+    what = {"tiny": "the whole case (16 queries x 16 heads)",
+            "v2lite_decode": "whole requests (all 16 heads each)",
+            "v3_decode": "whole requests (all 128 heads each) of the 64; extrapolated to the batch",
+            "chunked_prefill": "(request, 8 query positions incl. the first and last, 16 heads) "
+                               "units; extrapolated per flop to the whole prefill"}
+    if name.startswith("rotate_gather_"):
+        samp = "the whole 1M-row rotate+gather" + ("" if name == "rotate_gather_1M" else
+                                                   f"; extrapolated per row to {name[14:]} rows")
+    else:
+        samp = f"{full['units']} units: {what.get(name, name)}"
+    return dict(value=round(full["value"], 6), unit=full["unit"], cores=full["threads"],
+                threads_used=full["threads"], host_cpus=ncpu, affinity=aff, kind="oracle",
+                sample=f"{samp}; {full['seconds']:.1f} s of oracle time",
+                one_thread=dict(value=round(one["value"], 6), unit=one["unit"],
+                                seconds=round(one["seconds"], 2), units=one["units"]),
+                extrapolated=name not in ("tiny", "v2lite_decode", "rotate_gather_1M"))
 
 
 # --------------------------------------------------------------------------- main
+
+# extra workloads reported beside the headline: timed steps each
+EXTRA_STEPS = {"tiny": 200, "v3_decode": 100, "chunked_prefill": 20, "rotate_gather_1M": 100,
+               "rotate_gather_4M": 50, "rotate_gather_16M": 20, "rotate_gather_64M": 20,
+               "cdc_4M": 100}
+E2E_STEPS = {"decode": 200, "prefill": 5, "gather": 20}
+
+
+def _value_unit(wl, ms):
+    if wl.kind == "prefill":
+        return wl.flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    return wl.bytes / (ms * 1e-3) / 1e9, "GB/s"
+
+
+def measure(name, steps, warmup, pk, device_index, rank, want_cpu, want_e2e=True):
+    """One workload: device-timed steps with their clock record, the roofline of its kernel,
+    the end-to-end figure through the C ABI, and the oracle on the host cores."""
+    wl = Workload(name, seed=rank)
+    per_step, clocks = timed(wl, steps, warmup, device_index)
+    ms = statistics.mean(per_step)
+    val, unit = _value_unit(wl, ms)
+    ent = dict(value=round(val, 4), unit=unit, ms_per_step=round(ms, 5), steps=steps,
+               clocks=clocks, description=DESCR.get(name))
+    if wl.kind != "cdc":
+        r = roofline(wl, ms, pk)
+        r["kernel"] = wl.kernel_name()
+        r["traffic"] = traffic_for(name)
+        ent["roofline"] = r
+        ent["table_bytes"] = wl.table_bytes
+    if wl.kind == "gather":
+        ent["rows_per_s"] = round(wl.ctx_total / (ms * 1e-3), 1)
+    elif wl.kind == "cdc":
+        ent["tokens_per_s"] = round(wl.n_tokens / (ms * 1e-3), 1)
+        ent["hbm_frac"] = round(wl.bytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)
+        ent["assemble_host"] = assemble_host(wl)
+    if want_e2e and wl.kind in E2E_STEPS:
+        e_ms, h2d, d2h = e2e(wl, E2E_STEPS[wl.kind])
+        ev, _ = _value_unit(wl, e_ms)
+        ent["e2e"] = dict(value=round(ev, 4), unit=unit, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                          ms_per_step=round(e_ms, 4), ratio_to_device_step=round(e_ms / ms, 3),
+                          note="median wall clock per step: H2D of the step's inputs from "
+                               "page-locked host memory, the C-ABI call (host chunk table "
+                               "validated and copied into the workspace), read-back of the "
+                               "result, synchronize")
+    lp = wl.launches_per_step()
+    del wl
+    torch.cuda.empty_cache()
+    if want_cpu and not name.startswith("cdc_"):
+        ent["cpu_baseline"] = cpu_baseline(name)
+    return ent, lp
+
+
+def run_config(name, world):
+    """The `config` of the JSON line (the same for the GPU arm and the oracle arm)."""
+    return dict(workload=name, description=DESCR.get(name),
+                step="one C-ABI call: chunk-table copy into the workspace + the fused kernel(s), "
+                     "replayed from a CUDA graph",
+                l2=L2_NOTE, parallelism=f"replicas x{world}" if world > 1 else "single GPU")
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -499,19 +748,26 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        steps = max(1, min(args.steps, 200))
-        value, secs, n, thr = oracle_sample(args.workload, steps=steps, warmup=min(args.warmup, 2))
-        line = dict(metric=METRIC, value=round(value, 4), unit="GB/s", n_gpus=args.gpus,
-                    steps=args.steps, warmup=args.warmup, impl="reference",
-                    ms_per_step=round(secs / n * 1e3, 3), higher_is_better=True,
+        import oracle
+        ncpu, aff = _host_cores()
+        oracle.build()
+        oracle.set_num_threads(aff)
+        steps = max(1, min(args.steps, 50))
+        if args.warmup > 0:
+            oracle_sample(args.workload, budget_s=5.0, max_units=min(args.warmup, 2))
+        r = oracle_sample(args.workload, budget_s=60.0, max_units=steps)
+        line = dict(metric=METRIC, value=round(r["value"], 6), unit=r["unit"], n_gpus=args.gpus,
+                    steps=r["units"], warmup=min(args.warmup, 2), impl="reference",
+                    ms_per_step=round(r["seconds"] / r["units"] * 1e3, 3), higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                    config=dict(workload=args.workload, description=DESCR.get(args.workload)),
-                    cpu_baseline=dict(value=round(value, 4), unit="GB/s", cores=thr, kind="oracle",
-                                      sample=f"{n} (request, head) units of {args.workload}, "
-                                             f"each assembling the request's rows in fp64 and "
-                                             f"computing one head's attention; bytes counted as "
-                                             f"ctx*1152/H per unit"),
-                    e2e=dict(value=round(value, 4), unit="GB/s", h2d_bytes_per_step=0,
+                    config=run_config(args.workload, world=1),
+                    cpu_baseline=dict(value=round(r["value"], 6), unit=r["unit"], cores=r["threads"],
+                                      host_cpus=ncpu, affinity=aff, kind="oracle",
+                                      sample=f"{r['units']} oracle units of {args.workload} "
+                                             f"({r['seconds']:.1f} s); a unit is a whole request "
+                                             f"with all its heads for decode, (request, 8 query "
+                                             f"positions, 16 heads) for prefill"),
+                    e2e=dict(value=round(r["value"], 6), unit=r["unit"], h2d_bytes_per_step=0,
                              d2h_bytes_per_step=0))
         print(json.dumps(line), flush=True)
         return
@@ -528,53 +784,40 @@ def main():
     barrier(world)
     ms = statistics.mean(per_step)
     ms = max_over_ranks(ms, world)
-    unit_val = wl.bytes if wl.kind != "prefill" else wl.flops
-    if wl.kind == "prefill":
-        value = world * wl.flops / (ms * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    else:
-        value = world * wl.bytes / (ms * 1e-3) / 1e9
-        unit = "GB/s"
+    val, unit = _value_unit(wl, ms)
+    value = world * val
     rf = roofline(wl, ms, pk)
     rf["peak_source"] = pk["src"]
     rf["kernel"] = wl.kernel_name()
     rf["traffic"] = traffic_for(args.workload)
-    e2e = None
-    if wl.kind == "decode":
-        e2e_ms, h2d, d2h = e2e_decode(wl, min(args.steps, 200))
-        e2e = dict(value=round(world * wl.bytes / (e2e_ms * 1e-3) / 1e9, 2), unit=unit,
-                   h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
-                   ms_per_step=round(e2e_ms, 4),
-                   note="wall clock per step: H2D of queries and chunk table from pinned host "
-                        "memory, the C-ABI call, D2H of the output, synchronize")
+    e2e_d = None
+    if wl.kind in E2E_STEPS:
+        e_ms, h2d, d2h = e2e(wl, min(args.steps, E2E_STEPS[wl.kind]))
+        e_ms = max_over_ranks(e_ms, world)
+        ev, _ = _value_unit(wl, e_ms)
+        e2e_d = dict(value=round(world * ev, 2), unit=unit, h2d_bytes_per_step=h2d,
+                     d2h_bytes_per_step=d2h, ms_per_step=round(e_ms, 4),
+                     ratio_to_device_step=round(e_ms / ms, 3),
+                     note="median wall clock per step: H2D of the queries from page-locked host "
+                          "memory, the C-ABI call (host chunk table validated and copied into "
+                          "the workspace, kernel launch), D2H of the output, synchronize")
     line = dict(metric=METRIC, value=round(value, 2), unit=unit, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(ms, 5), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
-                config=dict(workload=args.workload, description=DESCR.get(args.workload),
-                            requests=(wl.table.B if wl.table is not None else len(wl.offsets) - 1),
-                            ctx_total=wl.ctx_total,
-                            l2=L2_NOTE,
-                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-                roofline=rf, e2e=e2e, gpu_launches=args.steps * wl.launches_per_step(),
+                config=run_config(args.workload, world),
+                roofline=rf, e2e=e2e_d, gpu_launches=args.steps * wl.launches_per_step(),
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"],
                             reasons=clocks["reasons"], samples=clocks["samples"]))
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, secs, n, thr = oracle_sample("v2lite_decode" if wl.kind != "prefill" else args.workload,
-                                        budget_s=12.0)
-        line["cpu_baseline"] = dict(value=round(v, 4), unit="GB/s", cores=thr, kind="oracle",
-                                    sample=f"{n} (request, head) units of v2lite_decode in "
-                                           f"{secs:.1f} s; bytes counted as ctx*1152/H per unit")
+    del wl
+    torch.cuda.empty_cache()
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if want_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     if not args.no_extras and world == 1:
         extras = {}
-        steps_of = {"v3_decode": 50, "chunked_prefill": 5, "rotate_gather_1M": 50,
-                    "rotate_gather_4M": 50, "rotate_gather_16M": 20, "rotate_gather_64M": 10,
-                    "cdc_4M": 50}
-        for name, st in steps_of.items():
+        for name, st in EXTRA_STEPS.items():
             if name == args.workload:
                 continue
-            del wl
-            wl = None
-            torch.cuda.empty_cache()
             if name.startswith("rotate_gather_"):
                 # row store + pages (2 x 1152 B per row), plus room for the L2 flush buffers
                 n = int(name.split("_")[-1].rstrip("M")) << 20
@@ -582,24 +825,8 @@ def main():
                 if torch.cuda.mem_get_info()[0] < need:
                     extras[name] = dict(skipped=f"needs {need / 1e9:.1f} GB of free device memory")
                     continue
-            wl = Workload(name, seed=rank)
-            t = statistics.mean(time_steps(wl, st, 3))
-            r = roofline(wl, t, pk)
-            r["kernel"] = wl.kernel_name()
-            ent = dict(ms_per_step=round(t, 4), roofline=r, steps=st)
-            if wl.kind == "gather":
-                ent["rows_per_s"] = round(wl.ctx_total / (t * 1e-3), 1)
-                ent["GB_per_s_moved"] = r["achieved"]
-            elif wl.kind == "cdc":
-                ent["tokens_per_s"] = round(wl.n_tokens / (t * 1e-3), 1)
-            elif wl.kind == "decode":
-                ent["logical_KV_GB_per_s"] = r["achieved"]
-            else:
-                ent["TFLOP_per_s"] = r["achieved"]
-            ent["traffic"] = traffic_for(name)
+            ent, _ = measure(name, st, 3, pk, local, rank, want_cpu)
             extras[name] = ent
-            if wl.kind == "cdc":
-                extras["assemble_host"] = assemble_host(wl)
         line["workloads"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -20,25 +20,45 @@
  *   - A fresh chunk (reused = 0) has delta = 0; its p_src is ignored.
  *   - Query i of n_q sits at position ctx - n_q + i and sees keys t <= that position.
  *
- * Memory and streams.  All pointers named *_dev / device are device memory owned by the
- * caller; pointers named *_host are host memory owned by the caller.  The library keeps
- * no allocation of its own and performs no host<->device copy: a chunk table is passed
- * twice, as the host copy (validated and used for launch geometry) and as a byte-identical
- * device copy (read by the kernels).  Every call is asynchronous on `stream`.  Kernels
- * re-check each source row against n_rows and record (never fault on) a violation.
+ * Memory and streams.  Pointers named *_host are host memory, every other buffer is device
+ * memory; the caller owns all of them, and the library keeps no allocation of its own.
+ * Every call is asynchronous on `stream`.
+ *
+ * Chunk tables.  A call takes the batch's chunk tables in host memory only (chunks_host,
+ * indptr_host, and for irm_cdc_chunk the stream offsets).  The library validates them,
+ * plans the launch from them, and hands those same bytes to the kernels, so the kernels
+ * always run on exactly the table that was validated:
+ *   - The attention calls pass a table of at most 1024 records for at most 256 requests
+ *     inside the kernel launch's parameter block, which the CUDA runtime copies when the
+ *     kernel is launched: no separate copy, any host memory, and the caller may reuse the
+ *     table as soon as the call returns (a captured graph replays the table as validated).
+ *   - Otherwise the library copies the table into the table area of the caller's workspace
+ *     on `stream` (cudaMemcpyAsync, host to device) before the kernels that read it.
+ *     Page-locked (pinned) host tables are copied asynchronously: keep them unchanged until
+ *     `stream` has passed the call.  Under CUDA stream capture the copy becomes part of the
+ *     graph and every replay copies the same host bytes again, so they must stay unchanged
+ *     for as long as the graph is replayed (the launch geometry was planned from them).
+ *     When indptr_host is followed, at the next 8-byte boundary, by chunks_host in one
+ *     pinned block, a single copy moves both; otherwise there is one copy per array.
+ *     Pageable host tables are packed by the library and handed to the CUDA runtime, which
+ *     has read them when the call returns, so the caller may reuse them at once; such a copy
+ *     cannot be captured into a CUDA graph (IRM_ERR_INVALID_ARG during capture).
+ * Kernels still re-check each source row against n_rows and each page index against
+ * n_pages, and record (never fault on) a violation.
  *
  * Errors.  Calls return an irm_status.  No exception crosses the ABI and nothing aborts.
- * Host-side checks happen before any launch.  Device-side problems (a source row out of
- * range because the device table differs from the host table, or a pipeline wait that
+ * Host-side checks happen before any copy or launch.  Device-side problems (a page index
+ * outside the paged output, a source row outside the row store, or a pipeline wait that
  * exceeded its 2 s limit) set bits in the status word at the start of the workspace; read
  * and clear it with irm_device_status().
  *
- * Workspace.  Each call takes a caller-owned device workspace of at least the size its
- * *_workspace_size function reports (>= IRM_WORKSPACE_HEADER bytes).  Its first
- * IRM_WORKSPACE_HEADER bytes hold the device status word.  Zero the whole workspace once
- * before first use: decode keeps split-KV completion counters in it, which every call
- * leaves at zero again.  After a call that reported a device error, zero it again.
- * Calls that share one workspace must not overlap on the GPU.
+ * Workspace.  Each call takes a caller-owned device workspace, 256-byte aligned, of at
+ * least the size its *_workspace_size function reports for the same tables.  Its first
+ * IRM_WORKSPACE_HEADER bytes hold the device status word, the next ones the copied chunk
+ * table, the rest the call's scratch.  Zero the whole workspace once before first use:
+ * decode keeps split-KV completion counters in it, which every call leaves at zero again.
+ * After a call that reported a device error, zero it again.  Calls that share one
+ * workspace must not overlap on the GPU.
  */
 #ifndef IRM_H_
 #define IRM_H_
@@ -154,8 +174,8 @@ irm_status irm_selftest_wait_timeout(void* workspace, size_t workspace_bytes, cu
  *   paged_out[page_table[b*max_pages + t/64]*64 + t%64] = [cKV(src_row) | R(delta) k_r(src_row)]
  * cKV bytes are copied unchanged; rows with delta = 0 are copied bit for bit.
  *
- *   chunks_host, indptr_host, B   host chunk tables (validated)
- *   chunks_dev, indptr_dev        device copies of the same bytes
+ *   chunks_host, indptr_host, B   host chunk tables (validated, then copied into the
+ *                workspace; see "Chunk tables" above)
  *   kv_rows      device bf16 [n_rows, 576], 16-byte aligned
  *   paged_out    device bf16 [n_pages, 64, 576] or NULL (plan only); rows of a page that
  *                no target row maps to are left untouched
@@ -164,11 +184,11 @@ irm_status irm_selftest_wait_timeout(void* workspace, size_t workspace_bytes, cu
  *                is out of range and records IRM_ERR_DEVICE_BOUNDS
  *   out_src_row, out_delta, out_pos_src   device int32 [sum ctx] or NULL; rows are listed
  *                request after request (pos_src = t - delta)
- * Workspace: irm_assemble_kv_workspace_size bytes.
+ * Workspace: irm_assemble_kv_workspace_size bytes for the same tables.
  */
-irm_status irm_assemble_kv_workspace_size(int B, size_t* bytes);
+irm_status irm_assemble_kv_workspace_size(const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                          int B, size_t* bytes);
 irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
-                           const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                            const void* kv_rows, int64_t n_rows, void* paged_out,
                            int64_t n_pages, const int32_t* page_table, int max_pages,
                            int32_t* out_src_row,
@@ -177,7 +197,6 @@ irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_h
 /* Same, with the model's RoPE variant (rope == NULL: the default).  IRM_ERR_INVALID_ARG for a
  * pairing other than the two above, a non-zero reserved field or a non-finite frequency. */
 irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
-                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                 const void* kv_rows, int64_t n_rows, void* paged_out,
                                 int64_t n_pages, const int32_t* page_table, int max_pages,
                                 int32_t* out_src_row, int32_t* out_delta, int32_t* out_pos_src,
@@ -197,14 +216,14 @@ irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* ind
  *   out     device bf16 [B, H, 512]:  O = softmax(s) . cKV, s_t = scale * (q_lat.cKV_t +
  *           q_rope.R(delta_t) k_r,t)
  *   lse     device fp32 [B, H] or NULL: natural-log sum of exp(s_t)
- * Workspace: irm_mla_attn_decode_workspace_size bytes (holds split-KV partials).
+ * Workspace: irm_mla_attn_decode_workspace_size bytes for the same tables and H (the copied
+ * chunk table and the split-KV partials).
  */
 irm_status irm_mla_attn_decode_workspace_size(const irm_chunk* chunks_host,
                                               const int32_t* indptr_host, int B, int H,
                                               size_t* bytes);
 irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int H,
                                const irm_chunk* chunks_host, const int32_t* indptr_host,
-                               const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                const void* kv_rows, int64_t n_rows, float softmax_scale,
                                void* out, float* lse, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
@@ -212,7 +231,6 @@ irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int
  * irm_assemble_kv_rope). */
 irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B, int H,
                                     const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                    const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                     const void* kv_rows, int64_t n_rows, float softmax_scale,
                                     void* out, float* lse, const irm_rope* rope, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
@@ -225,33 +243,40 @@ irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B
  * provide the workspace that irm_mla_attn_decode wants.
  *
  * Same arguments and results as irm_mla_attn_decode, minus the workspace.  The split-KV
- * scratch lives in a fixed 32 MiB device array inside this library (every GPU that loads
- * the library holds it until the process exits).  A decode whose scratch would exceed 32 MiB
- * (IRM_ERR_WORKSPACE) is rejected before anything is launched; use irm_mla_attn_decode then.
- * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.  Each call
- * clears the array's status word and completion counters on `stream` (cudaMemsetAsync) and
- * allocates nothing.  All calls share the one array: calls that overlap on the GPU (other
- * streams, other threads) race and must be serialized by the caller.  Device-side status
- * (timeouts, out-of-range rows) is not reported by this entry point.
+ * scratch and the copied chunk table live in a fixed 32 MiB device array inside this library
+ * (every GPU that loads the library holds it until the process exits).  A decode whose table
+ * and scratch would exceed 32 MiB (IRM_ERR_WORKSPACE) is rejected before anything is copied
+ * or launched; use irm_mla_attn_decode then.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current and caches it per
+ * device ordinal, which assumes the CUDA runtime's primary context of that device (a caller
+ * that binds another context through the driver API must not use this entry point); make
+ * that first call before any stream capture.  Each call clears the array's split-KV
+ * completion counters on `stream` (cudaMemsetAsync) and allocates nothing.  All calls share
+ * the one array: calls that overlap on the GPU (other streams, other threads) race and must
+ * be serialized by the caller.  Device-side status (timeouts, out-of-range rows) collects in
+ * the array's own status word across calls: read and clear it with
+ * irm_decode_noalloc_status().
  */
 irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, int B, int H,
                                        const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                       const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                        const void* kv_rows, int64_t n_rows, float softmax_scale,
                                        void* out, float* lse, cudaStream_t stream);
+/* Reads and clears the status word of the no-allocation scratch array of the current device
+ * (synchronizes `stream`).  Returns what irm_device_status() returns for a workspace. */
+irm_status irm_decode_noalloc_status(cudaStream_t stream);
 
 /*
  * Fused delta-rotate + absorbed MLA prefill attention (n_q causal query tokens per request,
  * the last n_q positions of each request's assembled context).
  *   q_lat [B, n_q, H, 512], q_rope [B, n_q, H, 64], out [B, n_q, H, 512] bf16,
  *   lse [B, n_q, H] fp32 or NULL; 1 <= n_q <= ctx_b for every request.
- * Workspace: irm_mla_attn_prefill_workspace_size bytes.
+ * Workspace: irm_mla_attn_prefill_workspace_size bytes for the same tables.
  */
-irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes);
+irm_status irm_mla_attn_prefill_workspace_size(const irm_chunk* chunks_host,
+                                               const int32_t* indptr_host, int B, int n_q, int H,
+                                               size_t* bytes);
 irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                                 const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                 const void* kv_rows, int64_t n_rows, float softmax_scale,
                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
@@ -259,7 +284,6 @@ irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, in
  * irm_assemble_kv_rope). */
 irm_status irm_mla_attn_prefill_rope(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                                      const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                     const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                      const void* kv_rows, int64_t n_rows, float softmax_scale,
                                      void* out, float* lse, const irm_rope* rope, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream);
@@ -308,8 +332,8 @@ irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_c
 /*
  *   tokens       device int32 [offsets[n_streams]], ids in [0, vocab) (an id outside is
  *                read as gear = 0 and recorded as IRM_ERR_DEVICE_BOUNDS in the status word)
- *   offsets_host / offsets_dev   the stream offsets, host copy (validated, sizes) and a
- *                byte-identical device copy (read by the kernels)
+ *   offsets_host the stream offsets (validated, then copied into the workspace like a
+ *                chunk table; see "Chunk tables" above)
  *   gear         device uint64 [vocab], the Gear table, or NULL for generated Gear words
  *   vocab        token ids lie in [0, vocab)
  *   n_chunks     device int32 [n_streams]: chunks of each stream
@@ -319,8 +343,8 @@ irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_c
  *   chunk_hash   device uint64 [slots] or NULL (no fingerprints)
  * Workspace: irm_cdc_sizes bytes, 256-byte aligned (its status word as for the other calls).
  */
-irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, const int64_t* offsets_dev,
-                         int n_streams, const uint64_t* gear, int32_t vocab,
+irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, int n_streams,
+                         const uint64_t* gear, int32_t vocab,
                          const irm_cdc_params* params, int32_t* n_chunks, int32_t* chunk_start,
                          int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream);

@@ -7,12 +7,15 @@ seeded synthetic workload generators.
 """
 from .binding import (CDC_LOW_BITS, CDC_THRESHOLD, ROPE_INTERLEAVED, ROPE_NEOX, CdcParams,
                       ChunkTable, IrmError, Registry, Rope, cdc_sizes, cdc_slot_base, irm_cdc_chunk,
-                      assemble_kv_workspace_size, decode_workspace_size, device_status,
-                      irm_assemble_kv, irm_mla_attn_decode, irm_mla_attn_prefill, lib,
+                      assemble_kv_workspace_size, decode_noalloc_status, decode_workspace_size,
+                      device_status, irm_assemble_kv, irm_mla_attn_decode,
+                      irm_mla_attn_decode_noalloc, irm_mla_attn_prefill, lib,
                       new_workspace, prefill_workspace_size, selftest_wait_timeout,
                       validate_chunks)
 
 __all__ = ["Registry", "CDC_LOW_BITS", "CDC_THRESHOLD", "CdcParams", "cdc_sizes", "cdc_slot_base",
            "irm_cdc_chunk", "ROPE_INTERLEAVED", "ROPE_NEOX", "Rope", "ChunkTable", "IrmError",
-           "assemble_kv_workspace_size", "decode_workspace_size", "device_status", "irm_assemble_kv", "irm_mla_attn_decode", "irm_mla_attn_prefill",
+           "assemble_kv_workspace_size", "decode_noalloc_status", "decode_workspace_size",
+           "device_status", "irm_assemble_kv", "irm_mla_attn_decode", "irm_mla_attn_decode_noalloc",
+           "irm_mla_attn_prefill",
            "lib", "new_workspace", "prefill_workspace_size", "selftest_wait_timeout", "validate_chunks"]

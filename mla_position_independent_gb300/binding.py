@@ -24,7 +24,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 EXPORTS = ["irm_status_string", "irm_last_error", "irm_version", "irm_validate_chunks",
            "irm_device_status", "irm_assemble_kv_workspace_size", "irm_assemble_kv",
            "irm_assemble_kv_rope", "irm_mla_attn_decode_workspace_size", "irm_mla_attn_decode",
-           "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc",
+           "irm_mla_attn_decode_rope", "irm_mla_attn_decode_noalloc", "irm_decode_noalloc_status",
            "irm_mla_attn_prefill_workspace_size", "irm_mla_attn_prefill", "irm_mla_attn_prefill_rope",
            "irm_cdc_sizes", "irm_cdc_chunk", "irm_registry_create", "irm_registry_stats",
            "irm_registry_assemble", "irm_selftest_wait_timeout"]
@@ -82,23 +82,22 @@ def lib():
         L.irm_validate_chunks.argtypes = [P, P, I, I64, P]
         L.irm_device_status.argtypes = [P, P]
         L.irm_selftest_wait_timeout.argtypes = [P, SZ, P]
-        L.irm_assemble_kv_workspace_size.argtypes = [I, P]
-        L.irm_assemble_kv.argtypes = [P, P, I, P, P, P, I64, P, I64, P, I, P, P, P, P, SZ, P]
+        L.irm_assemble_kv_workspace_size.argtypes = [P, P, I, P]
+        L.irm_assemble_kv.argtypes = [P, P, I, P, I64, P, I64, P, I, P, P, P, P, SZ, P]
         L.irm_mla_attn_decode_workspace_size.argtypes = [P, P, I, I, P]
-        L.irm_mla_attn_decode.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float, P, P, P,
-                                          SZ, P]
-        L.irm_mla_attn_decode_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float,
-                                                  P, P, P]
-        L.irm_mla_attn_prefill_workspace_size.argtypes = [I, I, I, P]
-        L.irm_mla_attn_prefill.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
-                                           P, P, SZ, P]
-        L.irm_assemble_kv_rope.argtypes = [P, P, I, P, P, P, I64, P, I64, P, I, P, P, P, P, P, SZ, P]
-        L.irm_mla_attn_decode_rope.argtypes = [P, P, I, I, P, P, P, P, P, I64, ctypes.c_float, P,
-                                               P, P, P, SZ, P]
-        L.irm_mla_attn_prefill_rope.argtypes = [P, P, I, I, I, P, P, P, P, P, I64, ctypes.c_float,
-                                                P, P, P, P, SZ, P]
+        L.irm_mla_attn_decode.argtypes = [P, P, I, I, P, P, P, I64, ctypes.c_float, P, P, P, SZ, P]
+        L.irm_mla_attn_decode_noalloc.argtypes = [P, P, I, I, P, P, P, I64, ctypes.c_float, P, P, P]
+        L.irm_decode_noalloc_status.argtypes = [P]
+        L.irm_mla_attn_prefill_workspace_size.argtypes = [P, P, I, I, I, P]
+        L.irm_mla_attn_prefill.argtypes = [P, P, I, I, I, P, P, P, I64, ctypes.c_float, P, P, P,
+                                           SZ, P]
+        L.irm_assemble_kv_rope.argtypes = [P, P, I, P, I64, P, I64, P, I, P, P, P, P, P, SZ, P]
+        L.irm_mla_attn_decode_rope.argtypes = [P, P, I, I, P, P, P, I64, ctypes.c_float, P, P, P,
+                                               P, SZ, P]
+        L.irm_mla_attn_prefill_rope.argtypes = [P, P, I, I, I, P, P, P, I64, ctypes.c_float, P, P,
+                                                P, P, SZ, P]
         L.irm_cdc_sizes.argtypes = [P, I, P, P, P]
-        L.irm_cdc_chunk.argtypes = [P, P, P, I, P, ctypes.c_int32, P, P, P, P, P, P, SZ, P]
+        L.irm_cdc_chunk.argtypes = [P, P, I, P, ctypes.c_int32, P, P, P, P, P, P, SZ, P]
         L.irm_registry_create.argtypes = [I64, I64, I64, P]
         L.irm_registry_destroy.argtypes = [P]
         L.irm_registry_destroy.restype = None
@@ -141,15 +140,30 @@ def _need(t, dtype, name, ndim=None):
 
 
 class ChunkTable:
-    """A batch of chunk tables kept twice, as the library wants it: the host copy (validated,
-    used for launch geometry) and a byte-identical device copy (read by the kernels)."""
+    """A batch of chunk tables in host memory, as the library takes them.  With CUDA present
+    the table sits in one page-locked block laid out as the library's workspace table area
+    (indptr [B+1] int32, padded to 8 bytes, then the chunk records), so a call stages it with
+    one asynchronous host-to-device copy; keep it unchanged while calls that use it are in
+    flight.  Without CUDA (host-only validation) it is plain pageable memory."""
 
-    def __init__(self, chunks: np.ndarray, indptr: np.ndarray, device="cuda"):
-        self.chunks_host = np.ascontiguousarray(chunks, dtype=CHUNK_DTYPE)
-        self.indptr_host = np.ascontiguousarray(indptr, dtype=np.int32)
-        self.B = int(self.indptr_host.shape[0] - 1)
-        self.chunks_dev = torch.from_numpy(self.chunks_host.view(np.uint8).copy()).to(device)
-        self.indptr_dev = torch.from_numpy(self.indptr_host.copy()).to(device)
+    def __init__(self, chunks: np.ndarray, indptr: np.ndarray, pinned: bool | None = None):
+        chunks = np.ascontiguousarray(chunks, dtype=CHUNK_DTYPE)
+        indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+        self.B = int(indptr.shape[0] - 1)
+        ia = (4 * (self.B + 1) + 7) // 8 * 8
+        nbytes = ia + chunks.nbytes
+        if pinned is None:
+            pinned = torch.cuda.is_available()
+        buf = torch.zeros(nbytes, dtype=torch.uint8)
+        if pinned:
+            buf = buf.pin_memory()
+        self._buf = buf  # keeps the block alive
+        raw = buf.numpy()
+        self.indptr_host = raw[:4 * (self.B + 1)].view(np.int32)
+        self.chunks_host = raw[ia:ia + chunks.nbytes].view(CHUNK_DTYPE)
+        self.indptr_host[:] = indptr
+        self.chunks_host[:] = chunks
+        self.n_chunks = int(chunks.shape[0])
 
     def validate(self, n_rows: int) -> np.ndarray:
         ctx = np.zeros(self.B, np.int64)
@@ -184,9 +198,10 @@ def selftest_wait_timeout(workspace: torch.Tensor, stream=None):
     _check(lib().irm_selftest_wait_timeout(_ptr(workspace), workspace.numel(), _stream(stream)))
 
 
-def assemble_kv_workspace_size(B: int) -> int:
+def assemble_kv_workspace_size(table: ChunkTable) -> int:
     n = ctypes.c_size_t(0)
-    _check(lib().irm_assemble_kv_workspace_size(int(B), ctypes.byref(n)))
+    _check(lib().irm_assemble_kv_workspace_size(_ptr(table.chunks_host), _ptr(table.indptr_host),
+                                                table.B, ctypes.byref(n)))
     return n.value
 
 
@@ -205,10 +220,10 @@ def irm_assemble_kv(table: ChunkTable, kv_rows: torch.Tensor, paged_out=None, pa
         if t is not None:
             _need(t, torch.int32, n, 1)
     if workspace is None:
-        workspace = new_workspace(assemble_kv_workspace_size(table.B), kv_rows.device)
+        workspace = new_workspace(assemble_kv_workspace_size(table), kv_rows.device)
     _check(lib().irm_assemble_kv_rope(
-        _ptr(table.chunks_host), _ptr(table.indptr_host), table.B, _ptr(table.chunks_dev),
-        _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]), _ptr(paged_out), n_pages,
+        _ptr(table.chunks_host), _ptr(table.indptr_host), table.B,
+        _ptr(kv_rows), int(kv_rows.shape[0]), _ptr(paged_out), n_pages,
         _ptr(page_table), max_pages, _ptr(out_src_row), _ptr(out_delta), _ptr(out_pos_src),
         _rope_ptr(rope), _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
@@ -222,9 +237,10 @@ def decode_workspace_size(table: ChunkTable, H: int) -> int:
     return n.value
 
 
-def prefill_workspace_size(B: int, n_q: int, H: int) -> int:
+def prefill_workspace_size(table: ChunkTable, n_q: int, H: int) -> int:
     n = ctypes.c_size_t(0)
-    _check(lib().irm_mla_attn_prefill_workspace_size(int(B), int(n_q), int(H), ctypes.byref(n)))
+    _check(lib().irm_mla_attn_prefill_workspace_size(_ptr(table.chunks_host), _ptr(table.indptr_host),
+                                                     table.B, int(n_q), int(H), ctypes.byref(n)))
     return n.value
 
 
@@ -245,7 +261,7 @@ def irm_mla_attn_decode(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale
         workspace = new_workspace(decode_workspace_size(table, H), q_lat.device)
     _check(lib().irm_mla_attn_decode_rope(
         _ptr(q_lat), _ptr(q_rope), B, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
-        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        _ptr(kv_rows), int(kv_rows.shape[0]),
         float(softmax_scale), _ptr(out), _ptr(lse), _rope_ptr(rope), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return out, lse, workspace
@@ -266,9 +282,15 @@ def irm_mla_attn_decode_noalloc(q_lat, q_rope, table: ChunkTable, kv_rows,
         _need(lse, torch.float32, "lse")
     _check(lib().irm_mla_attn_decode_noalloc(
         _ptr(q_lat), _ptr(q_rope), B, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
-        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        _ptr(kv_rows), int(kv_rows.shape[0]),
         float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def decode_noalloc_status(stream=None):
+    """Raises IrmError if a no-allocation decode recorded a timeout or an out-of-range row in
+    the library's scratch array (and clears it)."""
+    _check(lib().irm_decode_noalloc_status(_stream(stream)))
 
 
 def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scale=DEFAULT_SCALE,
@@ -285,10 +307,10 @@ def irm_mla_attn_prefill(q_lat, q_rope, table: ChunkTable, kv_rows, softmax_scal
     if lse is not None:
         _need(lse, torch.float32, "lse")
     if workspace is None:
-        workspace = new_workspace(prefill_workspace_size(B, n_q, H), q_lat.device)
+        workspace = new_workspace(prefill_workspace_size(table, n_q, H), q_lat.device)
     _check(lib().irm_mla_attn_prefill_rope(
         _ptr(q_lat), _ptr(q_rope), B, n_q, H, _ptr(table.chunks_host), _ptr(table.indptr_host),
-        _ptr(table.chunks_dev), _ptr(table.indptr_dev), _ptr(kv_rows), int(kv_rows.shape[0]),
+        _ptr(kv_rows), int(kv_rows.shape[0]),
         float(softmax_scale), _ptr(out), _ptr(lse), _rope_ptr(rope), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return out, lse, workspace
@@ -312,7 +334,7 @@ def cdc_slot_base(offsets: np.ndarray, min_len: int = 32) -> np.ndarray:
 
 def irm_cdc_chunk(tokens: torch.Tensor, offsets: np.ndarray, gear: torch.Tensor | None,
                   params: CdcParams | None = None, fingerprints=True, out=None, workspace=None,
-                  stream=None, offsets_dev=None, vocab: int | None = None):
+                  stream=None, vocab: int | None = None):
     """Content-defined chunks of token streams (tokens int32 on the GPU, streams at host
     offsets; gear: the 64-bit Gear table as an int64 tensor on the GPU, or None for Gear
     words generated from params.gear_seed, with token ids in [0, vocab)).  Returns
@@ -334,12 +356,10 @@ def irm_cdc_chunk(tokens: torch.Tensor, offsets: np.ndarray, gear: torch.Tensor 
                torch.empty(max(slots, 1), dtype=torch.int32, device=dev),
                torch.empty(max(slots, 1), dtype=torch.int64, device=dev) if fingerprints else None)
     n_chunks, c_start, c_len, c_hash = out
-    if offsets_dev is None:
-        offsets_dev = torch.from_numpy(offsets.copy()).to(dev)
     if workspace is None:
         workspace = new_workspace(nbytes, dev)
     pp = None if params is None else ctypes.cast(ctypes.pointer(params), ctypes.c_void_p)
-    _check(lib().irm_cdc_chunk(_ptr(tokens), _ptr(offsets), _ptr(offsets_dev), S, _ptr(gear),
+    _check(lib().irm_cdc_chunk(_ptr(tokens), _ptr(offsets), S, _ptr(gear),
                                int(vocab), pp, _ptr(n_chunks), _ptr(c_start), _ptr(c_len),
                                _ptr(c_hash), _ptr(workspace), workspace.numel(), _stream(stream)))
     return n_chunks, c_start, c_len, c_hash, workspace

@@ -47,6 +47,7 @@
 #include <cuda_runtime.h>
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "irm_internal.h"
 #include "irm_pipeline.cuh"
@@ -193,11 +194,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int b = blockIdx.y;
   const int unit = blockIdx.x >> 1;
   const int qtile = unit / a.S, split = unit % a.S;
-  int c_begin = a.indptr[b], c_end = a.indptr[b + 1];
+  // the chunk table: in the parameter block (small tables) or in the workspace
+  const irm_chunk* chunks = a.inline_table ? a.tab.chunks : a.chunks;
+  const int32_t* indptr = a.inline_table ? a.tab.indptr : a.indptr;
+  int c_begin = indptr[b], c_end = indptr[b + 1];
   int ctx = 0;
   const bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks;
   if (table_ok) {
-    const irm_chunk last = a.chunks[c_end - 1];
+    const irm_chunk last = chunks[c_end - 1];
     ctx = last.p_tgt + last.len;
   } else {
     c_begin = c_end = 0;
@@ -706,7 +710,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // slot j % NS once tile j-NS has been published (its copies issued and its k_r rotated),
     // so maps are ready up to NS tiles ahead of the copies.
     ChunkWindow cw;
-    cw.chunks = a.chunks;
+    cw.chunks = chunks;
     cw.c_end = c_end;
     cw.win = c_begin;
     bool ok = true;
@@ -840,9 +844,21 @@ cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream) {
   if (make_layout(a.Mv, 0).stages < 2 || make_layout(a.Mv, 1).stages < 2)
     return cudaErrorInvalidConfiguration;
   const uint32_t smem = launch_smem(a.Mv);
-  cudaError_t e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
+  {
+    // the kernel's dynamic shared memory limit belongs to the device: raised when a launch
+    // needs more than what was set on this device before
+    static std::mutex mu;
+    static uint32_t set_to[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 128 || set_to[dev] < smem) {
+      e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 128) set_to[dev] = smem;
+    }
+  }
   dim3 grid(2 * a.n_qtiles * a.S, a.B);
   mla_attn_kernel<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();

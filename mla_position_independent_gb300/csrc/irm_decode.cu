@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "irm_internal.h"
 #include "irm_pipeline.cuh"
@@ -193,6 +194,9 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   const int crank = split % C, g = split / C;
   const int b = blockIdx.y;
 
+  // the chunk table: in the parameter block (small tables) or in the workspace
+  const irm_chunk* chunks = a.inline_table ? a.tab.chunks : a.chunks;
+  const int32_t* indptr = a.inline_table ? a.tab.indptr : a.indptr;
   int c_begin, c_end, ctx = 0, c_first = -1;
   if (a.n_hints > 0) {
     const DecodeHint hint = a.hint[b * C * G + split];
@@ -201,14 +205,14 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     ctx = hint.ctx;
     c_first = hint.c_first;
   } else {
-    c_begin = a.indptr[b];
-    c_end = a.indptr[b + 1];
+    c_begin = indptr[b];
+    c_end = indptr[b + 1];
   }
   const bool table_ok = c_begin >= 0 && c_end > c_begin && c_end <= a.n_chunks &&
                         (c_first < 0 || (c_first >= c_begin && c_first < c_end));
   if (table_ok) {
     if (a.n_hints == 0) {
-      const irm_chunk last = a.chunks[c_end - 1];
+      const irm_chunk last = chunks[c_end - 1];
       ctx = last.p_tgt + last.len;
     }
   } else {
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   } else if (warp == kMapWarp) {
     // ======================= row maps: tile t into slot t % 3 once tile t-3's S^T is done ======
     ChunkWindow cw;
-    cw.chunks = a.chunks;
+    cw.chunks = chunks;
     cw.c_end = c_end;
     cw.win = c_begin;
     bool ok = true;
@@ -782,11 +786,21 @@ cudaLaunchConfig_t decode_config(const DecodeArgs& a, cudaStream_t stream, cudaL
   return cfg;
 }
 
+// Kernel attributes belong to the device: they are set once per device (not per launch).
 template <int H>
 cudaError_t prepare_decode() {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)make_dlayout(H).total);
+  static std::mutex mu;
+  static bool done[128];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 128;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(mla_decode_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)make_dlayout(H).total);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<H>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && cached) done[dev] = true;
   return e;
 }
 

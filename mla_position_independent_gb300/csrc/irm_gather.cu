@@ -82,12 +82,20 @@ __global__ void __launch_bounds__(kGatherThreads) rotate_gather_kernel(const Gat
     __syncthreads();
     const int b = req_sh;
     const int len = ch.len;
-    bool src_ok = ch.pool_offset >= 0 && ch.pool_offset + len <= a.n_rows;
+    // The table in the workspace is the validated one; these checks only keep a table that
+    // was overwritten meanwhile (calls overlapping on one workspace) inside every buffer.
+    bool src_ok = len > 0 && ch.p_tgt >= 0 && ch.pool_offset >= 0 && ch.pool_offset + len <= a.n_rows;
+    if (a.paged_out != nullptr)
+      src_ok = src_ok && (int64_t)ch.p_tgt + len <= (int64_t)a.max_pages * kPage;
+    int64_t r0 = 0;
+    if (a.out_src != nullptr && src_ok) {
+      r0 = a.row_start[b] + ch.p_tgt;
+      src_ok = r0 + len <= a.row_start[a.B];
+    }
     if (!src_ok) {
       if (tid == 0) set_status(a.status, kDevErrBounds);
     }
     if (a.out_src != nullptr && src_ok) {
-      const int64_t r0 = a.row_start[b] + ch.p_tgt;
       for (int i = tid; i < len; i += kGatherThreads) {
         a.out_src[r0 + i] = (int32_t)(ch.pool_offset + i);
         a.out_delta[r0 + i] = delta;

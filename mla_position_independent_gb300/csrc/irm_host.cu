@@ -1,11 +1,12 @@
-// C ABI of the library: host-side validation of chunk tables, launch geometry, launches.
-// No allocation, no host<->device copy on any compute path (see include/irm.h).
+// C ABI of the library: host-side validation of chunk tables, the copy of the validated
+// tables into the caller's workspace, launch geometry, launches.  No allocation.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -135,6 +136,84 @@ irm_status validate(const irm_chunk* chunks, const int32_t* indptr, int B, int64
   return IRM_OK;
 }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Table area of a workspace, right after the status header: indptr [B+1] int32 (padded to
+// 8 bytes), then the chunk records.  The kernels read the table from here only.
+size_t indptr_area(int B) { return align_up((size_t)(B + 1) * sizeof(int32_t), 8); }
+size_t table_bytes(int B, int64_t n_chunks) {
+  return align_up(indptr_area(B) + (size_t)n_chunks * sizeof(irm_chunk), 256);
+}
+
+bool host_pinned(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+// A host array and where it goes inside the destination block.
+struct HostPart {
+  const void* src;
+  size_t off, bytes;
+};
+
+// Copies host arrays into a device block on `stream`.  Page-locked arrays are copied
+// directly (one copy when they already sit at the block's offsets in one host block);
+// pageable ones are packed into a host staging buffer and copied once, which the runtime has
+// read when cudaMemcpyAsync returns (pageable copies cannot be captured into a graph).
+irm_status stage_to_device(const HostPart* parts, int n, uint8_t* dst, cudaStream_t stream) {
+  bool pinned = true;
+  for (int i = 0; i < n && pinned; ++i) pinned = host_pinned(parts[i].src);
+  cudaError_t e = cudaSuccess;
+  if (pinned) {
+    const uint8_t* base = static_cast<const uint8_t*>(parts[0].src) - parts[0].off;
+    bool one_block = true;
+    for (int i = 1; i < n; ++i) one_block &= static_cast<const uint8_t*>(parts[i].src) == base + parts[i].off;
+    if (one_block) {
+      const size_t end = parts[n - 1].off + parts[n - 1].bytes;
+      e = cudaMemcpyAsync(dst + parts[0].off, base + parts[0].off, end - parts[0].off, cudaMemcpyHostToDevice,
+                          stream);
+    } else {
+      for (int i = 0; i < n && e == cudaSuccess; ++i)
+        e = cudaMemcpyAsync(dst + parts[i].off, parts[i].src, parts[i].bytes, cudaMemcpyHostToDevice, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "copying the chunk table to the workspace");
+    return IRM_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(IRM_ERR_INVALID_ARG,
+                "a chunk table in pageable host memory cannot be captured into a CUDA graph; "
+                "pass page-locked host memory");
+  thread_local std::vector<uint8_t> staging;
+  const size_t end = parts[n - 1].off + parts[n - 1].bytes;
+  staging.resize(end - parts[0].off);
+  for (int i = 0; i < n; ++i) std::memcpy(staging.data() + (parts[i].off - parts[0].off), parts[i].src, parts[i].bytes);
+  e = cudaMemcpyAsync(dst + parts[0].off, staging.data(), staging.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copying the chunk table to the workspace");
+  return IRM_OK;
+}
+
+// Copies a validated chunk table into the workspace's table area; returns the device
+// addresses the kernels read.
+irm_status stage_table(const irm_chunk* chunks_host, const int32_t* indptr_host, int B, int64_t n_chunks,
+                       void* workspace, cudaStream_t stream, const irm_chunk** chunks_dev,
+                       const int32_t** indptr_dev) {
+  uint8_t* tab = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
+  const HostPart parts[2] = {{indptr_host, 0, (size_t)(B + 1) * sizeof(int32_t)},
+                             {chunks_host, indptr_area(B), (size_t)n_chunks * sizeof(irm_chunk)}};
+  irm_status st = stage_to_device(parts, 2, tab, stream);
+  if (st != IRM_OK) return st;
+  *indptr_dev = reinterpret_cast<const int32_t*>(tab);
+  *chunks_dev = reinterpret_cast<const irm_chunk*>(tab + indptr_area(B));
+  return IRM_OK;
+}
+
 constexpr int kBM = 128;
 constexpr int kBN = 64;
 
@@ -163,8 +242,6 @@ int choose_splits(int B, int64_t max_ctx, int H, int sms) {
   return best;
 }
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
 // Split-KV scratch: fp32 partial O, per-rank partial LSE, finished-split counters.
 size_t partial_o_bytes(int B, int units) {
   return align_up((size_t)B * units * kBM * IRM_D_LAT * sizeof(float), 256);
@@ -181,6 +258,7 @@ struct AttnPlan {
   int qpt, n_qtiles, S;
   bool few_heads;  // decode with H in {16, 32}: the split-KV decode kernel
   int C, G;        // its cluster size and clusters per request
+  size_t scratch_off;  // workspace offset of the split-KV scratch (after header and table)
   size_t ws_bytes;
 };
 
@@ -244,22 +322,22 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
   if (p->n_qtiles > 32767) return fail(IRM_ERR_UNSUPPORTED, "too many query tiles (%d)", p->n_qtiles);
   if (B > 65535) return fail(IRM_ERR_UNSUPPORTED, "B=%d exceeds 65535", B);
   p->few_heads = decode && n_q == 1 && irm::decode_supported(H);
+  p->scratch_off = IRM_WORKSPACE_HEADER + table_bytes(B, info.n_chunks);
   if (p->few_heads) {
     p->S = 1;
     choose_decode_split(B, info.max_ctx, H, &p->C, &p->G);
-    p->ws_bytes = IRM_WORKSPACE_HEADER;
+    p->ws_bytes = p->scratch_off;
     if (p->G > 1)
       p->ws_bytes += decode_gpart_bytes(B, p->G, H) + decode_glse_bytes(B, p->G, H) + decode_counter_bytes(B, p->C);
     return IRM_OK;
   }
   p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms()) : 1;
-  p->ws_bytes = IRM_WORKSPACE_HEADER + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
+  p->ws_bytes = p->scratch_off + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
   return IRM_OK;
 }
 
 irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H,
-                    const irm_chunk* chunks_host, const int32_t* indptr_host,
-                    const irm_chunk* chunks_dev, const int32_t* indptr_dev, const void* kv_rows,
+                    const irm_chunk* chunks_host, const int32_t* indptr_host, const void* kv_rows,
                     int64_t n_rows, float softmax_scale, void* out, float* lse, const irm_rope* rope,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode) {
   TableInfo info;
@@ -270,23 +348,41 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
   AttnPlan pl{};
   if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
-  if (!q_lat || !q_rope || !kv_rows || !out || !chunks_dev || !indptr_dev)
-    return fail(IRM_ERR_INVALID_ARG, "null device pointer");
+  if (!q_lat || !q_rope || !kv_rows || !out) return fail(IRM_ERR_INVALID_ARG, "null device pointer");
   if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_rows, 16) || !aligned(out, 16))
     return fail(IRM_ERR_INVALID_ARG, "q_lat, q_rope, kv_rows and out must be 16-byte aligned");
-  if (!aligned(chunks_dev, 8) || !aligned(indptr_dev, 4) || (lse && !aligned(lse, 4)))
-    return fail(IRM_ERR_INVALID_ARG, "misaligned chunk table or lse pointer");
+  if (lse && !aligned(lse, 4)) return fail(IRM_ERR_INVALID_ARG, "misaligned lse pointer");
   if (!std::isfinite(softmax_scale)) return fail(IRM_ERR_INVALID_ARG, "softmax_scale must be finite");
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.ws_bytes)
     return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
                 pl.ws_bytes, workspace_bytes);
+  // The validated table reaches the kernel in its parameter block when it is small (the
+  // launch copies it), else through the workspace (one host-to-device copy before the launch).
+  const bool inline_tab = info.n_chunks <= irm::kInlineChunks && B + 1 <= irm::kInlineIndptr;
+  const irm_chunk* chunks_dev = nullptr;
+  const int32_t* indptr_dev = nullptr;
+  if (!inline_tab &&
+      (st = stage_table(chunks_host, indptr_host, B, info.n_chunks, workspace, stream, &chunks_dev, &indptr_dev)) !=
+          IRM_OK)
+    return st;
+  auto fill_inline = [&](int* flag, irm::InlineTable* tab) {
+    *flag = inline_tab ? 1 : 0;
+    if (inline_tab) {
+      std::memcpy(tab->chunks, chunks_host, (size_t)info.n_chunks * sizeof(irm_chunk));
+      std::memcpy(tab->indptr, indptr_host, (size_t)(B + 1) * sizeof(int32_t));
+    }
+  };
   if (pl.few_heads) {
-    irm::DecodeArgs d{};
+    // ~30 KB with the inline table: kept off the stack; every field before the table is reset
+    // (the table is written up to its length, and the kernel reads no further)
+    thread_local irm::DecodeArgs d;
+    std::memset(static_cast<void*>(&d), 0, offsetof(irm::DecodeArgs, tab));
     d.q_lat = q_lat;
     d.q_rope = q_rope;
     d.kv = kv_rows;
     d.chunks = chunks_dev;
     d.indptr = indptr_dev;
+    fill_inline(&d.inline_table, &d.tab);
     d.n_rows = n_rows;
     d.n_chunks = info.n_chunks;
     d.B = B;
@@ -294,7 +390,7 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     d.C = pl.C;
     d.G = pl.G;
     if (pl.G > 1) {
-      uint8_t* ws = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
+      uint8_t* ws = static_cast<uint8_t*>(workspace) + pl.scratch_off;
       d.gpart = reinterpret_cast<float*>(ws);
       d.glse = reinterpret_cast<float*>(ws + decode_gpart_bytes(B, pl.G, H));
       d.counters = reinterpret_cast<int*>(ws + decode_gpart_bytes(B, pl.G, H) + decode_glse_bytes(B, pl.G, H));
@@ -326,12 +422,14 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     if (e != cudaSuccess) return cuda_fail(e, "mla decode launch");
     return IRM_OK;
   }
-  irm::AttnArgs a{};
+  thread_local irm::AttnArgs a;  // ~25 KB with the inline table (see above)
+  std::memset(static_cast<void*>(&a), 0, offsetof(irm::AttnArgs, tab));
   a.q_lat = q_lat;
   a.q_rope = q_rope;
   a.kv = kv_rows;
   a.chunks = chunks_dev;
   a.indptr = indptr_dev;
+  fill_inline(&a.inline_table, &a.tab);
   a.n_rows = n_rows;
   a.n_chunks = info.n_chunks;
   a.B = B;
@@ -346,7 +444,7 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   a.out = out;
   a.lse = lse;
   a.status = static_cast<int*>(workspace);
-  uint8_t* ws = static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER;
+  uint8_t* ws = static_cast<uint8_t*>(workspace) + pl.scratch_off;
   if (pl.S > 1) {
     const int units = pl.n_qtiles * pl.S;
     a.opart = reinterpret_cast<float*>(ws);
@@ -388,10 +486,11 @@ irm_status noalloc_scratch(void** out) {
   return IRM_OK;
 }
 
-// Workspace of irm_cdc_chunk: status header, slot and segment bases [S + 1] each, the
+// Workspace of irm_cdc_chunk: status header, the copied stream offsets [S + 1], slot and
+// segment bases [S + 1] each, the
 // candidate bitmask, then per speculative segment its chunk ends [spec_cap] and count.
 struct CdcLayout {
-  size_t base, seg_base, words, spec_ends, spec_count, total;
+  size_t offsets, base, seg_base, words, spec_ends, spec_count, total;
   int64_t n_segs, spec_cap;
 };
 irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
@@ -420,7 +519,8 @@ irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_p
   L.spec_cap = (seg + p->max_len) / p->min_len + 2;  // chunk ends in [seg start, seg end + max_len)
   const size_t words = (size_t)(offsets_host[n_streams] >> 5) + (size_t)n_streams + 1;
   const size_t bases = align_up((size_t)(n_streams + 1) * sizeof(int64_t), 256);
-  L.base = IRM_WORKSPACE_HEADER;
+  L.offsets = IRM_WORKSPACE_HEADER;
+  L.base = L.offsets + bases;
   L.seg_base = L.base + bases;
   L.words = L.seg_base + bases;
   L.spec_ends = L.words + align_up(words * sizeof(uint32_t), 256);
@@ -484,25 +584,28 @@ irm_status irm_device_status(void* workspace, cudaStream_t stream) {
   return IRM_OK;
 }
 
-irm_status irm_assemble_kv_workspace_size(int B, size_t* bytes) {
-  if (B <= 0 || bytes == nullptr) return fail(IRM_ERR_INVALID_ARG, "B must be positive and bytes non-null");
-  *bytes = IRM_WORKSPACE_HEADER + align_up((size_t)(B + 1) * sizeof(int64_t), 256);
+irm_status irm_assemble_kv_workspace_size(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
+                                          size_t* bytes) {
+  if (bytes == nullptr) return fail(IRM_ERR_INVALID_ARG, "bytes is null");
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, INT32_MAX, &info);
+  if (st != IRM_OK) return st;
+  // header, table, row starts [B+1] int64
+  *bytes = IRM_WORKSPACE_HEADER + table_bytes(B, info.n_chunks) + align_up((size_t)(B + 1) * sizeof(int64_t), 256);
   return IRM_OK;
 }
 
 irm_status irm_assemble_kv(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
-                           const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                            const void* kv_rows, int64_t n_rows, void* paged_out, int64_t n_pages,
                            const int32_t* page_table, int max_pages, int32_t* out_src_row,
                            int32_t* out_delta, int32_t* out_pos_src, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-  return irm_assemble_kv_rope(chunks_host, indptr_host, B, chunks_dev, indptr_dev, kv_rows, n_rows,
+  return irm_assemble_kv_rope(chunks_host, indptr_host, B, kv_rows, n_rows,
                               paged_out, n_pages, page_table, max_pages, out_src_row, out_delta,
                               out_pos_src, nullptr, workspace, workspace_bytes, stream);
 }
 
 irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* indptr_host, int B,
-                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                 const void* kv_rows, int64_t n_rows, void* paged_out,
                                 int64_t n_pages, const int32_t* page_table, int max_pages,
                                 int32_t* out_src_row, int32_t* out_delta, int32_t* out_pos_src,
@@ -517,7 +620,6 @@ irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* ind
   const bool plan_out = out_src_row || out_delta || out_pos_src;
   if (plan_out && !(out_src_row && out_delta && out_pos_src))
     return fail(IRM_ERR_INVALID_ARG, "out_src_row, out_delta and out_pos_src go together");
-  if (!chunks_dev || !indptr_dev) return fail(IRM_ERR_INVALID_ARG, "null device chunk table");
   if (paged_out) {
     if (!kv_rows || !page_table) return fail(IRM_ERR_INVALID_ARG, "paged output needs kv_rows and page_table");
     if (!aligned(kv_rows, 16) || !aligned(paged_out, 16))
@@ -527,10 +629,16 @@ irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* ind
       return fail(IRM_ERR_INVALID_ARG, "a context of %lld rows needs more than max_pages=%d pages",
                   (long long)info.max_ctx, max_pages);
   }
-  size_t need = 0;
-  irm_assemble_kv_workspace_size(B, &need);
+  const size_t tab_bytes = table_bytes(B, info.n_chunks);
+  const size_t need = IRM_WORKSPACE_HEADER + tab_bytes + align_up((size_t)(B + 1) * sizeof(int64_t), 256);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
     return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+  if (!paged_out && !plan_out) return IRM_OK;
+  const irm_chunk* chunks_dev = nullptr;
+  const int32_t* indptr_dev = nullptr;
+  if ((st = stage_table(chunks_host, indptr_host, B, info.n_chunks, workspace, stream, &chunks_dev, &indptr_dev)) !=
+      IRM_OK)
+    return st;
   irm::GatherArgs g{};
   g.chunks = chunks_dev;
   g.indptr = indptr_dev;
@@ -549,12 +657,12 @@ irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* ind
   std::memcpy(g.phase.F, phaseF, sizeof g.phase.F);
   g.interleaved = interleaved;
   if (plan_out) {
-    int64_t* row_start = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER);
+    int64_t* row_start =
+        reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER + tab_bytes);
     g.row_start = row_start;
     cudaError_t e = irm::launch_row_start(chunks_dev, indptr_dev, B, row_start, stream);
     if (e != cudaSuccess) return cuda_fail(e, "row-start launch");
   }
-  if (!paged_out && !plan_out) return IRM_OK;
   cudaError_t e = irm::launch_rotate_gather(g, num_sms(), stream);
   if (e != cudaSuccess) return cuda_fail(e, "rotate+gather launch");
   return IRM_OK;
@@ -574,27 +682,24 @@ irm_status irm_mla_attn_decode_workspace_size(const irm_chunk* chunks_host, cons
 
 irm_status irm_mla_attn_decode(const void* q_lat, const void* q_rope, int B, int H,
                                const irm_chunk* chunks_host, const int32_t* indptr_host,
-                               const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                const void* kv_rows, int64_t n_rows, float softmax_scale, void* out,
                                float* lse, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
-  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, kv_rows,
                   n_rows, softmax_scale, out, lse, nullptr, workspace, workspace_bytes, stream, true);
 }
 
 irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B, int H,
                                     const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                    const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                     const void* kv_rows, int64_t n_rows, float softmax_scale,
                                     void* out, float* lse, const irm_rope* rope, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream) {
-  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, kv_rows,
                   n_rows, softmax_scale, out, lse, rope, workspace, workspace_bytes, stream, true);
 }
 
 irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, int B, int H,
                                        const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                       const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                        const void* kv_rows, int64_t n_rows, float softmax_scale,
                                        void* out, float* lse, cudaStream_t stream) {
   TableInfo info;
@@ -604,28 +709,35 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
   if (pl.ws_bytes > kNoAllocScratchBytes)
     return fail(IRM_ERR_WORKSPACE,
-                "this decode needs %zu bytes of scratch, more than the %zu bytes the no-allocation "
+                "this decode needs %zu bytes of table and scratch, more than the %zu bytes the no-allocation "
                 "entry point holds; use irm_mla_attn_decode with a workspace",
                 pl.ws_bytes, kNoAllocScratchBytes);
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws)) != IRM_OK) return st;
-  // The array keeps the last call's contents: clear the status word and the split-KV
-  // completion counters, which must start at zero.
-  cudaError_t e = cudaMemsetAsync(ws, 0, IRM_WORKSPACE_HEADER, stream);
-  if (e == cudaSuccess && pl.few_heads && pl.G > 1) {
-    const size_t off = IRM_WORKSPACE_HEADER + decode_gpart_bytes(B, pl.G, H) + decode_glse_bytes(B, pl.G, H);
+  // The array keeps the last call's contents: clear the split-KV completion counters, which
+  // must start at zero.  The status word is left alone, so that a device error of any call
+  // stays readable through irm_decode_noalloc_status().
+  cudaError_t e = cudaSuccess;
+  if (pl.few_heads && pl.G > 1) {
+    const size_t off = pl.scratch_off + decode_gpart_bytes(B, pl.G, H) + decode_glse_bytes(B, pl.G, H);
     e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + off, 0, decode_counter_bytes(B, pl.C), stream);
   }
   if (e == cudaSuccess && !pl.few_heads && pl.S > 1) {
     const int units = pl.n_qtiles * pl.S;
-    const size_t off = IRM_WORKSPACE_HEADER + partial_o_bytes(B, units) + partial_lse_bytes(B, units);
+    const size_t off = pl.scratch_off + partial_o_bytes(B, units) + partial_lse_bytes(B, units);
     e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + off, 0, counter_bytes(B, pl.n_qtiles), stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
-  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+  return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, kv_rows,
                   n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true);
 }
 
+irm_status irm_decode_noalloc_status(cudaStream_t stream) {
+  void* ws = nullptr;
+  irm_status st = noalloc_scratch(&ws);
+  if (st != IRM_OK) return st;
+  return irm_device_status(ws, stream);
+}
 
 irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
                          size_t* bytes, int64_t* slots) {
@@ -635,8 +747,8 @@ irm_status irm_cdc_sizes(const int64_t* offsets_host, int n_streams, const irm_c
   return cdc_check(offsets_host, n_streams, params, &p, slots, &mx, bytes);
 }
 
-irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, const int64_t* offsets_dev,
-                         int n_streams, const uint64_t* gear, int32_t vocab,
+irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, int n_streams,
+                         const uint64_t* gear, int32_t vocab,
                          const irm_cdc_params* params, int32_t* n_chunks, int32_t* chunk_start,
                          int32_t* chunk_len, uint64_t* chunk_hash, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream) {
@@ -647,16 +759,19 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, con
   irm_status st = cdc_check(offsets_host, n_streams, params, &p, &slots, &max_len, &need, &lay);
   if (st != IRM_OK) return st;
   if (vocab <= 0) return fail(IRM_ERR_INVALID_ARG, "vocab must be positive");
-  if (!offsets_dev || !n_chunks || !chunk_start || !chunk_len ||
+  if (!n_chunks || !chunk_start || !chunk_len ||
       (!tokens && offsets_host[n_streams] > 0))
     return fail(IRM_ERR_INVALID_ARG, "null device pointer");
-  if (!aligned(tokens, 4) || !aligned(offsets_dev, 8) || !aligned(gear, 8) || !aligned(chunk_hash, 8))
+  if (!aligned(tokens, 4) || !aligned(gear, 8) || !aligned(chunk_hash, 8))
     return fail(IRM_ERR_INVALID_ARG, "misaligned device pointer");
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
     return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const HostPart part = {offsets_host, 0, (size_t)(n_streams + 1) * sizeof(int64_t)};
+  if ((st = stage_to_device(&part, 1, ws + lay.offsets, stream)) != IRM_OK) return st;
   irm::CdcArgs a{};
   a.tokens = tokens;
-  a.offsets = offsets_dev;
+  a.offsets = reinterpret_cast<const int64_t*>(ws + lay.offsets);
   a.S = n_streams;
   a.gear = gear;
   a.gear_seed = p.gear_seed;
@@ -666,7 +781,6 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, con
   a.bits = p.bits;
   a.mode = p.mode;
   a.seed = p.seed;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<int*>(ws);
   a.base = reinterpret_cast<int64_t*>(ws + lay.base);
   a.seg_base = reinterpret_cast<int64_t*>(ws + lay.seg_base);
@@ -683,30 +797,33 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, con
   return IRM_OK;
 }
 
-irm_status irm_mla_attn_prefill_workspace_size(int B, int n_q, int H, size_t* bytes) {
-  if (bytes == nullptr || B <= 0 || n_q <= 0 || H <= 0 || H > IRM_MAX_HEADS)
-    return fail(IRM_ERR_INVALID_ARG, "bad arguments");
-  *bytes = IRM_WORKSPACE_HEADER;
+irm_status irm_mla_attn_prefill_workspace_size(const irm_chunk* chunks_host, const int32_t* indptr_host,
+                                               int B, int n_q, int H, size_t* bytes) {
+  if (bytes == nullptr) return fail(IRM_ERR_INVALID_ARG, "bytes is null");
+  TableInfo info;
+  irm_status st = validate(chunks_host, indptr_host, B, INT32_MAX, &info);
+  if (st != IRM_OK) return st;
+  AttnPlan pl{};
+  if ((st = plan_attn(info, B, n_q, H, false, &pl)) != IRM_OK) return st;
+  *bytes = pl.ws_bytes;
   return IRM_OK;
 }
 
 irm_status irm_mla_attn_prefill(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                                 const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                 const void* kv_rows, int64_t n_rows, float softmax_scale, void* out,
                                 float* lse, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
-  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, kv_rows,
                   n_rows, softmax_scale, out, lse, nullptr, workspace, workspace_bytes, stream, false);
 }
 
 irm_status irm_mla_attn_prefill_rope(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                                      const irm_chunk* chunks_host, const int32_t* indptr_host,
-                                     const irm_chunk* chunks_dev, const int32_t* indptr_dev,
                                      const void* kv_rows, int64_t n_rows, float softmax_scale,
                                      void* out, float* lse, const irm_rope* rope, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream) {
-  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, chunks_dev, indptr_dev, kv_rows,
+  return run_attn(q_lat, q_rope, B, n_q, H, chunks_host, indptr_host, kv_rows,
                   n_rows, softmax_scale, out, lse, rope, workspace, workspace_bytes, stream, false);
 }
 

@@ -33,6 +33,16 @@ struct GatherArgs {
   } phase;
 };
 
+// A small chunk table travels inside the kernel's parameter block: the launch copies it from
+// the validated host table, so no separate host-to-device copy (and no wait for one)
+// precedes the kernel.  Kernels read it through the parameter's address (param space).
+constexpr int kInlineChunks = 1024;
+constexpr int kInlineIndptr = 257;  // B <= 256
+struct InlineTable {
+  irm_chunk chunks[kInlineChunks];
+  int32_t indptr[kInlineIndptr];
+};
+
 // Fused attention (decode and prefill share one kernel).
 struct AttnArgs {
   const void* q_lat;    // bf16 [B, n_q, H, 512]
@@ -58,6 +68,8 @@ struct AttnArgs {
   struct {
     uint64_t F[32];
   } phase;
+  int inline_table;  // 1: the table is `tab` below (chunks / indptr unused)
+  InlineTable tab;
 };
 
 // Split-KV decode for a few heads (one query token per request): one CTA per (request,
@@ -95,7 +107,11 @@ struct DecodeArgs {
   } phase;
   int n_hints;      // B * C * G when the hints below are filled in, else 0
   DecodeHint hint[kDecodeHints];  // [b * C * G + split]
+  int inline_table;  // 1: the table is `tab` below (chunks / indptr unused)
+  InlineTable tab;
 };
+// kernel parameter blocks are limited to 32764 bytes
+static_assert(sizeof(DecodeArgs) <= 32764 && sizeof(AttnArgs) <= 32764, "kernel parameter block");
 
 // Content-defined chunking of a batch of token streams.
 struct CdcArgs {

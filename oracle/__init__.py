@@ -78,6 +78,8 @@ def _load():
             lib.oracle_attn.argtypes = [P, P, I, P, I, ctypes.c_double, P, P]
             lib.oracle_widen.argtypes = [P, I, P]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_num_threads.restype = None
             lib.oracle_gear_hash.argtypes = [P, I, P, P]
             lib.oracle_cdc.argtypes = [P, I, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, P, P]
@@ -101,6 +103,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls (for timing only; results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def rope_theta() -> np.ndarray:

@@ -227,6 +227,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Sets the number of OpenMP threads of later calls (timing runs; results do not depend on it). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------------------
  * Content-defined chunking of a token stream [summary §2.2, walkthrough §6].
  *   Gear hash over a 64-token window: h_i = sum_{k=0}^{min(i,63)} G[x_{i-k}] * 2^k

@@ -190,10 +190,12 @@ def test_decode_v2lite_full(oracle_mod, q_std):
 
 
 def test_decode_v3_sampled(oracle_mod):
+    """The full V3-shaped decode, checked on 4 heads of every one of the 64 requests (head 0,
+    head 127 and two seeded ones), so every request's KV split and merge is covered."""
     case = synth.v3_decode(0, device="cuda")
     rng = np.random.default_rng(5)
-    bs = rng.choice(64, 3, replace=False)
-    sel = np.array([[b, 0, h] for b in bs for h in rng.choice(128, 12, replace=False)])
+    sel = np.array([[b, 0, h] for b in range(64)
+                    for h in np.unique(np.concatenate([[0, 127], rng.choice(126, 2, replace=False) + 1]))])
     _check_attn(case, oracle_mod, prefill=False, select=sel)
 
 
@@ -204,9 +206,20 @@ def test_decode_v3_sharp_sampled(oracle_mod):
 
 
 def test_prefill_chunked_sampled(oracle_mod):
+    """The full chunked prefill (128 heads: a 128-row query tile is one query), checked in
+    every request on one query of every block of 64 consecutive query tiles (two heads each)
+    and on the first, second and last query (three heads each).  Every query sees the whole
+    prefix, so every KV tile, including each one that straddles a chunk boundary, enters
+    every sampled row."""
     case = synth.chunked_prefill(0, device="cuda")
-    sel = np.array([[b, i, h] for b in (0, 3) for i in (0, 1, 1000, 2047) for h in (0, 64, 127)])
-    _check_attn(case, oracle_mod, prefill=True, select=sel)
+    rng = np.random.default_rng(6)
+    sel = []
+    for b in range(4):
+        for blk in range(0, 2048, 64):
+            i = blk + int(rng.integers(0, 64))
+            sel += [[b, i, int(h)] for h in rng.choice(128, 2, replace=False)]
+        sel += [[b, i, h] for i in (0, 1, 2047) for h in (0, 64, 127)]
+    _check_attn(case, oracle_mod, prefill=True, select=np.array(sel))
 
 
 @pytest.mark.parametrize("H", [8, 16, 32, 64, 128])
@@ -307,16 +320,117 @@ def test_decode_beyond_launch_hints(oracle_mod, H):
     _check_attn(case, oracle_mod, prefill=False, select=sel, what=f"decode 300 requests H={H}")
 
 
-def test_device_table_mismatch_is_recorded_not_faulted(oracle_mod):
-    """A device chunk table whose rows leave the row store (the host copy is valid) is caught
-    by the kernels' bounds check: rows are zero filled and the status word is set."""
-    case = to_device(synth.custom_case([[(0, 32, 0, 0), (40, 64, 5, 1)]], n_rows=200, n_q=1, H=16))
+def _long_table_case(n_chunks=1500, n_q=1):
+    """One request whose table is too long to travel in the launch parameters (more than 1024
+    records), so the library copies it into the workspace."""
+    rng = np.random.default_rng(9)
+    reqs, p = [[(0, 32, 0, 0)]], 32
+    for k in range(n_chunks):
+        n = 1 + k % 5
+        reqs[0].append((int(rng.integers(0, 8000 - n)), n, p - int(rng.integers(-3000, 3000)), 1))
+        p += n
+    return to_device(synth.custom_case(reqs, n_rows=8000, n_q=n_q, H=16, q_std=1.0))
+
+
+@pytest.mark.parametrize("long_table", [False, True])
+def test_pageable_table_is_read_before_the_call_returns(oracle_mod, long_table):
+    """The library hands the validated host table to the kernels itself (in the launch
+    parameters when short, by a copy into the workspace when long).  A pageable table has
+    been read when the call returns, so overwriting it right after the call (before the GPU
+    has run anything) changes nothing: the kernels run on the table that was validated."""
+    if long_table:
+        case = _long_table_case()
+        ql, qr = case.q_lat[:, 0].contiguous(), case.q_rope[:, 0].contiguous()
+    else:
+        case = to_device(encode_rope_rows(synth.tiny_case(0, q_std=1.0), oracle_mod))
+        ql, qr = case.q_lat[:, -1].contiguous(), case.q_rope[:, -1].contiguous()
+    table = irm.ChunkTable(case.chunks, case.indptr, pinned=False)
+    ref, _, _ = irm.irm_mla_attn_decode(ql, qr, irm.ChunkTable(case.chunks, case.indptr), case.kv_rows, SCALE)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    block = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(side):
+        block.fill_(1)  # keeps the stream busy while the host table is overwritten
+        out, _, ws = irm.irm_mla_attn_decode(ql, qr, table, case.kv_rows, SCALE, stream=side)
+        table.chunks_host["pool_offset"][:] = 10_000_000
+        table.chunks_host["p_src"][:] = 7
+        table.indptr_host[:] = 0
+    torch.cuda.synchronize()
+    irm.device_status(ws)
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("long_table", [False, True])
+def test_graph_capture_of_the_table(oracle_mod, long_table):
+    """A call captured into a CUDA graph replays the table it validated at capture time.  A
+    short table travels in the launch parameters, so any host memory works; a long one is
+    copied into the workspace by a captured copy, which needs page-locked host memory (a
+    pageable one is refused during capture)."""
+    if long_table:
+        case = _long_table_case()
+        ql, qr = case.q_lat[:, 0].contiguous(), case.q_rope[:, 0].contiguous()
+    else:
+        case = to_device(encode_rope_rows(synth.tiny_case(0, q_std=1.0), oracle_mod))
+        ql, qr = case.q_lat[:, -1].contiguous(), case.q_rope[:, -1].contiguous()
+    pinned = irm.ChunkTable(case.chunks, case.indptr)
+    pageable = irm.ChunkTable(case.chunks, case.indptr, pinned=False)
+    ref, _, ws = irm.irm_mla_attn_decode(ql, qr, pinned, case.kv_rows, SCALE)
+    out = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    for table, ok in ((pinned, True), (pageable, not long_table)):
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        if not ok:
+            with pytest.raises(irm.IrmError) as e:
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        irm.irm_mla_attn_decode(ql, qr, table, case.kv_rows, SCALE, out=out,
+                                                workspace=ws, stream=side)
+            assert e.value.status == -1 and "page-locked" in str(e.value)
+            torch.cuda.synchronize()
+            continue
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                irm.irm_mla_attn_decode(ql, qr, table, case.kv_rows, SCALE, out=out, workspace=ws,
+                                        stream=side)
+        for _ in range(2):
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref)
+        irm.device_status(ws)
+
+
+def test_long_table_decode_and_prefill(oracle_mod):
+    """Tables copied into the workspace (more records than the launch parameters carry) give
+    the same results as the oracle, for decode and for prefill."""
+    case = _long_table_case()
+    sel = np.array([[0, 0, h] for h in range(16)])
+    _check_attn(case, oracle_mod, prefill=False, select=sel, what="decode, 1501-chunk table")
+    pcase = _long_table_case(n_q=9)
+    sel = np.array([[0, i, h] for i in (0, 4, 8) for h in (0, 7, 15)])
+    _check_attn(pcase, oracle_mod, prefill=True, select=sel, what="prefill, 1501-chunk table")
+
+
+def test_bad_page_index_is_recorded_not_faulted(oracle_mod):
+    """Page indices live in device memory and are not seen by the host: one outside the paged
+    output is caught by the gather kernel (the rows of that page are skipped, the status word
+    records IRM_ERR_DEVICE_BOUNDS) while every other page is still written."""
+    case = encode_rope_rows(synth.tiny_case(0), oracle_mod)
+    case = to_device(case)
     table = irm.ChunkTable(case.chunks, case.indptr)
-    bad = case.chunks.copy()
-    bad["pool_offset"][1] = 10_000_000
-    table.chunks_dev.copy_(torch.from_numpy(bad.view(np.uint8).copy()).cuda())
-    out, _, ws = irm.irm_mla_attn_decode(case.q_lat[:, 0], case.q_rope[:, 0], table, case.kv_rows)
+    pt_np = np.arange(8, dtype=np.int32)[None].copy()
+    pt_np[0, 3] = 8  # rows 192..255 would land past the 8 pages
+    paged = torch.zeros((8, 64, 576), dtype=torch.bfloat16, device="cuda")
+    ws = irm.irm_assemble_kv(table, case.kv_rows, paged, torch.from_numpy(pt_np).cuda())
     with pytest.raises(irm.IrmError) as e:
         irm.device_status(ws)
     assert e.value.status == -7
     irm.device_status(ws)  # cleared
+    got = synth.bits(paged.view(-1, 576))
+    pl = oracle_mod.plan(case.chunks, case.indptr)
+    src = synth.bits(case.kv_rows)[pl["src_row"]]
+    keep = np.ones(512, bool)
+    keep[192:256] = False
+    assert np.array_equal(got[np.arange(512)[keep], :512], src[keep, :512])
+    assert not got[192:256].any()

@@ -161,8 +161,7 @@ def test_plain_entry_points_equal_the_default_variant(oracle_mod):
     out = torch.empty_like(ref)
     ws = irm.new_workspace(irm.decode_workspace_size(table, 16))
     st = L.irm_mla_attn_decode(ql.data_ptr(), qr.data_ptr(), 1, 16, table.chunks_host.ctypes.data,
-                               table.indptr_host.ctypes.data, table.chunks_dev.data_ptr(),
-                               table.indptr_dev.data_ptr(), case.kv_rows.data_ptr(), case.kv_rows.shape[0],
+                               table.indptr_host.ctypes.data, case.kv_rows.data_ptr(), case.kv_rows.shape[0],
                                ctypes.c_float(SCALE), out.data_ptr(), None, ws.data_ptr(), ws.numel(),
                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0
@@ -170,10 +169,9 @@ def test_plain_entry_points_equal_the_default_variant(oracle_mod):
     assert torch.equal(out, ref)
     pref, _, _ = irm.irm_mla_attn_prefill(case.q_lat, case.q_rope, table, case.kv_rows, SCALE)
     out2 = torch.empty_like(pref)
-    ws2 = irm.new_workspace(irm.prefill_workspace_size(1, 16, 16))
+    ws2 = irm.new_workspace(irm.prefill_workspace_size(table, 16, 16))
     st = L.irm_mla_attn_prefill(case.q_lat.data_ptr(), case.q_rope.data_ptr(), 1, 16, 16,
                                 table.chunks_host.ctypes.data, table.indptr_host.ctypes.data,
-                                table.chunks_dev.data_ptr(), table.indptr_dev.data_ptr(),
                                 case.kv_rows.data_ptr(), case.kv_rows.shape[0], ctypes.c_float(SCALE),
                                 out2.data_ptr(), None, ws2.data_ptr(), ws2.numel(),
                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))

@@ -89,10 +89,47 @@ def test_null_and_error_paths_return_codes(irm):
     assert L.irm_validate_chunks(None, None, 1, 10, None) == -1
     assert L.irm_device_status(None, None) == -1
     n = ctypes.c_size_t(0)
-    assert L.irm_assemble_kv_workspace_size(0, ctypes.byref(n)) == -1
-    assert L.irm_assemble_kv_workspace_size(3, ctypes.byref(n)) == 0 and n.value >= 256 + 32
-    assert L.irm_mla_attn_prefill_workspace_size(1, 1, 129, ctypes.byref(n)) == -1
+    chunks, indptr = synth.make_table([[(0, 32, 0, 0)], [(40, 5, 0, 0)], [(60, 7, 0, 0)]])
+    assert L.irm_assemble_kv_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 0, ctypes.byref(n)) == -1
+    assert L.irm_assemble_kv_workspace_size(None, None, 3, ctypes.byref(n)) == -1
+    assert L.irm_assemble_kv_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 3, ctypes.byref(n)) == 0
+    assert n.value >= 256 + 16 + 3 * 24 + 32
+    assert L.irm_mla_attn_prefill_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 1, 1, 129,
+                                                 ctypes.byref(n)) == -4
     assert L.irm_status_string(-3).decode().startswith("reused chunk")
+
+
+def test_workspace_holds_the_copied_table(irm):
+    """Every workspace size counts the table area the library copies the validated table
+    into (status header, indptr padded to 8 bytes, 24-byte records, rounded to 256 bytes), so
+    it grows with the number of chunks."""
+    L = irm.lib()
+    n = ctypes.c_size_t(0)
+    sizes = {}
+    for k in (1, 9, 10, 100):
+        reqs = [[(0, 32, 0, 0)] + [(100 + 10 * i, 10, 7, 1) for i in range(k)]]
+        chunks, indptr = synth.make_table(reqs)
+        assert L.irm_assemble_kv_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 1, ctypes.byref(n)) == 0
+        asm = n.value
+        assert L.irm_mla_attn_prefill_workspace_size(chunks.ctypes.data, indptr.ctypes.data, 1, 4, 16,
+                                                     ctypes.byref(n)) == 0
+        sizes[k] = (asm, n.value)
+        tab = -(-(8 + 24 * (k + 1)) // 256) * 256
+        assert n.value == 256 + tab                       # prefill: header + table
+        assert asm == 256 + tab + 256                     # rotate+gather: + row starts [B+1] int64
+    assert sizes[1] == sizes[9] and sizes[10][0] > sizes[9][0] and sizes[100][1] > sizes[10][1]
+
+
+def test_chunk_table_block_layout(irm):
+    """The binding's ChunkTable keeps indptr and the records in one block laid out as the
+    workspace's table area (records at the next 8-byte boundary after indptr), which lets the
+    library copy a page-locked table with one transfer."""
+    chunks, indptr = synth.make_table([[(0, 32, 0, 0), (100, 50, 7, 1)], [(500, 3, 0, 0)]])
+    t = irm.ChunkTable(chunks, indptr, pinned=False)
+    base = t.indptr_host.ctypes.data
+    assert t.chunks_host.ctypes.data - base == 16 and t.chunks_host.ctypes.data % 8 == 0
+    assert list(t.indptr_host) == [0, 2, 3] and t.chunks_host.tobytes() == chunks.tobytes()
+    assert list(t.validate(1000)) == [82, 3]
 
 
 def test_attention_rejects_before_launch(irm):
@@ -102,7 +139,7 @@ def test_attention_rejects_before_launch(irm):
     chunks, indptr = synth.make_table([[(0, 32, 0, 0), (100, 50, 7, 1)]])
     fake = ctypes.c_void_p(1 << 20)
     ws = ctypes.c_void_p(1 << 21)
-    args = lambda H, ws_bytes: (fake, fake, 1, H, chunks.ctypes.data, indptr.ctypes.data, fake, fake,
+    args = lambda H, ws_bytes: (fake, fake, 1, H, chunks.ctypes.data, indptr.ctypes.data,
                                 fake, 1000, ctypes.c_float(0.07), fake, None, ws, ws_bytes, None)
     assert L.irm_mla_attn_decode(*args(0, 1 << 20)) == -4
     assert L.irm_mla_attn_decode(*args(200, 1 << 20)) == -4
@@ -112,13 +149,17 @@ def test_attention_rejects_before_launch(irm):
     assert L.irm_mla_attn_decode(*args(16, n.value - 1)) == -8
     # n_q larger than the context
     assert L.irm_mla_attn_prefill(fake, fake, 1, 83, 16, chunks.ctypes.data, indptr.ctypes.data,
-                                  fake, fake, fake, 1000, ctypes.c_float(0.07), fake, None, ws,
+                                  fake, 1000, ctypes.c_float(0.07), fake, None, ws,
                                   1 << 20, None) == -1
     # misaligned q pointer
     bad = ctypes.c_void_p((1 << 20) + 2)
     assert L.irm_mla_attn_prefill(bad, fake, 1, 1, 16, chunks.ctypes.data, indptr.ctypes.data,
-                                  fake, fake, fake, 1000, ctypes.c_float(0.07), fake, None, ws,
+                                  fake, 1000, ctypes.c_float(0.07), fake, None, ws,
                                   1 << 20, None) == -1
+    # a workspace too small for the copied table is refused before the copy
+    assert L.irm_mla_attn_prefill(fake, fake, 1, 1, 16, chunks.ctypes.data, indptr.ctypes.data,
+                                  fake, 1000, ctypes.c_float(0.07), fake, None, ws,
+                                  256, None) == -8
 
 
 def test_chunk_struct_layout_matches_header(irm):
@@ -151,14 +192,14 @@ def test_rope_entry_points_reject_bad_specs(irm, bad):
     chunks, indptr = synth.make_table([[(0, 32, 0, 0), (100, 50, 7, 1)]])
     L = irm.lib()
     rp = ctypes.cast(ctypes.pointer(r), ctypes.c_void_p)
-    st = L.irm_assemble_kv_rope(chunks.ctypes.data, indptr.ctypes.data, 1, None, None, None, 1000,
+    st = L.irm_assemble_kv_rope(chunks.ctypes.data, indptr.ctypes.data, 1, None, 1000,
                                 None, 0, None, 0, None, None, None, rp, None, 0, None)
     assert st == -1, L.irm_last_error()
-    st = L.irm_mla_attn_decode_rope(None, None, 1, 16, chunks.ctypes.data, indptr.ctypes.data, None,
-                                    None, None, 1000, 0.1, None, None, rp, None, 0, None)
+    st = L.irm_mla_attn_decode_rope(None, None, 1, 16, chunks.ctypes.data, indptr.ctypes.data,
+                                    None, 1000, 0.1, None, None, rp, None, 0, None)
     assert st == -1
     st = L.irm_mla_attn_prefill_rope(None, None, 1, 4, 16, chunks.ctypes.data, indptr.ctypes.data,
-                                     None, None, None, 1000, 0.1, None, None, rp, None, 0, None)
+                                     None, 1000, 0.1, None, None, rp, None, 0, None)
     assert st == -1
     assert "rope" in L.irm_last_error().decode()
 
