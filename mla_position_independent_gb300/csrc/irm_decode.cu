@@ -259,23 +259,37 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     tmem_alloc(sb + kOffTmemPtr, tmem_cols(H));
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
 
-  if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-    // ======================= loaders: row gather with cp.async =========================
-    const int tp = tid - kSoftmaxThreads;
-    const int pw = warp - kSoftmaxWarps;
-    const int chk = tp & 7;    // 16-byte chunk of a 128-byte slab row
-    const int rsub = tp >> 3;  // row within a pass
-    const __nv_bfloat16* ql = static_cast<const __nv_bfloat16*>(a.q_lat);
-    const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
-    const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
-
-    // Q (H rows, all 576 columns, slab-major); it lands with the first units (same arrives)
+  // ---- start-up work that needs no mbarrier: while the barriers and TMEM are being set up,
+  //      the row-map warp builds tile 0's map and the loaders issue the copies of Q and of
+  //      tile 0 (their landing is signalled after the block-wide barrier) ------------------
+  const bool is_loader = warp >= kSoftmaxWarps && warp < kMmaWarp;
+  const int tp = tid - kSoftmaxThreads;
+  const int chk = tp & 7;    // loaders: 16-byte chunk of a 128-byte slab row
+  const int rsub = tp >> 3;  // loaders: row within a pass
+  const __nv_bfloat16* kvp = static_cast<const __nv_bfloat16*>(a.kv);
+  ChunkWindow cw;
+  cw.chunks = chunks;
+  cw.c_end = c_end;
+  cw.win = c_begin;
+  if (warp == kMapWarp) {
     if (ntiles > 0) {
+      if (c_first >= 0) {
+        cw.win = c_first;  // the chunk holding the split's first row (launch hint)
+        cw.load(lane);
+      } else {
+        cw.seek(c_begin, kb * kBN, lane);
+      }
+      cw.build_map(kb * kBN, ctx, a.n_rows, map_src, map_delta, a.status, lane);
+    }
+    __syncwarp();
+    named_bar_arrive(2, kLoaderThreads + 32);  // tile 0's map is in slot 0
+  } else if (is_loader) {
+    named_bar_sync(2, kLoaderThreads + 32);
+    if (ntiles > 0) {
+      const __nv_bfloat16* ql = static_cast<const __nv_bfloat16*>(a.q_lat);
+      const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope);
+      // Q (H rows, all 576 columns, slab-major); it lands with tile 0 (same arrives)
       for (int h = rsub; h < H; h += kRowsPerPass) {
         const int64_t row = (int64_t)b * H + h;
         for (int slab = 0; slab < 9; ++slab) {
@@ -284,6 +298,42 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
           cp_async_16(sb + L.q + (uint32_t)slab * H * 128u + sw128_offset(h, chk), src, 16u);
         }
       }
+      // tile 0 into k_r slot 0 and ring units 0-3 (all free at start)
+      const __nv_bfloat16* rowp[kLoadPasses];
+      uint32_t nb[kLoadPasses];
+#pragma unroll
+      for (int i = 0; i < kLoadPasses; ++i) {
+        const int sr = map_src[kRowsPerPass * i + rsub];
+        rowp[i] = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + chk * 8;
+        nb[i] = sr >= 0 ? 16u : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kLoadPasses; ++i)
+        cp_async_16(sb + L.kr + sw128_offset(kRowsPerPass * i + rsub, chk), rowp[i] + 8 * 64, nb[i]);
+      for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t ub = sb + L.ring + (uint32_t)pr * kPairBytes;
+#pragma unroll
+        for (int i = 0; i < kLoadPasses; ++i) {
+          const uint32_t r = (uint32_t)(kRowsPerPass * i + rsub);
+          cp_async_16(ub + pair_offset(r, 0u, (uint32_t)chk), rowp[i] + (2 * pr) * 64, nb[i]);
+          cp_async_16(ub + pair_offset(r, 1u, (uint32_t)chk), rowp[i] + (2 * pr + 1) * 64, nb[i]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
+
+  if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
+    // ======================= loaders: row gather with cp.async =========================
+    const int pw = warp - kSoftmaxWarps;
+    // tile 0 (and Q) went out before the block-wide barrier: signal its landing now (each
+    // arrive fires once all of this thread's earlier copies have landed)
+    if (ntiles > 0) {
+      cp_async_arrive_noinc(bar(BAR_KR_LANDED + 0));
+      for (int pr = 0; pr < 4; ++pr) cp_async_arrive_noinc(bar(BAR_PAIR_FULL + pr));
     }
 
     // k_r rotation, in tile order: this warp's 8 rows of every slot whose bytes have landed
@@ -322,7 +372,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     };
 
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
+    for (int j = 1; j < ntiles && ok; ++j) {
       const int ks = j % kKrSlots;
       const uint32_t kph = (uint32_t)(j / kKrSlots) & 1u;
       // k_r slot ks and its row map are free once the S^T of tile j - kKrSlots is done
@@ -369,20 +419,10 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     }
   } else if (warp == kMapWarp) {
     // ======================= row maps: tile t into slot t % 3 once tile t-3's S^T is done ======
-    ChunkWindow cw;
-    cw.chunks = chunks;
-    cw.c_end = c_end;
-    cw.win = c_begin;
+    // (tile 0's map was built before the block-wide barrier; its arrive keeps the phases)
     bool ok = true;
-    if (ntiles > 0) {
-      if (c_first >= 0) {
-        cw.win = c_first;  // the chunk holding the split's first row (launch hint)
-        cw.load(lane);
-      } else {
-        cw.seek(c_begin, kb * kBN, lane);
-      }
-    }
-    for (int t = 0; t < ntiles && ok; ++t) {
+    if (ntiles > 0 && lane == 0) mbar_arrive(bar(BAR_MAP + 0));
+    for (int t = 1; t < ntiles && ok; ++t) {
       const int ks = t % kKrSlots;
       if (t >= kKrSlots &&
           !(ok = warp_wait(bar(BAR_KR_EMPTY + ks), ((uint32_t)(t / kKrSlots) & 1u) ^ 1u, abort_flag)))

@@ -137,6 +137,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrives on a named barrier without waiting (the waiting side uses named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Named barrier over `nthreads` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
   uint32_t r;
