@@ -16,6 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libirm.so")
+TIMELINE_OUT = os.path.join(PKG, "libirm_timeline.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,24 +38,30 @@ def _inputs():
     return srcs, deps
 
 
-def needs_build() -> bool:
-    if not os.path.exists(OUT):
+def needs_build(out: str = OUT) -> bool:
+    if not os.path.exists(out):
         return True
     _, deps = _inputs()
-    t = os.path.getmtime(OUT)
+    t = os.path.getmtime(out)
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not needs_build():
-        return OUT
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    """Builds libirm.so; with timeline=True, libirm_timeline.so instead: the same library with
+    the decode kernel's phase stamps compiled in (for measuring where a decode's time goes;
+    never loaded by the product path)."""
+    out = TIMELINE_OUT if timeline else OUT
+    if not force and not needs_build(out):
+        return out
     nvcc = _nvcc()
     srcs, _ = _inputs()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    bdir = BUILD_DIR + ("_timeline" if timeline else "")
+    os.makedirs(bdir, exist_ok=True)
+    flags = NVCC_FLAGS + (["-DIRM_TIMELINE"] if timeline else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -64,13 +71,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = OUT + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

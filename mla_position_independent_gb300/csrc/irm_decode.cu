@@ -50,6 +50,34 @@
 #include "irm_pipeline.cuh"
 
 namespace irm {
+
+// Timeline instrumentation, compiled only into the separately built timeline library
+// (build.build(timeline=True) defines IRM_TIMELINE): the CTAs of request 0 stamp %globaltimer
+// at the phases of a decode (kernel entry, set-up, each tile's scores and P.V issued, pipeline
+// end, cluster merge, end) into a device array that irm_timeline_read() copies out.  The
+// product library contains none of it.
+#ifdef IRM_TIMELINE
+constexpr int kTlCtas = 64, kTlTiles = 64;
+enum : int { TL_ENTRY, TL_SETUP, TL_PIPE_END, TL_PARKED, TL_CLUSTER, TL_MERGED, TL_END, TL_N };
+__device__ unsigned long long g_tl_cta[kTlCtas][TL_N];
+__device__ unsigned long long g_tl_tile[kTlCtas][kTlTiles][3];  // data landed, S issued, P.V issued
+#define IRM_TL(ev)                                                                        \
+  do {                                                                                    \
+    if (blockIdx.y == 0 && blockIdx.x < kTlCtas) g_tl_cta[blockIdx.x][(ev)] = globaltimer_ns(); \
+  } while (0)
+#define IRM_TL_TILE(j, k)                                                                           \
+  do {                                                                                              \
+    if (blockIdx.y == 0 && blockIdx.x < kTlCtas && (j) < kTlTiles) g_tl_tile[blockIdx.x][(j)][(k)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define IRM_TL(ev) \
+  do {             \
+  } while (0)
+#define IRM_TL_TILE(j, k) \
+  do {                    \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kBN = 64;                         // KV rows per tile
@@ -180,6 +208,7 @@ __device__ __forceinline__ void merge_batch(const float (&mq)[8], const float (&
 template <int H>
 __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
   using R = Roles<H>;
+  if (threadIdx.x == 0) IRM_TL(TL_ENTRY);
   constexpr int kLoaderWarps = R::kLoaderWarps, kMmaWarp = R::kMmaWarp, kPvWarp = R::kPvWarp,
                 kMapWarp = R::kMapWarp;
   constexpr int kThreads = R::kThreads, kLoaderThreads = R::kLoaderThreads;
@@ -325,6 +354,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
+  if (threadIdx.x == 0) IRM_TL(TL_SETUP);
 
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ======================= loaders: row gather with cp.async =========================
@@ -462,6 +492,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         }
         if (!ok) break;
         const int ks = ns % kKrSlots;
+        IRM_TL_TILE(ns, 0);
         if (!(ok = mbar_wait(bar(BAR_KR_FULL + ks), (uint32_t)(ns / kKrSlots) & 1u, abort_flag))) break;
         // rotated rows (generic-proxy writes of the loaders) -> async proxy
         tc_fence_after();
@@ -475,6 +506,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         }
         umma_commit(bar(BAR_KR_EMPTY + ks));
         umma_commit(bar(BAR_S_FULL + (ns & 1)));
+        IRM_TL_TILE(ns, 1);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -508,6 +540,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
           umma_commit(bar(BAR_PAIR_EMPTY + (4 * np + blk) % L.units));
         }
         umma_commit(bar(BAR_PV_DONE + (np & 1)));
+        IRM_TL_TILE(np, 2);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -677,6 +710,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
 
   // ---- park this split's unnormalised O^T [H][512] (fp32) in the drained KV stages ------
   __syncthreads();
+  if (threadIdx.x == 0) IRM_TL(TL_PIPE_END);
   const bool cta_ok = *abort_flag == 0 && ntiles > 0;
   float* opart = reinterpret_cast<float*>(smem + L.ring);
   if (warp < kSoftmaxWarps) {
@@ -702,8 +736,10 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) IRM_TL(TL_PARKED);
   cluster_arrive();  // every split of the request has parked its partial
   cluster_wait();
+  if (threadIdx.x == 0) IRM_TL(TL_CLUSTER);
 
   // ---- merge the C splits of this cluster through distributed shared memory: CTA crank
   //      takes items [crank * per, (crank + 1) * per) of the H x 128 (head, 4-column group)
@@ -752,6 +788,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       if (c4 == 0 || it == 0) a.glse[((int64_t)b * G + g) * H + h] = lse2;
     }
   }
+  if (threadIdx.x == 0) IRM_TL(TL_MERGED);
   if (G > 1) {
     // the last of the G clusters to finish slice crank merges it (threadfence reduction; the
     // counter resets itself so the workspace stays reusable)
@@ -802,6 +839,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       }
     }
   }
+  if (threadIdx.x == 0) IRM_TL(TL_END);
   cluster_arrive();  // peers are done reading this CTA's shared memory
   cluster_wait();
   if (warp == kMmaWarp) {
@@ -878,6 +916,18 @@ int decode_max_active_clusters(int H, int C) {
   if (C < 1 || C > kMaxDecodeCluster) return 0;
   return H == 16 ? max_clusters_h<16>(C) : H == 32 ? max_clusters_h<32>(C) : 0;
 }
+
+#ifdef IRM_TIMELINE
+// Timeline build only: copies out (and clears) the stamps of the last decode.
+extern "C" int irm_timeline_read(unsigned long long* cta, unsigned long long* tile) {
+  cudaError_t e = cudaMemcpyFromSymbol(cta, g_tl_cta, sizeof(g_tl_cta));
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(tile, g_tl_tile, sizeof(g_tl_tile));
+  static unsigned long long zero[kTlCtas * kTlTiles * 3];
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tl_cta, zero, sizeof(g_tl_cta));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tl_tile, zero, sizeof(g_tl_tile));
+  return (int)e;
+}
+#endif
 
 cudaError_t launch_mla_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.C < 1 || a.C > kMaxDecodeCluster || (a.C & (a.C - 1)) != 0 || a.G < 1 ||
