@@ -205,6 +205,48 @@ __device__ __forceinline__ void merge_batch(const float (&mq)[8], const float (&
   M = Mn;
 }
 
+// The same for 8 columns (two float4 per partial).
+__device__ __forceinline__ void merge_batch2(const float (&mq)[8], const float (&lq)[8], const float4 (&va)[8],
+                                             const float4 (&vb)[8], float& M, float& den, float4& acc_a,
+                                             float4& acc_b) {
+  float Mn = M;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mq[k]);
+  if (Mn == -INFINITY) return;
+  const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+  den *= sc;
+  acc_a = make_float4(acc_a.x * sc, acc_a.y * sc, acc_a.z * sc, acc_a.w * sc);
+  acc_b = make_float4(acc_b.x * sc, acc_b.y * sc, acc_b.z * sc, acc_b.w * sc);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float w = (mq[k] == -INFINITY) ? 0.f : fast_exp2(mq[k] - Mn);
+    den += w * lq[k];
+    acc_a.x += w * va[k].x;
+    acc_a.y += w * va[k].y;
+    acc_a.z += w * va[k].z;
+    acc_a.w += w * va[k].w;
+    acc_b.x += w * vb[k].x;
+    acc_b.y += w * vb[k].y;
+    acc_b.z += w * vb[k].z;
+    acc_b.w += w * vb[k].w;
+  }
+  M = Mn;
+}
+
+// 8 fp32 values scaled by `inv`, rounded to bf16 (one 16-byte word).
+__device__ __forceinline__ uint4 pack_bf16x8(float4 a, float4 b, float inv) {
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x * inv, b.y * inv);
+  const __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z * inv, b.w * inv);
+  uint4 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&h0);
+  w.y = *reinterpret_cast<const uint32_t*>(&h1);
+  w.z = *reinterpret_cast<const uint32_t*>(&h2);
+  w.w = *reinterpret_cast<const uint32_t*>(&h3);
+  return w;
+}
+
 template <int H>
 __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
   using R = Roles<H>;
@@ -742,50 +784,49 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   if (threadIdx.x == 0) IRM_TL(TL_CLUSTER);
 
   // ---- merge the C splits of this cluster through distributed shared memory: CTA crank
-  //      takes items [crank * per, (crank + 1) * per) of the H x 128 (head, 4-column group)
-  //      items ---------------------------------------------------------------------------
-  const int per = H * 128 / C;
+  //      takes items [crank * per, (crank + 1) * per) of the H x 64 (head, 8-column group)
+  //      items (at most one per thread for 16 heads and C >= 4) --------------------------------
+  const int per = H * 64 / C;
   float4* gpart = reinterpret_cast<float4*>(a.gpart);
   for (int it = tid; it < per; it += kThreads) {
     const int item = crank * per + it;
-    const int h = item >> 7, c4 = item & 127;
+    const int h = item >> 6, c8 = item & 63;
     // online merge over the splits, 8 at a time: every remote load of a batch is issued before
     // any is used, so a batch costs one round trip through the cluster
     float M = -INFINITY, den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc_a = make_float4(0.f, 0.f, 0.f, 0.f), acc_b = acc_a;
     for (int q0 = 0; q0 < C; q0 += 8) {
       float mq[8], lq[8];
-      float4 vq[8];
+      float4 va[8], vb[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (q0 + k < C) {
           const uint32_t base = mapa_shared(sb, (uint32_t)(q0 + k));
+          const uint32_t vaddr = base + L.ring + (uint32_t)(h * kDLat + 8 * c8) * 4u;
           mq[k] = ld_cluster_f32(base + kOffML + 4u * h);
           lq[k] = ld_cluster_f32(base + kOffML + 128u + 4u * h);
-          vq[k] = ld_cluster_v4(base + L.ring + (uint32_t)(h * kDLat + 4 * c4) * 4u);
+          va[k] = ld_cluster_v4(vaddr);
+          vb[k] = ld_cluster_v4(vaddr + 16u);
         } else {
           mq[k] = -INFINITY;
           lq[k] = 0.f;
-          vq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          va[k] = vb[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      merge_batch(mq, lq, vq, M, den, acc);
+      merge_batch2(mq, lq, va, vb, M, den, acc_a, acc_b);
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     const float lse2 = den > 0.f ? M + __log2f(den) : -INFINITY;  // log2 units
     const int64_t orow = (int64_t)b * H + h;
     if (G == 1) {
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 w2;
-      w2.x = *reinterpret_cast<const uint32_t*>(&h0);
-      w2.y = *reinterpret_cast<const uint32_t*>(&h1);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + 4 * c4) = w2;
-      if (c4 == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + 8 * c8) =
+          pack_bf16x8(acc_a, acc_b, inv);
+      if (c8 == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
     } else {
-      gpart[((int64_t)b * G + g) * (H * 128) + item] = acc;
-      if (c4 == 0 || it == 0) a.glse[((int64_t)b * G + g) * H + h] = lse2;
+      float4* dst = gpart + ((int64_t)b * G + g) * (H * 128) + 2 * item;
+      dst[0] = make_float4(acc_a.x * inv, acc_a.y * inv, acc_a.z * inv, acc_a.w * inv);
+      dst[1] = make_float4(acc_b.x * inv, acc_b.y * inv, acc_b.z * inv, acc_b.w * inv);
+      if (c8 == 0) a.glse[((int64_t)b * G + g) * H + h] = lse2;
     }
   }
   if (threadIdx.x == 0) IRM_TL(TL_MERGED);
@@ -806,36 +847,34 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       __threadfence();
       for (int it = tid; it < per; it += kThreads) {
         const int item = crank * per + it;
-        const int h = item >> 7, c4 = item & 127;
+        const int h = item >> 6, c8 = item & 63;
         const float* gl = a.glse + (int64_t)b * G * H + h;
         float M = -INFINITY, den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc_a = make_float4(0.f, 0.f, 0.f, 0.f), acc_b = acc_a;
         for (int q0 = 0; q0 < G; q0 += 8) {
           float mq[8], lq[8];
-          float4 vq[8];
+          float4 va[8], vb[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             if (q0 + k < G) {
+              const float4* src = gpart + ((int64_t)b * G + q0 + k) * (H * 128) + 2 * item;
               mq[k] = __ldcg(gl + (int64_t)(q0 + k) * H);  // log2-sum-exp of a normalised partial
               lq[k] = 1.f;
-              vq[k] = __ldcg(gpart + ((int64_t)b * G + q0 + k) * (H * 128) + item);
+              va[k] = __ldcg(src);
+              vb[k] = __ldcg(src + 1);
             } else {
               mq[k] = -INFINITY;
               lq[k] = 0.f;
-              vq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+              va[k] = vb[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
-          merge_batch(mq, lq, vq, M, den, acc);
+          merge_batch2(mq, lq, va, vb, M, den, acc_a, acc_b);
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
         const int64_t orow = (int64_t)b * H + h;
-        const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-        const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-        uint2 w2;
-        w2.x = *reinterpret_cast<const uint32_t*>(&h0);
-        w2.y = *reinterpret_cast<const uint32_t*>(&h1);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + 4 * c4) = w2;
-        if (c4 == 0 && a.lse != nullptr) a.lse[orow] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDLat + 8 * c8) =
+            pack_bf16x8(acc_a, acc_b, inv);
+        if (c8 == 0 && a.lse != nullptr) a.lse[orow] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
       }
     }
   }
