@@ -8,21 +8,20 @@
 //   a chunk from s ends at the first candidate i >= s + min_len - 1, else at s + max_len - 1,
 //   else at the stream's end.
 //
-// Passes:
-//   1. cdc_hash_kernel (grid-wide): a warp takes runs of 128-position steps of one stream,
-//      4 positions per lane, and forms all hashes with one 4-step shuffle scan per step (see
-//      the kernel); the candidate tests become bitmask words by shuffle-OR of lane nibbles.
-//   2. The chunk boundaries depend on where the previous chunk started, so they are resolved
-//      from the bitmask in order, one ballot per chunk (next_end: the words covering
-//      [start + min_len - 1, start + max_len - 1] masked, then a find-first-set).  To use the
-//      whole GPU on long streams the walk is speculative: cdc_spec_kernel walks every
-//      4096-token segment with its own warp (its bitmask words staged in shared memory) as if a chunk started at the segment start, and
-//      records its chunk ends; cdc_fixup_kernel (one warp per stream) then follows the true
-//      chain: entering a segment at its true start, it re-walks only until it reaches one of
-//      the segment's speculative ends (from then on both walks agree, usually after one or
-//      two chunks) and copies the rest.
-//   3. cdc_fingerprint_kernel: four lanes per chunk (one per xxHash64 accumulator), xxHash64
-//      of its token ids as little-endian int32 bytes.
+// Passes (two kernels):
+//   1. cdc_segment_kernel, one CTA per 4096-token segment of a stream: the CTA hashes the
+//      segment and the max_len - 1 positions after it (a chunk starting in the segment ends
+//      there at the latest) into a candidate bitmask in shared memory (its own words also go
+//      to global memory), walks the chunks speculatively from the segment start (one ballot
+//      per chunk: next_end) and fingerprints those chunks while their tokens are hot.
+//   2. cdc_resolve_kernel, one CTA per stream.  A walk entering a segment anywhere meets the
+//      segment's speculative chain within a chunk or two, after which both agree; the segment
+//      then exits where its speculative walk does.  So each warp takes one segment, enters it
+//      at the previous segment's speculative exit, re-walks until it meets the speculative
+//      chain, and counts its chunks; a prefix over the counts places every segment's chunks
+//      (the re-walked ones fingerprinted now, the speculative ones copied with their
+//      fingerprints).  A segment whose re-walk does not meet its chain (possible only with
+//      very long chunks) makes the rest of the stream follow the exact chain in order.
 // Token ids outside the Gear table are read as G = 0 and recorded in the status word.
 #include <cuda_runtime.h>
 #include <climits>
@@ -34,7 +33,8 @@ namespace irm {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kHashWarps = 8;          // warps per block of the hash pass
+constexpr int kSegThreads = 128;      // threads per CTA of the segment pass (4 warps, a segment each)
+constexpr int kResWarps = 16;         // warps per CTA of the resolve pass (segments at a time)
 
 // Gear word of token t from SplitMix64 (Steele, Lea, Flood 2014): the generator's (t+1)-th
 // output for the seed, its state seed + (t + 1) * gamma passed through the output mix.
@@ -50,7 +50,6 @@ __device__ __forceinline__ bool cdc_candidate(uint64_t h, int bits, int mode) {
 }
 
 constexpr int kSeg = 4096;                           // tokens per speculative walk segment
-constexpr int kWinWords = (kSeg + 1024) / 32;         // bitmask words a walk keeps in shared memory
 
 // Prefix sums over streams (two blocks): slot_base[s] = sum_{s' < s} (len_s' / min_len + 1)
 // (output slots) and seg_base[s] = sum_{s' < s} ceil(len_s' / kSeg) (speculative segments).
@@ -95,69 +94,6 @@ __global__ void __launch_bounds__(1024) cdc_base_kernel(const int64_t* __restric
   if (threadIdx.x == 0) base[S] = carry;
 }
 
-// A warp takes a run of kRunSteps steps of 128 positions of one stream, lane l holding the
-// 4 consecutive positions 4l .. 4l+3 of a step.  With g0..g3 their Gear words, the lane's block
-// contributes L = 8 g0 + 4 g1 + 2 g2 + g3 to the hash at its last position, and a 4-step
-// shuffle scan X_l = sum_{j <= l} L_j 2^(4 (l - j)) gives the hash there:
-// h(4l+3) = h_prev 2^(4l+4) + X_l (terms shifted by 64 or more vanish).  The lane then steps
-// h = 2 h + g through its own 4 positions from h(4l-1).  The step before the run (its 128
-// positions include the 64 the run's first hash depends on) is hashed the same way, first.
-constexpr int kRunSteps = 4;
-__device__ __forceinline__ uint64_t gear_word(const CdcArgs& a, int32_t x, int* bad) {
-  if (x < 0 || x >= a.vocab) {
-    *bad = 1;
-    return 0;
-  }
-  return a.gear != nullptr ? __ldg(a.gear + x) : splitmix_word(a.gear_seed, x);
-}
-
-__global__ void __launch_bounds__(32 * kHashWarps) cdc_hash_kernel(const CdcArgs a) {
-  const int s = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t off = a.offsets[s], len = a.offsets[s + 1] - off;
-  const int64_t nsteps = (len + 127) / 128;
-  const int64_t r0 = ((int64_t)blockIdx.x * kHashWarps + warp) * kRunSteps;
-  if (r0 >= nsteps) return;
-  const int32_t* tok = a.tokens + off;
-  uint32_t* words = a.words + (off >> 5) + s;  // word base of the stream (see the header)
-  const int64_t nwords = (len + 31) / 32;
-  int bad = 0;
-  uint64_t h_prev = 0;
-  const int64_t r1 = min(nsteps, r0 + kRunSteps);
-  for (int64_t r = (r0 > 0 ? r0 - 1 : 0); r < r1; ++r) {
-    const int64_t p = 128 * r + 4 * lane;  // the lane's first position
-    uint64_t g[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) g[e] = p + e < len ? gear_word(a, __ldg(tok + p + e), &bad) : 0ull;
-    uint64_t x = (g[0] << 3) + (g[1] << 2) + (g[2] << 1) + g[3];
-#pragma unroll
-    for (int d = 1; d < 16; d <<= 1) {  // shifts 4, 8, 16, 32 (the shift-64 step vanishes)
-      const uint64_t y = __shfl_up_sync(kFull, x, d);
-      if (lane >= d) x += y << (4 * d);
-    }
-    const uint64_t h_last = (lane < 15 ? (h_prev << (4 * lane + 4)) : 0ull) + x;
-    uint64_t h = __shfl_up_sync(kFull, h_last, 1);  // hash at position 4l - 1
-    if (lane == 0) h = h_prev;
-    uint32_t nib = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      h = (h << 1) + g[e];
-      if (p + e < len && cdc_candidate(h, a.bits, a.mode)) nib |= 1u << e;
-    }
-    // word j of the step collects the nibbles of lanes 8j .. 8j+7
-    uint32_t wv = nib << (4 * (lane & 7));
-    wv |= __shfl_xor_sync(kFull, wv, 1);
-    wv |= __shfl_xor_sync(kFull, wv, 2);
-    wv |= __shfl_xor_sync(kFull, wv, 4);
-    if (r >= r0 && (lane & 7) == 0) {
-      const int64_t w = 4 * r + (lane >> 3);
-      if (w < nwords) words[w] = wv;
-    }
-    h_prev = __shfl_sync(kFull, h_last, 31);
-  }
-  if (__any_sync(kFull, bad) && lane == 0) set_status(a.status, kDevErrBounds);
-}
-
 // Candidate bitmask of a stream as a warp reads it: words [win0, win0 + nwin) from a copy
 // in shared memory, the rest from global memory.
 struct WordSrc {
@@ -192,140 +128,6 @@ __device__ __forceinline__ int next_end(const WordSrc& words, int len, int t, in
     }
   }
   return last;
-}
-
-// Speculative walk of one segment: chunk ends from a chunk start at the segment start until
-// a chunk ends at or past the segment's last position.
-__global__ void __launch_bounds__(128) cdc_spec_kernel(const CdcArgs a, int64_t n_segs) {
-  __shared__ uint32_t win_sh[4][kWinWords];
-  const int64_t g = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (g >= n_segs) return;
-  int lo = 0, hi = a.S;  // stream owning segment g: last s with seg_base[s] <= g
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (a.seg_base[mid] <= g) lo = mid; else hi = mid;
-  }
-  const int s = lo;
-  const int64_t k = g - a.seg_base[s];
-  const int64_t off = a.offsets[s], len = a.offsets[s + 1] - off;
-  const int64_t seg_end = min(len, (k + 1) * kSeg);  // one past the segment
-  // the segment's bitmask words (and those a chunk crossing its end reads) to shared memory
-  uint32_t* win = win_sh[threadIdx.x >> 5];
-  const int64_t nwords = (len + 31) / 32, wbeg = k * kSeg / 32;
-  const int64_t nwin = min((int64_t)kWinWords, nwords - wbeg);
-  const uint32_t* gw = a.words + (off >> 5) + s;
-  for (int64_t r = lane; r < nwin; r += 32) win[r] = __ldg(gw + wbeg + r);
-  __syncwarp();
-  const WordSrc words{gw, win, wbeg, nwin};
-  int32_t* ends = a.spec_ends + g * a.spec_cap;
-  int64_t t = k * kSeg, c = 0;
-  while (t < seg_end && c < a.spec_cap) {
-    const int64_t e = next_end(words, len, t, a.min_len, a.max_len, lane);
-    if (lane == 0) ends[c] = (int32_t)e;
-    ++c;
-    t = e + 1;
-  }
-  if (lane == 0) a.spec_count[g] = (int32_t)c;
-}
-
-// The true chain of one stream: re-walk from the true start of each segment until a
-// speculative end of that segment is met, then take the segment's remaining ends.
-constexpr int kFixWin = 64;  // bitmask words the fix-up keeps for a segment's first 2048 positions
-__global__ void __launch_bounds__(128) cdc_fixup_kernel(const CdcArgs a) {
-  __shared__ uint32_t win_sh[4][kFixWin];
-  const int s = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (s >= a.S) return;
-  const int64_t off = a.offsets[s], len = a.offsets[s + 1] - off;
-  const uint32_t* gw = a.words + (off >> 5) + s;
-  uint32_t* win = win_sh[threadIdx.x >> 5];
-  const int64_t cb = a.base[s], gb = a.seg_base[s];
-  const int64_t nseg = (len + kSeg - 1) / kSeg;
-  const int64_t nwords = (len + 31) / 32;
-  // What segment k needs first (its speculative end count, first 32 ends and the bitmask of
-  // its first 2048 positions) is loaded one segment ahead, so those loads overlap the work
-  // on the segment before.
-  uint32_t pa = 0, pb = 0;
-  int32_t pend = INT_MAX;
-  int pcnt = 0;
-  auto prefetch = [&](int64_t k) {
-    if (k >= nseg) return;
-    const int64_t w0 = k * kSeg / 32;
-    pa = w0 + lane < nwords ? __ldg(gw + w0 + lane) : 0u;
-    pb = w0 + 32 + lane < nwords ? __ldg(gw + w0 + 32 + lane) : 0u;
-    pcnt = a.spec_count[gb + k];
-    pend = lane < a.spec_cap ? a.spec_ends[(gb + k) * a.spec_cap + lane] : INT_MAX;
-  };
-  prefetch(0);
-  int64_t t = 0, count = 0;
-  auto emit = [&](int64_t start, int64_t e) {
-    if (lane == 0) {
-      a.chunk_start[cb + count] = (int32_t)start;
-      a.chunk_len[cb + count] = (int32_t)(e - start + 1);
-    }
-    ++count;
-  };
-  for (int64_t k = 0; k < nseg && t < len; ++k) {
-    const int64_t seg_end = min(len, (k + 1) * kSeg);
-    const int nspec = pcnt;
-    const int32_t first = pend;
-    __syncwarp();
-    win[lane] = pa;
-    win[32 + lane] = pb;
-    __syncwarp();
-    prefetch(k + 1);
-    if (t >= seg_end) continue;  // a chunk longer than a segment covers this one
-    const int32_t* ends = a.spec_ends + (gb + k) * a.spec_cap;
-    const WordSrc words{gw, win, k * kSeg / 32, min((int64_t)kFixWin, nwords - k * kSeg / 32)};
-    // re-walk until a chunk ends where a speculative one does (the segment-start case
-    // agrees from its first chunk: both walks start at the same place)
-    int p = 0;  // first speculative end not below the last true end
-    bool met = false;
-    if (t == k * kSeg) {
-      met = true;
-      p = -1;
-    }
-    // the segment's speculative ends, 32 at a time in registers (lane i: ends[sb + i])
-    int sb = 0;
-    int32_t mine = lane < nspec ? first : INT_MAX;
-    while (!met && t < seg_end) {
-      const int64_t e = next_end(words, len, t, a.min_len, a.max_len, lane);
-      emit(t, e);
-      t = e + 1;
-      for (;;) {  // first speculative end >= e
-        const uint32_t ge = __ballot_sync(kFull, mine >= e);
-        if (ge != 0u) {
-          const int i = __ffs(ge) - 1;
-          p = sb + i;
-          met = __shfl_sync(kFull, mine, i) == e;
-          break;
-        }
-        sb += 32;
-        if (sb >= nspec) {
-          p = nspec;
-          break;
-        }
-        mine = sb + lane < nspec ? ends[sb + lane] : INT_MAX;
-      }
-    }
-    if (met) {
-      // speculative chunks after index p (all of them when p == -1) are the true ones
-      for (int i0 = p + 1; i0 < nspec; i0 += 32) {
-        const int i = i0 + lane;
-        if (i < nspec) {
-          const int64_t st = i == 0 ? k * kSeg : (int64_t)ends[i - 1] + 1;
-          a.chunk_start[cb + count + (i - (p + 1))] = (int32_t)st;
-          a.chunk_len[cb + count + (i - (p + 1))] = (int32_t)(ends[i] - st + 1);
-        }
-      }
-      if (nspec > p + 1) {
-        count += nspec - (p + 1);
-        t = (int64_t)ends[nspec - 1] + 1;
-      }
-    }
-  }
-  if (lane == 0) a.n_chunks[s] = (int32_t)count;
 }
 
 // xxHash64 (four 64-bit lanes over 32-byte stripes, lane merge, 8/4/1-byte tails, final
@@ -392,42 +194,342 @@ __device__ uint64_t chunk_xxh64_x4(const int32_t* __restrict__ t, int n, uint64_
   return h;
 }
 
-// Four lanes per chunk; blockIdx.y = stream, the x dimension walks its chunks.
-__global__ void __launch_bounds__(256) cdc_fingerprint_kernel(const CdcArgs a) {
-  const int s = blockIdx.y;
-  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2;
-  const int q = threadIdx.x & 3, lane = threadIdx.x & 31;
-  const uint32_t gmask = 0xfu << (lane & ~3);
-  // the 4 lanes of a chunk agree on the test (same c), so the group shuffles stay within it
-  if (a.chunk_hash == nullptr || c >= a.n_chunks[s]) return;
-  const int64_t t = a.base[s] + c;
-  const int32_t st = a.chunk_start[t], n = a.chunk_len[t];
-  const uint64_t h = chunk_xxh64_x4(a.tokens + a.offsets[s] + st, n, a.seed, q, gmask, lane & ~3);
-  if (q == 0) a.chunk_hash[t] = h;
+
+// Stream offsets and per-stream bases: in the kernel parameters when the batch is small, else
+// in the workspace.
+struct StreamTab {
+  const int64_t* offsets;
+  const int64_t* base;      // first output slot of each stream
+  const int64_t* seg_base;  // first segment of each stream
+};
+__device__ __forceinline__ StreamTab stream_tab(const CdcArgs& a) {
+  return a.inline_streams ? StreamTab{a.ib.offsets, a.ib.base, a.ib.seg_base}
+                          : StreamTab{a.offsets, a.base, a.seg_base};
 }
 
+// Pass 1: two warps per segment (two segments per CTA; each pair syncs on its own named
+// barrier, never the whole block).
+// Hashing: the window [p0, p_end) is cut into steps of 128 positions, lane l holding the 4
+// consecutive positions 4l .. 4l+3 of a step.  With g0..g3 their Gear words, the lane's block
+// contributes L = 8 g0 + 4 g1 + 2 g2 + g3 to the hash at its last position, and a 4-step
+// shuffle scan X_l = sum_{j <= l} L_j 2^(4 (l - j)) gives the hash there:
+// h(4l+3) = h_prev 2^(4l+4) + X_l (terms shifted by 64 or more vanish).  The lane then steps
+// h = 2 h + g through its own 4 positions from h(4l-1).  The step before the segment (whose
+// 128 positions include the 64 the first hash depends on) is hashed first, to warm the hash
+// up; each step's tokens are loaded one step ahead.  The two warps of a segment hash one half of
+// its steps each (the second warming up on the last step of the first half); the first walks.
+constexpr int kSegWarps = kSegThreads / 32;
+constexpr int kSegsPerCta = kSegWarps / 2;
+static_assert(kSegsPerCta == 2, "pair_sync");
+// Named barrier of a segment's two warps (ids fixed at compile time, so that the kernel uses
+// only the barriers it names).
+__device__ __forceinline__ void pair_sync(int pair) {
+  if (pair == 0) named_bar_sync(1, 64); else named_bar_sync(2, 64);
+}
+__global__ void __launch_bounds__(kSegThreads) cdc_segment_kernel(const __grid_constant__ CdcArgs a) {
+  extern __shared__ uint32_t win_all[];  // per segment: candidate words of positions [p0, p_end)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = warp >> 1, half = warp & 1;
+  const int64_t g = (int64_t)blockIdx.x * kSegsPerCta + pair;
+  if (g >= a.n_segs) return;  // both warps of a pair leave together
+  const int win_words = (kSeg + a.max_len - 1 + 31) / 32;
+  uint32_t* win = win_all + pair * win_words;
+  const StreamTab st = stream_tab(a);
+  int lo = 0, hi = a.S;  // the stream owning segment g: last s with seg_base[s] <= g
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (st.seg_base[mid] <= g) lo = mid; else hi = mid;
+  }
+  const int s = lo;
+  const int64_t k = g - st.seg_base[s];
+  const int64_t off = st.offsets[s], len = st.offsets[s + 1] - off;
+  const int64_t p0 = k * kSeg;
+  const int64_t seg_end = min(len, p0 + kSeg);                 // one past the segment
+  const int64_t p_end = min(len, p0 + kSeg + a.max_len - 1);   // one past the last end reachable
+  const int nwin = (int)((p_end - p0 + 31) / 32);
+  const int seg_words = (int)((seg_end - p0 + 31) / 32);
+  const int32_t* tok = a.tokens + off;
+  uint32_t* gw = a.words + (off >> 5) + s;  // word base of the stream (see the header)
+  const int64_t w0 = p0 >> 5;
+  const uint64_t* gear = a.gear;
+  const uint64_t gseed = a.gear_seed;
+  const int vocab = a.vocab, bits = a.bits, mode = a.mode;
+  // ---- candidate bitmask of the window
+  {
+    const int nsteps_all = (int)((p_end - p0 + 127) / 128);
+    const int mid = (nsteps_all + 1) / 2;
+    const int rbeg = half ? mid : 0, nsteps = half ? nsteps_all : mid;
+    int bad = 0;
+    uint64_t h_prev = 0;
+    int r = (rbeg > 0 || p0 > 0) ? rbeg - 1 : 0;
+    int32_t cur[4];
+    auto load_step = [&](int rr, int32_t (&t4)[4]) {
+      const int64_t p = p0 + 128 * (int64_t)rr + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t4[e] = p + e < len ? __ldg(tok + p + e) : -1;
+    };
+    load_step(r, cur);
+    for (; r < nsteps; ++r) {
+      int32_t nxt[4];
+      if (r + 1 < nsteps) load_step(r + 1, nxt);
+      const int64_t p = p0 + 128 * (int64_t)r + 4 * lane;  // the lane's first position (>= 0)
+      uint64_t gv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int32_t x = cur[e];
+        if (p + e >= len) {
+          gv[e] = 0ull;
+        } else if (x < 0 || x >= vocab) {
+          bad = 1;
+          gv[e] = 0ull;
+        } else {
+          gv[e] = gear != nullptr ? __ldg(gear + x) : splitmix_word(gseed, x);
+        }
+      }
+      uint64_t xs = (gv[0] << 3) + (gv[1] << 2) + (gv[2] << 1) + gv[3];
+#pragma unroll
+      for (int d = 1; d < 16; d <<= 1) {  // shifts 4, 8, 16, 32 (the shift-64 step vanishes)
+        const uint64_t y = __shfl_up_sync(kFull, xs, d);
+        if (lane >= d) xs += y << (4 * d);
+      }
+      const uint64_t h_last = (lane < 15 ? (h_prev << (4 * lane + 4)) : 0ull) + xs;
+      uint64_t h = __shfl_up_sync(kFull, h_last, 1);  // hash at position 4l - 1
+      if (lane == 0) h = h_prev;
+      uint32_t nib = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h = (h << 1) + gv[e];
+        if (p + e < len && cdc_candidate(h, bits, mode)) nib |= 1u << e;
+      }
+      // word j of the step collects the nibbles of lanes 8j .. 8j+7
+      uint32_t wv = nib << (4 * (lane & 7));
+      wv |= __shfl_xor_sync(kFull, wv, 1);
+      wv |= __shfl_xor_sync(kFull, wv, 2);
+      wv |= __shfl_xor_sync(kFull, wv, 4);
+      if (r >= rbeg && (lane & 7) == 0) {
+        const int w = 4 * r + (lane >> 3);
+        if (w < nwin) win[w] = wv;
+        if (w < seg_words) gw[w0 + w] = wv;  // the segment's own words, for the resolve pass
+      }
+      h_prev = __shfl_sync(kFull, h_last, 31);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
+    }
+    if (__any_sync(kFull, bad) && lane == 0) set_status(a.status, kDevErrBounds);
+  }
+  pair_sync(pair);  // the pair's window is complete
+  // ---- speculative walk from the segment start until a chunk ends at or past its end
+  int32_t* ends = a.spec_ends + g * a.spec_cap;
+  int* count_sh = reinterpret_cast<int*>(win_all + kSegsPerCta * win_words) + pair;
+  if (half == 0) {
+    const WordSrc words{gw, win, w0, nwin};
+    int64_t t = p0;
+    int c = 0;
+    while (t < seg_end && c < a.spec_cap) {
+      const int e = next_end(words, (int)len, (int)t, a.min_len, a.max_len, lane);
+      if (lane == 0) ends[c] = e;
+      ++c;
+      t = (int64_t)e + 1;
+    }
+    if (lane == 0) {
+      a.spec_count[g] = c;
+      a.spec_exit[g] = (int32_t)t;
+      *count_sh = c;
+    }
+  }
+  pair_sync(pair);  // the walk's ends are visible to both warps
+  const int c = *count_sh;
+  // ---- fingerprints of the speculative chunks, four lanes per chunk
+  if (a.chunk_hash != nullptr) {
+    const int q = lane & 3;
+    const uint32_t gmask = 0xfu << (lane & ~3);
+    for (int i = (32 * half + lane) >> 2; i < c; i += 16) {
+      const int stt = i == 0 ? (int)p0 : ends[i - 1] + 1;
+      const uint64_t h = chunk_xxh64_x4(tok + stt, ends[i] - stt + 1, a.seed, q, gmask, lane & ~3);
+      if (q == 0) a.spec_hash[g * a.spec_cap + i] = h;
+    }
+  }
+}
+
+// One segment of the chain, warp-collective: entering segment k of stream s at position t (the
+// first chunk start at or after the segment start), re-walk until a chunk ends where a
+// speculative one does, then take the rest of the speculative chunks.  Returns the chunks the
+// segment contributes; *exit = the first chunk start after the segment; *met = the walk met
+// the speculative chain (so that *exit is the speculative exit).  With `out` >= 0 the chunks
+// are written from output slot `out` on (re-walked ones fingerprinted here).
+struct SegCtx {
+  const int32_t* tok;
+  const uint32_t* gw;
+  int64_t len, gb;
+};
+__device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_t t, int64_t out, int lane,
+                            int64_t* exit, bool* met_out) {
+  const int64_t seg_start = k * kSeg, seg_end = min(x.len, seg_start + kSeg);
+  if (t >= seg_end) {  // a chunk longer than a segment covers this one
+    *exit = t;
+    *met_out = false;
+    return 0;
+  }
+  const int64_t gseg = x.gb + k;
+  const int32_t* ends = a.spec_ends + gseg * a.spec_cap;
+  const int nspec = a.spec_count[gseg];
+  const WordSrc words{x.gw, nullptr, 0, 0};
+  int count = 0;
+  int p = -1;  // last speculative chunk already covered by the re-walk
+  bool met = t == seg_start;  // both walks start at the same place
+  if (!met) {
+    int sb = 0;  // the speculative ends, 32 at a time in registers (lane i: ends[sb + i])
+    int32_t mine = lane < nspec ? ends[lane] : INT_MAX;
+    while (t < seg_end) {
+      const int e = next_end(words, (int)x.len, (int)t, a.min_len, a.max_len, lane);
+      if (out >= 0) {
+        if (lane == 0) {
+          a.chunk_start[out + count] = (int32_t)t;
+          a.chunk_len[out + count] = (int32_t)(e - t + 1);
+        }
+        if (a.chunk_hash != nullptr && lane < 4) {
+          const uint64_t h = chunk_xxh64_x4(x.tok + t, (int)(e - t + 1), a.seed, lane, 0xfu, 0);
+          if (lane == 0) a.chunk_hash[out + count] = h;
+        }
+      }
+      ++count;
+      t = (int64_t)e + 1;
+      bool found = false;
+      for (;;) {  // first speculative end >= e
+        const uint32_t ge = __ballot_sync(kFull, mine >= e);
+        if (ge != 0u) {
+          const int i = __ffs(ge) - 1;
+          if (__shfl_sync(kFull, mine, i) == e) {
+            met = true;
+            p = sb + i;
+          }
+          found = true;
+          break;
+        }
+        sb += 32;
+        if (sb >= nspec) break;
+        mine = sb + lane < nspec ? ends[sb + lane] : INT_MAX;
+      }
+      if (met || !found) break;
+    }
+  }
+  if (!met) {
+    *exit = t;
+    *met_out = false;
+    return count;
+  }
+  // speculative chunks after index p are the true ones
+  const int rest = nspec - (p + 1);
+  if (out >= 0) {
+    for (int i0 = p + 1; i0 < nspec; i0 += 32) {
+      const int i = i0 + lane;
+      if (i < nspec) {
+        const int64_t stt = i == 0 ? seg_start : (int64_t)ends[i - 1] + 1;
+        const int64_t o = out + count + (i - (p + 1));
+        a.chunk_start[o] = (int32_t)stt;
+        a.chunk_len[o] = (int32_t)(ends[i] - stt + 1);
+        if (a.chunk_hash != nullptr) a.chunk_hash[o] = a.spec_hash[gseg * a.spec_cap + i];
+      }
+    }
+  }
+  *exit = a.spec_exit[gseg];
+  *met_out = true;
+  return count + rest;
+}
+
+// Pass 2: one CTA per stream, kResWarps segments at a time (see the header).
+__global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __grid_constant__ CdcArgs a) {
+  __shared__ int cnt_sh[kResWarps];
+  __shared__ int met_sh[kResWarps];
+  __shared__ int64_t exit_sh[kResWarps];
+  __shared__ int64_t pos_sh[kResWarps + 1];
+  __shared__ int bad_sh;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const StreamTab st = stream_tab(a);
+  const int s = blockIdx.x;
+  const int64_t off = st.offsets[s], len = st.offsets[s + 1] - off;
+  const int64_t cb = st.base[s];
+  const SegCtx x{a.tokens + off, a.words + (off >> 5) + s, len, st.seg_base[s]};
+  const int64_t nseg = (len + kSeg - 1) / kSeg;
+  int64_t done = 0;  // chunks written so far
+  for (int64_t g0 = 0; g0 < nseg; g0 += kResWarps) {
+    const int64_t k = g0 + warp;
+    // the segment's entry, assuming the previous segment met its speculative chain
+    const int64_t entry = k == 0 ? 0 : (k < nseg ? (int64_t)a.spec_exit[x.gb + k - 1] : 0);
+    int64_t ex = 0;
+    bool met = false;
+    const int cnt = k < nseg ? walk_segment(a, x, k, entry, -1, lane, &ex, &met) : 0;
+    if (lane == 0) {
+      cnt_sh[warp] = cnt;
+      met_sh[warp] = (k < nseg - 1) ? (met ? 1 : 0) : 1;  // the last segment's exit matters to nobody
+      exit_sh[warp] = ex;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // the first segment whose exit is not its speculative one: its successors' assumed entries
+      // are wrong, so the chain continues in order after it
+      int bad = kResWarps;
+      for (int w = 0; w < kResWarps && g0 + w < nseg; ++w)
+        if (!met_sh[w]) {
+          bad = w;
+          break;
+        }
+      int64_t acc = done;
+      for (int w = 0; w <= min(bad, kResWarps - 1); ++w) {
+        pos_sh[w] = acc;
+        acc += (g0 + w < nseg) ? cnt_sh[w] : 0;
+      }
+      pos_sh[kResWarps] = acc;
+      bad_sh = bad;
+    }
+    __syncthreads();
+    const int bad = bad_sh;
+    if (k < nseg && warp <= bad) {
+      int64_t ex2;
+      bool met2;
+      walk_segment(a, x, k, entry, cb + pos_sh[warp], lane, &ex2, &met2);
+    }
+    done = pos_sh[kResWarps];
+    if (bad < kResWarps) {
+      // exact chain in order from the segment after `bad` (one warp)
+      if (warp == 0) {
+        int64_t t = exit_sh[bad];
+        for (int64_t kk = g0 + bad + 1; kk < nseg && t < len; ++kk) {
+          int64_t ex3;
+          bool met3;
+          done += walk_segment(a, x, kk, t, cb + done, lane, &ex3, &met3);
+          t = ex3;
+        }
+        if (lane == 0) a.n_chunks[s] = (int32_t)done;
+      }
+      return;
+    }
+    __syncthreads();  // the shared arrays are reused by the next group
+  }
+  if (threadIdx.x == 0) a.n_chunks[s] = (int32_t)done;
+}
 }  // namespace
 
 int cdc_segment_len() { return kSeg; }
 
 cudaError_t launch_cdc(const CdcArgs& a, int64_t max_stream_len, int64_t slots, int64_t n_segs,
                        cudaStream_t stream) {
+  (void)max_stream_len;
+  (void)slots;
   if (a.S <= 0) return cudaSuccess;
-  cdc_base_kernel<<<2, 1024, 0, stream>>>(a.offsets, a.S, a.min_len, a.base, a.seg_base);
-  const int64_t steps = (max_stream_len + 127) / 128;
-  const int64_t per_block = (int64_t)kHashWarps * kRunSteps;
-  const int64_t gx = steps > 0 ? (steps + per_block - 1) / per_block : 0;
-  if (gx > 0) {
-    dim3 grid((unsigned)gx, (unsigned)a.S);
-    cdc_hash_kernel<<<grid, 32 * kHashWarps, 0, stream>>>(a);
+  if (!a.inline_streams)
+    cdc_base_kernel<<<2, 1024, 0, stream>>>(a.offsets, a.S, a.min_len, a.base, a.seg_base);
+  if (n_segs > 0) {
+    // each segment's window words (at most (4096 + 65535) / 32, 8.7 KB), then the walks' counts
+    const size_t smem = (size_t)kSegsPerCta * ((kSeg + a.max_len - 1 + 31) / 32) * sizeof(uint32_t) +
+                        kSegsPerCta * sizeof(int);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(cdc_segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    cdc_segment_kernel<<<(unsigned)((n_segs + kSegsPerCta - 1) / kSegsPerCta), kSegThreads, smem, stream>>>(a);
   }
-  if (n_segs > 0) cdc_spec_kernel<<<(unsigned)((n_segs + 3) / 4), 128, 0, stream>>>(a, n_segs);
-  cdc_fixup_kernel<<<(a.S + 3) / 4, 128, 0, stream>>>(a);
-  if (a.chunk_hash != nullptr && slots > 0) {
-    const int64_t per_stream = max_stream_len / a.min_len + 1;  // most slots one stream owns
-    dim3 grid((unsigned)((4 * per_stream + 255) / 256), (unsigned)a.S);
-    cdc_fingerprint_kernel<<<grid, 256, 0, stream>>>(a);
-  }
+  cdc_resolve_kernel<<<(unsigned)a.S, kResWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

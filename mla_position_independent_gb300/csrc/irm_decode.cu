@@ -182,30 +182,9 @@ __device__ __forceinline__ void tmem_st_h<16>(uint32_t taddr, const uint32_t (&r
 template <>
 __device__ __forceinline__ void tmem_st_h<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
 
-// Fold 8 partial results (log2 max or log2-sum-exp mq, sum lq, output vq) into a running
-// (M, den, acc): acc and den are kept relative to M, rescaled when M grows.
-__device__ __forceinline__ void merge_batch(const float (&mq)[8], const float (&lq)[8], const float4 (&vq)[8],
-                                            float& M, float& den, float4& acc) {
-  float Mn = M;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mq[k]);
-  if (Mn == -INFINITY) return;
-  const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
-  den *= sc;
-  acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float w = (mq[k] == -INFINITY) ? 0.f : fast_exp2(mq[k] - Mn);
-    den += w * lq[k];
-    acc.x += w * vq[k].x;
-    acc.y += w * vq[k].y;
-    acc.z += w * vq[k].z;
-    acc.w += w * vq[k].w;
-  }
-  M = Mn;
-}
-
-// The same for 8 columns (two float4 per partial).
+// Fold 8 partial results (log2 max or log2-sum-exp mq, sum lq, and 8 output columns va | vb)
+// into a running (M, den, acc_a | acc_b): acc and den are kept relative to M, rescaled when M
+// grows.
 __device__ __forceinline__ void merge_batch2(const float (&mq)[8], const float (&lq)[8], const float4 (&va)[8],
                                              const float4 (&vb)[8], float& M, float& den, float4& acc_a,
                                              float4& acc_b) {

@@ -487,10 +487,11 @@ irm_status noalloc_scratch(void** out) {
 }
 
 // Workspace of irm_cdc_chunk: status header, the copied stream offsets [S + 1], slot and
-// segment bases [S + 1] each, the
-// candidate bitmask, then per speculative segment its chunk ends [spec_cap] and count.
+// segment bases [S + 1] each (used when the batch is too large for the kernel parameters),
+// the candidate bitmask, then per speculative segment its chunk ends [spec_cap], count and
+// exit, and its chunks' fingerprints [spec_cap].
 struct CdcLayout {
-  size_t offsets, base, seg_base, words, spec_ends, spec_count, total;
+  size_t offsets, base, seg_base, words, spec_ends, spec_count, spec_exit, spec_hash, total;
   int64_t n_segs, spec_cap;
 };
 irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_params* params,
@@ -525,7 +526,9 @@ irm_status cdc_check(const int64_t* offsets_host, int n_streams, const irm_cdc_p
   L.words = L.seg_base + bases;
   L.spec_ends = L.words + align_up(words * sizeof(uint32_t), 256);
   L.spec_count = L.spec_ends + align_up((size_t)L.n_segs * (size_t)L.spec_cap * sizeof(int32_t), 256);
-  L.total = L.spec_count + align_up((size_t)(L.n_segs + 1) * sizeof(int32_t), 256);
+  L.spec_exit = L.spec_count + align_up((size_t)(L.n_segs + 1) * sizeof(int32_t), 256);
+  L.spec_hash = L.spec_exit + align_up((size_t)(L.n_segs + 1) * sizeof(int32_t), 256);
+  L.total = L.spec_hash + align_up((size_t)L.n_segs * (size_t)L.spec_cap * sizeof(uint64_t), 256);
   *bytes = L.total;
   if (lay) *lay = L;
   return IRM_OK;
@@ -767,9 +770,28 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, int
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
     return fail(IRM_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const HostPart part = {offsets_host, 0, (size_t)(n_streams + 1) * sizeof(int64_t)};
-  if ((st = stage_to_device(&part, 1, ws + lay.offsets, stream)) != IRM_OK) return st;
-  irm::CdcArgs a{};
+  // ~25 KB with the inline stream table: kept off the stack; the fields before it are reset
+  thread_local irm::CdcArgs a;
+  std::memset(static_cast<void*>(&a), 0, offsetof(irm::CdcArgs, ib));
+  if (n_streams <= irm::kCdcInline) {
+    // offsets and per-stream bases (output slots, speculative segments) travel in the launch
+    a.inline_streams = 1;
+    int64_t sb = 0, gb = 0;
+    const int64_t seg = irm::cdc_segment_len();
+    for (int s = 0; s <= n_streams; ++s) {
+      a.ib.offsets[s] = offsets_host[s];
+      a.ib.base[s] = sb;
+      a.ib.seg_base[s] = gb;
+      if (s < n_streams) {
+        const int64_t len = offsets_host[s + 1] - offsets_host[s];
+        sb += len / p.min_len + 1;
+        gb += (len + seg - 1) / seg;
+      }
+    }
+  } else {
+    const HostPart part = {offsets_host, 0, (size_t)(n_streams + 1) * sizeof(int64_t)};
+    if ((st = stage_to_device(&part, 1, ws + lay.offsets, stream)) != IRM_OK) return st;
+  }
   a.tokens = tokens;
   a.offsets = reinterpret_cast<const int64_t*>(ws + lay.offsets);
   a.S = n_streams;
@@ -787,7 +809,10 @@ irm_status irm_cdc_chunk(const int32_t* tokens, const int64_t* offsets_host, int
   a.words = reinterpret_cast<uint32_t*>(ws + lay.words);
   a.spec_ends = reinterpret_cast<int32_t*>(ws + lay.spec_ends);
   a.spec_count = reinterpret_cast<int32_t*>(ws + lay.spec_count);
+  a.spec_exit = reinterpret_cast<int32_t*>(ws + lay.spec_exit);
+  a.spec_hash = reinterpret_cast<uint64_t*>(ws + lay.spec_hash);
   a.spec_cap = lay.spec_cap;
+  a.n_segs = lay.n_segs;
   a.n_chunks = n_chunks;
   a.chunk_start = chunk_start;
   a.chunk_len = chunk_len;

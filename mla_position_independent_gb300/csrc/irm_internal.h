@@ -113,10 +113,17 @@ struct DecodeArgs {
 // kernel parameter blocks are limited to 32764 bytes
 static_assert(sizeof(DecodeArgs) <= 32764 && sizeof(AttnArgs) <= 32764, "kernel parameter block");
 
-// Content-defined chunking of a batch of token streams.
+// Content-defined chunking of a batch of token streams.  A batch of at most kCdcInline
+// streams carries its offsets and per-stream bases in the kernel parameters.
+constexpr int kCdcInline = 1024;
+struct CdcStreams {
+  int64_t offsets[kCdcInline + 1];
+  int64_t base[kCdcInline + 1];
+  int64_t seg_base[kCdcInline + 1];
+};
 struct CdcArgs {
   const int32_t* tokens;    // [offsets[S]] token ids, streams concatenated
-  const int64_t* offsets;   // device [S + 1]
+  const int64_t* offsets;   // device [S + 1] (unused with inline_streams)
   int S;
   const uint64_t* gear;     // device [vocab], or nullptr: SplitMix64 words from gear_seed
   uint64_t gear_seed;
@@ -128,13 +135,19 @@ struct CdcArgs {
   uint32_t* words;          // workspace: candidate bitmask, stream s from word (offsets[s] >> 5) + s
   int32_t* spec_ends;       // workspace [segments][spec_cap]: speculative chunk ends
   int32_t* spec_count;      // workspace [segments]
+  int32_t* spec_exit;       // workspace [segments]: first chunk start after the speculative walk
+  uint64_t* spec_hash;      // workspace [segments][spec_cap]: fingerprints of the speculative chunks
   int64_t spec_cap;
+  int64_t n_segs;           // speculative segments over all streams
   int32_t* n_chunks;        // [S]
   int32_t* chunk_start;     // [slots] stream-relative start of each chunk
   int32_t* chunk_len;       // [slots]
   uint64_t* chunk_hash;     // [slots] or nullptr
   int* status;
+  int inline_streams;       // 1: offsets and bases are `ib` (S <= kCdcInline)
+  CdcStreams ib;
 };
+static_assert(sizeof(CdcArgs) <= 32764, "kernel parameter block");
 int cdc_segment_len();
 cudaError_t launch_cdc(const CdcArgs& a, int64_t max_stream_len, int64_t slots, int64_t n_segs,
                        cudaStream_t stream);

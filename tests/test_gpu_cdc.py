@@ -125,3 +125,28 @@ def test_cdc_long_chunks_cross_segments(oracle_mod):
     gear = oracle_mod.splitmix_gear(102400, 5)
     _run_and_check(oracle_mod, tokens, offsets, gear,
                    irm.CdcParams.make(min_len=3000, max_len=20000, bits=12, gear_seed=5), generated=True)
+
+
+def test_cdc_many_streams(oracle_mod):
+    """More streams than the launch parameters carry (1500, lengths 0 to 700): the offsets go
+    through the workspace and the per-stream bases are computed on the device."""
+    rng = np.random.default_rng(62)
+    gear = synth.gear_table(5000, seed=6)
+    lens = rng.integers(0, 700, 1500)
+    lens[::97] = 0
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tokens = rng.integers(0, 5000, offsets[-1]).astype(np.int32)
+    _run_and_check(oracle_mod, tokens, offsets, gear, irm.CdcParams.make(seed=9))
+
+
+def test_cdc_segment_boundaries(oracle_mod):
+    """Streams whose lengths sit at and around multiples of the 4096-token walk segment, with
+    chunk limits that make chunks end exactly at, before and after segment ends."""
+    rng = np.random.default_rng(63)
+    gear = synth.gear_table(3000, seed=7)
+    lens = [4095, 4096, 4097, 8191, 8192, 8193, 12288 + 511, 12288 + 512]
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tokens = rng.integers(0, 3000, offsets[-1]).astype(np.int32)
+    for params in (irm.CdcParams.make(), irm.CdcParams.make(min_len=64, max_len=64),
+                   irm.CdcParams.make(min_len=512, max_len=4096, bits=9)):
+        _run_and_check(oracle_mod, tokens, offsets, gear, params)
