@@ -98,15 +98,17 @@ struct ChunkWindow {
   }
 };
 
-// Rotate 8 rows [r0, r0 + 8) of a staged k_r slab by R(delta[row]) with one warp: lane =
-// (row of 8, 16-byte chunk v of 4) takes chunks v and v + 4 of the row (NeoX: k_r[8v .. 8v+7]
-// and their partners k_r[32+8v .. 32+8v+7]; interleaved: the 4 pairs inside each chunk).
+// Rotate 8 rows [r0, r0 + 8) of a staged k_r slab by R(delta[row]) with one warp: a lane takes
+// chunks v and v + 4 of one row (NeoX: k_r[8v .. 8v+7] and their partners k_r[32+8v .. 32+8v+7];
+// interleaved: the 4 pairs inside each chunk).  A 16-byte access is served a quarter-warp at a
+// time, so the 8 lanes of a quarter take rows p and p + 4 (r0 a multiple of 8): their swizzled
+// chunk positions v ^ p and v ^ (p + 4) are 8 distinct ones, every bank once.
 // dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls (recomputed only when the
 // row's delta changes; chunks are runs of equal delta).
 __device__ __forceinline__ void rotate_krope_8rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
                                                    int interleaved, int r0, int lane, int& dprev,
                                                    float (&cs_c)[8], float (&cs_s)[8]) {
-  const int r = r0 + (lane >> 2), v = lane & 3;
+  const int r = r0 + (lane >> 3) + 4 * ((lane >> 2) & 1), v = lane & 3;
   const int d = delta[r];
   if (d == 0) return;
   if (d != dprev) {
@@ -132,12 +134,14 @@ __device__ __forceinline__ int half_chunk(int interleaved, int rank, int c) {
 
 // Rotate 16 rows [r0, r0 + 16) of a staged half k_r slab (a CTA's 16 pairs per row, stored as
 // the chunks half_chunk(., rank, 0..3) at swizzled chunk positions cb .. cb + 3; cb = 0 or 4,
-// two stages share a slab).  Lane = (row of 16, c of 2) takes stored chunks c and c + 2.
+// two stages share a slab).  A lane takes stored chunks c and c + 2 of one row; the 8 lanes of a
+// quarter-warp (one 16-byte access phase) share c and take 8 consecutive rows (r0 a multiple of
+// 16), so their swizzled positions (cb + c) ^ (r & 7) are 8 distinct ones, every bank once.
 // dprev / cs_c / cs_s carry the lane's last (cos, sin) between calls.
 __device__ __forceinline__ void rotate_krope_half_16rows(uint8_t* kr, const int32_t* delta, const uint64_t* phaseF,
                                                          int interleaved, int rank, int r0, int cb, int lane,
                                                          int& dprev, float (&cs_c)[8], float (&cs_s)[8]) {
-  const int r = r0 + (lane >> 1), c = lane & 1;
+  const int r = r0 + (lane & 7) + 8 * (lane >> 4), c = (lane >> 3) & 1;
   const int d = delta[r];
   if (d == 0) return;
   if (d != dprev) {
