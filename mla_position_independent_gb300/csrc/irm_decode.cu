@@ -115,9 +115,8 @@ constexpr uint32_t kOffWmax = kOffAbort + 60;        // float [4 warps][32 heads
 constexpr uint32_t kOffWfail = kOffWmax + 512;       // int [4 warps]
 constexpr uint32_t kOffLsum = kOffWfail + 64;        // float [4 warps][32 heads]
 constexpr uint32_t kOffML = kOffLsum + 512;          // float m[32], l[32] of this split
-constexpr uint32_t kOffMapRun = kOffML + 256;        // uint32 [kKrSlots]: 8-row groups that are runs
 constexpr uint32_t kFixedBytes = 4096;
-static_assert(kOffMapRun + 4 * kKrSlots <= kFixedBytes, "fixed area overflow");
+static_assert(kOffML + 256 <= kFixedBytes, "fixed area overflow");
 
 enum : int {
   BAR_PAIR_FULL = 0,                           // [unit] every loader thread's copies landed
@@ -285,7 +284,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   if (tid == 0) {
     if (!table_ok) set_status(a.status, kDevErrBounds);
     for (int u = 0; u < kMaxUnits; ++u) {
-      mbar_init(bar(BAR_PAIR_FULL + u), kLoaderThreads + 1);  // + the TMA issuer's expect_tx
+      mbar_init(bar(BAR_PAIR_FULL + u), kLoaderThreads);
       mbar_init(bar(BAR_PAIR_EMPTY + u), 1);
     }
     for (int k = 0; k < kKrSlots; ++k) {
@@ -385,12 +384,8 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     // arrive fires once all of this thread's earlier copies have landed)
     if (ntiles > 0) {
       cp_async_arrive_noinc(bar(BAR_KR_LANDED + 0));
-      for (int pr = 0; pr < 4; ++pr) {
-        cp_async_arrive_noinc(bar(BAR_PAIR_FULL + pr));
-        if (pw == 0 && lane == 0) mbar_arrive(bar(BAR_PAIR_FULL + pr));  // tile 0 has no TMA boxes
-      }
+      for (int pr = 0; pr < 4; ++pr) cp_async_arrive_noinc(bar(BAR_PAIR_FULL + pr));
     }
-    const uint32_t* map_run = reinterpret_cast<const uint32_t*>(smem + kOffMapRun);
 
     // k_r rotation, in tile order: this warp's 8 rows of every slot whose bytes have landed
     int rot = 0;
@@ -434,19 +429,13 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       // k_r slot ks and its row map are free once the S^T of tile j - kKrSlots is done
       if (j >= kKrSlots && !(ok = wait_rotating(bar(BAR_KR_EMPTY + ks), kph ^ 1u, j))) break;
       if (!(ok = warp_wait(bar(BAR_MAP + ks), kph, abort_flag))) break;
-      // 8-row groups whose 8 source rows are consecutive go as TMA boxes (64 columns x 8 rows per
-      // slab, landing as one 1 KiB swizzle atom), the other rows as 16-byte cp.async
-      const uint32_t runm = map_run[ks];
       const __nv_bfloat16* rowp[kLoadPasses];
       uint32_t nb[kLoadPasses];
-      bool boxed[kLoadPasses];
 #pragma unroll
       for (int i = 0; i < kLoadPasses; ++i) {
-        const int r = kRowsPerPass * i + rsub;
-        const int sr = map_src[ks * kBN + r];
+        const int sr = map_src[ks * kBN + kRowsPerPass * i + rsub];
         rowp[i] = kvp + (int64_t)(sr >= 0 ? sr : 0) * kDRow + chk * 8;
         nb[i] = sr >= 0 ? 16u : 0u;
-        boxed[i] = (runm >> (r >> 3)) & 1u;
       }
       // k_r first: its rotation then overlaps the cKV copies
       const uint32_t kr = sb + L.kr + (uint32_t)ks * kSlab;
@@ -459,20 +448,8 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
         const int u = gu % L.units, use = gu / L.units;
         if (use >= 1 && !(ok = wait_rotating(bar(BAR_PAIR_EMPTY + u), (uint32_t)(use - 1) & 1u, j))) break;
         const uint32_t ub = sb + L.ring + (uint32_t)u * kPairBytes;
-        if (pw == 0 && lane == 0) {
-          mbar_arrive_expect_tx(bar(BAR_PAIR_FULL + u), (uint32_t)__popc(runm) * 2u * 1024u);
-          for (uint32_t m = runm; m != 0u; m &= m - 1u) {
-            const int gg = __ffs((int)m) - 1;
-            const int y = map_src[ks * kBN + 8 * gg];
-            // slab pair: 8-row group gg of slab e is the 1 KiB block 2 gg + e
-            tma_load_2d(ub + (uint32_t)(2 * gg) * 1024u, &a.kv_map, (2 * pr) * 64, y, bar(BAR_PAIR_FULL + u));
-            tma_load_2d(ub + (uint32_t)(2 * gg + 1) * 1024u, &a.kv_map, (2 * pr + 1) * 64, y,
-                        bar(BAR_PAIR_FULL + u));
-          }
-        }
 #pragma unroll
         for (int i = 0; i < kLoadPasses; ++i) {
-          if (boxed[i]) continue;
           const uint32_t r = (uint32_t)(kRowsPerPass * i + rsub);
           cp_async_16(ub + pair_offset(r, 0u, (uint32_t)chk), rowp[i] + (2 * pr) * 64, nb[i]);
           cp_async_16(ub + pair_offset(r, 1u, (uint32_t)chk), rowp[i] + (2 * pr + 1) * 64, nb[i]);
@@ -502,19 +479,6 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
           !(ok = warp_wait(bar(BAR_KR_EMPTY + ks), ((uint32_t)(t / kKrSlots) & 1u) ^ 1u, abort_flag)))
         break;
       cw.build_map((kb + t) * kBN, ctx, a.n_rows, map_src + ks * kBN, map_delta + ks * kBN, a.status, lane);
-      __syncwarp();
-      {
-        // group g (lanes 0-7) is a run when its 8 source rows are valid and consecutive
-        bool run = false;
-        if (lane < 8) {
-          const int32_t* ms = map_src + ks * kBN + 8 * lane;
-          run = ms[0] >= 0;
-#pragma unroll
-          for (int i = 1; i < 8; ++i) run = run && ms[i] == ms[0] + i;
-        }
-        const uint32_t m = __ballot_sync(kFullMask, run);
-        if (lane == 0) *reinterpret_cast<uint32_t*>(smem + kOffMapRun + 4u * (uint32_t)ks) = m;
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_MAP + ks));
     }

@@ -1,7 +1,5 @@
 // C ABI of the library: host-side validation of chunk tables, the copy of the validated
 // tables into the caller's workspace, launch geometry, launches.  No allocation.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -216,46 +214,6 @@ irm_status stage_table(const irm_chunk* chunks_host, const int32_t* indptr_host,
   return IRM_OK;
 }
 
-// The row store as a 2-D tensor for the decode kernel's TMA boxes: [n_rows, 576] bf16 (row pitch
-// 1152 B), boxes of 64 columns x 8 rows with the 128-byte swizzle of the UMMA operand layout.  The
-// encoder is the driver's, reached through the runtime (no link-time dependency on the driver
-// library); the last encoding per thread is reused while the row store stays the same.
-irm_status encode_kv_map(const void* kv_rows, int64_t n_rows, CUtensorMap* out) {
-  static std::mutex mu;
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (encode == nullptr) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q{};
-      const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return fail(IRM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
-  thread_local const void* last_ptr = nullptr;
-  thread_local int64_t last_rows = -1;
-  thread_local CUtensorMap last_map;
-  if (kv_rows != last_ptr || n_rows != last_rows) {
-    const cuuint64_t dims[2] = {(cuuint64_t)IRM_D_ROW, (cuuint64_t)n_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)IRM_D_ROW * 2};
-    const cuuint32_t box[2] = {64, 8};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = encode(&last_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_rows), dims,
-                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      last_ptr = nullptr;
-      return fail(IRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the row store", (int)r);
-    }
-    last_ptr = kv_rows;
-    last_rows = n_rows;
-  }
-  *out = last_map;
-  return IRM_OK;
-}
-
 constexpr int kBM = 128;
 constexpr int kBN = 64;
 
@@ -419,7 +377,6 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
     // (the table is written up to its length, and the kernel reads no further)
     thread_local irm::DecodeArgs d;
     std::memset(static_cast<void*>(&d), 0, offsetof(irm::DecodeArgs, tab));
-    if ((st = encode_kv_map(kv_rows, n_rows, &d.kv_map)) != IRM_OK) return st;
     d.q_lat = q_lat;
     d.q_rope = q_rope;
     d.kv = kv_rows;

@@ -1,7 +1,6 @@
 // Internal launch interfaces between the C ABI (irm_host.cu) and the kernels.
 #pragma once
 #include <cstdint>
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/irm.h"
@@ -85,7 +84,6 @@ struct DecodeHint {
 };
 constexpr int kDecodeHints = 256;
 struct DecodeArgs {
-  CUtensorMap kv_map;   // the row store as [n_rows, 576] bf16, boxes of 64 columns x 8 rows, 128B swizzle
   const void* q_lat;    // bf16 [B, H, 512]
   const void* q_rope;   // bf16 [B, H, 64]
   const void* kv;       // bf16 [n_rows, 576]

@@ -154,18 +154,6 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 }
 
 // ----------------------------------------------------------------------------------
-// TMA: 2-D tiled load of a tensor-map box into this CTA's shared memory, completion counted in
-// bytes on a CTA-local mbarrier.  x (the innermost coordinate) must be a multiple of 16 bytes.
-// ----------------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// ----------------------------------------------------------------------------------
 // Cluster helpers
 // ----------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
