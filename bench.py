@@ -156,6 +156,10 @@ def _prep_case(name, seed):
 # content-defined chunking workloads: (streams, tokens per stream)
 CDC_SHAPES = {"cdc_4M": (64, 1 << 16), "cdc_16M": (256, 1 << 16)}
 CDC_VOCAB = 102400
+# table sizes that the library passes in the kernel launch parameters (larger ones are copied
+# into the workspace by one more kernel): chunk records and requests of an attention call,
+# streams of a chunking call
+INLINE_CHUNKS, INLINE_REQUESTS, CDC_INLINE_STREAMS = 1024, 256, 1024
 
 
 DESCR = {
@@ -275,13 +279,22 @@ class Workload:
                                 workspace=self.ws, stream=stream)
 
     def launches_per_step(self):
+        """Kernels of this library that one step launches."""
         if self.kind == "cdc":
-            return 5  # base scans, hash + candidate bits, speculative walks, fix-up, fingerprints
-        return 1  # one fused kernel per call (the split-KV merge runs inside it)
+            # segment hashing + speculative walks, resolve; a batch of more than 1024 streams
+            # adds the kernel that scans the stream offsets on the device
+            return 2 + (len(self.offsets) - 1 > CDC_INLINE_STREAMS)
+        if self.kind == "gather":
+            return 2  # the table copy into the workspace, the rotate+gather kernel
+        # one fused kernel (the split-KV merge runs inside it); a table of more than 1024
+        # records or 256 requests is copied into the workspace by one more kernel
+        B = self.table.indptr_host.numel() - 1
+        inline = self.table.n_chunks <= INLINE_CHUNKS and B <= INLINE_REQUESTS
+        return 1 if inline else 2
 
     def kernel_name(self):
         if self.kind == "cdc":
-            return "cdc (5 kernels: base, hash, spec walk, fix-up, fingerprint)"
+            return "cdc_segment_kernel + cdc_resolve_kernel"
         if self.kind == "gather":
             return "rotate_gather_kernel"
         if self.kind == "decode" and self.H in (16, 32):

@@ -33,16 +33,16 @@
  *     kernel is launched: no separate copy, any host memory, and the caller may reuse the
  *     table as soon as the call returns (a captured graph replays the table as validated).
  *   - Otherwise the library copies the table into the table area of the caller's workspace
- *     on `stream` (cudaMemcpyAsync, host to device) before the kernels that read it.
- *     Page-locked (pinned) host tables are copied asynchronously: keep them unchanged until
- *     `stream` has passed the call.  Under CUDA stream capture the copy becomes part of the
- *     graph and every replay copies the same host bytes again, so they must stay unchanged
- *     for as long as the graph is replayed (the launch geometry was planned from them).
- *     When indptr_host is followed, at the next 8-byte boundary, by chunks_host in one
- *     pinned block, a single copy moves both; otherwise there is one copy per array.
- *     Pageable host tables are packed by the library and handed to the CUDA runtime, which
- *     has read them when the call returns, so the caller may reuse them at once; such a copy
- *     cannot be captured into a CUDA graph (IRM_ERR_INVALID_ARG during capture).
+ *     on `stream` before the kernels that read it.
+ *     Page-locked (pinned) host tables are read by a small copy kernel of the library straight
+ *     from host memory, when `stream` reaches the call: keep them unchanged until `stream`
+ *     has passed it.  Under CUDA stream capture the copy kernel becomes part of the graph and
+ *     every replay reads the same host bytes again, so they must stay unchanged for as long
+ *     as the graph is replayed (the launch geometry was planned from them).
+ *     Pageable host tables are packed by the library and handed to the CUDA runtime
+ *     (cudaMemcpyAsync, host to device), which has read them when the call returns, so the
+ *     caller may reuse them at once; such a copy cannot be captured into a CUDA graph
+ *     (IRM_ERR_INVALID_ARG during capture).
  * Kernels still re-check each source row against n_rows and each page index against
  * n_pages, and record (never fault on) a violation.
  *

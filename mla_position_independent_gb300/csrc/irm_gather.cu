@@ -160,6 +160,28 @@ __global__ void __launch_bounds__(kGatherThreads) rotate_gather_kernel(const Gat
   }
 }
 
+// Copies up to three host arrays into a device block: the sources are page-locked host memory
+// that the GPU reads directly (device-accessible addresses), in 4-byte words (every array is a
+// whole number of them).  One launch instead of one copy-engine transfer per array.
+__global__ void __launch_bounds__(256) host_copy_kernel(HostCopyArgs a) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int p = 0; p < a.n; ++p) {
+    const uint32_t* __restrict__ src = static_cast<const uint32_t*>(a.src[p]);
+    uint32_t* __restrict__ dst = reinterpret_cast<uint32_t*>(a.dst + a.off[p]);
+    const int64_t words = (int64_t)(a.bytes[p] / 4);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride) dst[i] = src[i];
+  }
+}
+
+cudaError_t launch_host_copy(const HostCopyArgs& a, cudaStream_t stream) {
+  size_t most = 0;
+  for (int p = 0; p < a.n; ++p) most = a.bytes[p] > most ? a.bytes[p] : most;
+  const int64_t words = (int64_t)(most / 4);
+  const int grid = (int)(words < 256 ? 1 : (words + 255) / 256 < 1024 ? (words + 255) / 256 : 1024);
+  host_copy_kernel<<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int B,
                              int64_t* row_start, cudaStream_t stream) {
   row_start_kernel<<<1, 1024, 0, stream>>>(chunks, indptr, B, row_start);

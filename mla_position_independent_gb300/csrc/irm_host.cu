@@ -145,13 +145,14 @@ size_t table_bytes(int B, int64_t n_chunks) {
   return align_up(indptr_area(B) + (size_t)n_chunks * sizeof(irm_chunk), 256);
 }
 
-bool host_pinned(const void* p) {
+// Device-accessible address of page-locked host memory, or nullptr for pageable memory.
+const void* host_pinned(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+    return nullptr;
   }
-  return at.type == cudaMemoryTypeHost;
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
 // A host array and where it goes inside the destination block.
@@ -160,26 +161,30 @@ struct HostPart {
   size_t off, bytes;
 };
 
-// Copies host arrays into a device block on `stream`.  Page-locked arrays are copied
-// directly (one copy when they already sit at the block's offsets in one host block);
-// pageable ones are packed into a host staging buffer and copied once, which the runtime has
-// read when cudaMemcpyAsync returns (pageable copies cannot be captured into a graph).
+// Copies host arrays into a device block on `stream`.  Page-locked arrays are read by one small
+// kernel straight from host memory (cheaper inside a step than a copy-engine transfer, whose
+// latency dominates for tables of a few hundred KB); pageable ones are packed into a host staging
+// buffer and copied once, which the runtime has read when cudaMemcpyAsync returns (pageable
+// copies cannot be captured into a graph).
 irm_status stage_to_device(const HostPart* parts, int n, uint8_t* dst, cudaStream_t stream) {
-  bool pinned = true;
-  for (int i = 0; i < n && pinned; ++i) pinned = host_pinned(parts[i].src);
+  const void* dev_src[3] = {nullptr, nullptr, nullptr};
+  bool pinned = n <= 3;
+  for (int i = 0; i < n && pinned; ++i) {
+    dev_src[i] = host_pinned(parts[i].src);
+    pinned = dev_src[i] != nullptr && parts[i].bytes % 4 == 0 && parts[i].off % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(dev_src[i]) % 4 == 0;
+  }
   cudaError_t e = cudaSuccess;
   if (pinned) {
-    const uint8_t* base = static_cast<const uint8_t*>(parts[0].src) - parts[0].off;
-    bool one_block = true;
-    for (int i = 1; i < n; ++i) one_block &= static_cast<const uint8_t*>(parts[i].src) == base + parts[i].off;
-    if (one_block) {
-      const size_t end = parts[n - 1].off + parts[n - 1].bytes;
-      e = cudaMemcpyAsync(dst + parts[0].off, base + parts[0].off, end - parts[0].off, cudaMemcpyHostToDevice,
-                          stream);
-    } else {
-      for (int i = 0; i < n && e == cudaSuccess; ++i)
-        e = cudaMemcpyAsync(dst + parts[i].off, parts[i].src, parts[i].bytes, cudaMemcpyHostToDevice, stream);
+    irm::HostCopyArgs c{};
+    c.dst = dst;
+    c.n = n;
+    for (int i = 0; i < n; ++i) {
+      c.src[i] = dev_src[i];
+      c.off[i] = parts[i].off;
+      c.bytes[i] = parts[i].bytes;
     }
+    e = irm::launch_host_copy(c, stream);
     if (e != cudaSuccess) return cuda_fail(e, "copying the chunk table to the workspace");
     return IRM_OK;
   }

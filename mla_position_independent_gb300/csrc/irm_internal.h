@@ -152,6 +152,15 @@ int cdc_segment_len();
 cudaError_t launch_cdc(const CdcArgs& a, int64_t max_stream_len, int64_t slots, int64_t n_segs,
                        cudaStream_t stream);
 
+// Copy of page-locked host arrays (device-accessible addresses) into a device block.
+struct HostCopyArgs {
+  const void* src[3];
+  size_t off[3], bytes[3];
+  uint8_t* dst;
+  int n;
+};
+cudaError_t launch_host_copy(const HostCopyArgs& a, cudaStream_t stream);
+
 cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int B,
                              int64_t* row_start, cudaStream_t stream);
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
