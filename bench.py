@@ -288,8 +288,7 @@ class Workload:
             return 2  # the table copy into the workspace, the rotate+gather kernel
         # one fused kernel (the split-KV merge runs inside it); a table of more than 1024
         # records or 256 requests is copied into the workspace by one more kernel
-        B = self.table.indptr_host.numel() - 1
-        inline = self.table.n_chunks <= INLINE_CHUNKS and B <= INLINE_REQUESTS
+        inline = self.table.n_chunks <= INLINE_CHUNKS and self.table.B <= INLINE_REQUESTS
         return 1 if inline else 2
 
     def kernel_name(self):
