@@ -531,6 +531,7 @@ KERNEL_SOURCES = {
     "mla_decode_kernel": ["irm_decode.cu", "irm_pipeline.cuh", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
     "mla_attn_kernel": ["irm_attn.cu", "irm_pipeline.cuh", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
     "rotate_gather_kernel": ["irm_gather.cu", "irm_common.cuh", "ptx.cuh", "irm_internal.h"],
+    "cdc_segment_kernel + cdc_resolve_kernel": ["irm_cdc.cu", "irm_common.cuh", "irm_internal.h"],
 }
 
 
