@@ -8,7 +8,6 @@
 #include <cstdarg>
 #include <cstddef>
 #include <cstdio>
-#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -228,7 +227,7 @@ constexpr int kBN = 64;
 // merge of the splits' partials.  In tile times (measured on the V3-shaped decode): a split's
 // pipeline fill and epilogue cost ~12 tiles, and the merge reads each split's fp32 partial,
 // ~3.6 tiles per split for 128 query rows (fewer rows, proportionally less).
-int choose_splits(int B, int64_t max_ctx, int H, int sms, double* cost_out = nullptr) {
+int choose_splits(int B, int64_t max_ctx, int H, int sms) {
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles = (max_ctx + kBN - 1) / kBN;
   const double split_cost = 12.0;
@@ -243,65 +242,6 @@ int choose_splits(int B, int64_t max_ctx, int H, int sms, double* cost_out = nul
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = S;
-    }
-  }
-  if (cost_out != nullptr) *cost_out = best_cost;
-  return best;
-}
-
-// Co-resident clusters of the attention kernel for Mv stored query rows, cached per device.
-int attn_clusters(int Mv) {
-  static std::mutex mu;
-  static int cache[64][17];
-  static bool have[64][17];
-  int dev = 0;
-  const int mi = std::min(16, std::max(0, Mv / 8));
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  std::lock_guard<std::mutex> lk(mu);
-  if (!have[dev][mi]) {
-    cache[dev][mi] = irm::attn_max_active_clusters(Mv);
-    have[dev][mi] = true;
-  }
-  return cache[dev][mi];
-}
-
-// Balanced launch of a one-query-tile-per-request attention: P clusters share the requests'
-// KV tiles laid end to end (cluster c takes tiles [cT/P, (c+1)T/P)).  Picks the P that
-// minimises, in tile times, a cluster's tiles + the pipeline fill and epilogue (~12) + ~3 per
-// further item + the merge of the most pieces a request is cut into (~3.6 per piece for 128
-// query rows).  Returns its cost (1e30 when none applies), the P and the most pieces.
-double choose_balanced(const std::vector<int64_t>& tiles, int H, int slots, int* P_out, int* pieces_out) {
-  const int B = (int)tiles.size();
-  int64_t T = 0;
-  for (int64_t t : tiles) T += t;
-  double best = 1e30;
-  *P_out = 0;
-  *pieces_out = 1;
-  if (slots <= 0 || T <= 0) return best;
-  const double merge_per_piece = 3.6 * std::min(H, kBM) / kBM;
-  for (int P = 1; P <= slots && P <= T; ++P) {
-    auto cl = [&](int64_t t) { return ((t + 1) * P - 1) / T; };
-    int64_t r0 = 0;
-    int most_pieces = 1;
-    std::vector<int> items(P, 0);
-    for (int b = 0; b < B; ++b) {
-      const int64_t r1 = r0 + tiles[b];
-      const int64_t c0 = cl(r0), c1 = cl(r1 - 1);
-      most_pieces = std::max(most_pieces, (int)(c1 - c0 + 1));
-      for (int64_t c = c0; c <= c1; ++c) ++items[c];
-      r0 = r1;
-    }
-    int most_items = 1;
-    for (int c = 0; c < P; ++c) most_items = std::max(most_items, items[c]);
-    const double cost = (double)((T + P - 1) / P) + 12.0 + 3.0 * (most_items - 1) +
-                        (most_pieces > 1 ? merge_per_piece * most_pieces : 0.0);
-    if (cost < best - 1e-9) {
-      best = cost;
-      *P_out = P;
-      *pieces_out = most_pieces;
     }
   }
   return best;
@@ -323,7 +263,6 @@ struct AttnPlan {
   int qpt, n_qtiles, S;
   bool few_heads;  // decode with H in {16, 32}: the split-KV decode kernel
   int C, G;        // its cluster size and clusters per request
-  int n_bal;       // attention kernel: balanced launch over n_bal clusters (0: split launch)
   size_t scratch_off;  // workspace offset of the split-KV scratch (after header and table)
   size_t ws_bytes;
 };
@@ -378,10 +317,7 @@ size_t decode_gpart_bytes(int B, int G, int H) { return ((size_t)B * G * H * IRM
 size_t decode_glse_bytes(int B, int G, int H) { return ((size_t)B * G * H * 4 + 255) / 256 * 256; }
 size_t decode_counter_bytes(int B, int C) { return ((size_t)B * C * 4 + 255) / 256 * 256; }
 
-// ws_cap: the most scratch the caller can offer for a balanced launch (a split launch is
-// planned instead when the balanced one needs more).
-irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p,
-                     size_t ws_cap = SIZE_MAX) {
+irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p) {
   if (H < 1 || H > IRM_MAX_HEADS) return fail(IRM_ERR_UNSUPPORTED, "H=%d outside [1, %d]", H, IRM_MAX_HEADS);
   if (n_q < 1) return fail(IRM_ERR_INVALID_ARG, "n_q must be >= 1");
   if (n_q > info.min_ctx)
@@ -400,33 +336,15 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
       p->ws_bytes += decode_gpart_bytes(B, p->G, H) + decode_glse_bytes(B, p->G, H) + decode_counter_bytes(B, p->C);
     return IRM_OK;
   }
-  double split_cost = 0.0;
-  p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms(), &split_cost) : 1;
-  p->n_bal = 0;
+  p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms()) : 1;
   p->ws_bytes = p->scratch_off + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
-  if (decode && p->n_qtiles == 1 && B + 1 <= irm::kInlineIndptr) {
-    // one query tile per request: the balanced launch when it is cheaper; every request then
-    // has at least one tile (n_q <= its context)
-    std::vector<int64_t> tiles(B);
-    for (int b = 0; b < B; ++b) tiles[b] = (info.ctx[b] + kBN - 1) / kBN;
-    const int Mv = std::min(kBM, (std::min(p->qpt, n_q) * H + 7) / 8 * 8);
-    int P = 0, pieces = 1;
-    const double bal_cost = choose_balanced(tiles, H, attn_clusters(Mv), &P, &pieces);
-    const size_t bal_ws = p->scratch_off + (pieces > 1 ? partial_bytes(B, 1, pieces) : 0);
-    if (P > 0 && bal_cost < split_cost - 1e-9 && bal_ws <= ws_cap) {
-      p->n_bal = P;
-      p->S = pieces;
-      p->ws_bytes = bal_ws;
-    }
-  }
   return IRM_OK;
 }
 
 irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                     const irm_chunk* chunks_host, const int32_t* indptr_host, const void* kv_rows,
                     int64_t n_rows, float softmax_scale, void* out, float* lse, const irm_rope* rope,
-                    void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode,
-                    size_t ws_cap = SIZE_MAX) {
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode) {
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
@@ -434,7 +352,7 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   int interleaved = 0;
   if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
   AttnPlan pl{};
-  if ((st = plan_attn(info, B, n_q, H, decode, &pl, ws_cap)) != IRM_OK) return st;
+  if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
   if (!q_lat || !q_rope || !kv_rows || !out) return fail(IRM_ERR_INVALID_ARG, "null device pointer");
   if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_rows, 16) || !aligned(out, 16))
     return fail(IRM_ERR_INVALID_ARG, "q_lat, q_rope, kv_rows and out must be 16-byte aligned");
@@ -525,15 +443,6 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   a.qpt = pl.qpt;
   a.n_qtiles = pl.n_qtiles;
   a.S = pl.S;
-  a.n_bal = pl.n_bal;
-  if (pl.n_bal > 0) {
-    int64_t t = 0;
-    for (int b = 0; b < B; ++b) {
-      a.tile_base[b] = (int32_t)t;
-      t += (info.ctx[b] + kBN - 1) / kBN;
-    }
-    a.tile_base[B] = (int32_t)t;
-  }
   // query rows a tile really holds (decode: H); Q, P and the score exchange store only these
   a.Mv = std::min(kBM, (std::min(pl.qpt, n_q) * H + 7) / 8 * 8);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -805,7 +714,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
   AttnPlan pl{};
-  if ((st = plan_attn(info, B, 1, H, true, &pl, kNoAllocScratchBytes)) != IRM_OK) return st;
+  if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
   if (pl.ws_bytes > kNoAllocScratchBytes)
     return fail(IRM_ERR_WORKSPACE,
                 "this decode needs %zu bytes of table and scratch, more than the %zu bytes the no-allocation "
@@ -828,8 +737,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   }
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, kv_rows,
-                  n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true,
-                  kNoAllocScratchBytes);
+                  n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true);
 }
 
 irm_status irm_decode_noalloc_status(cudaStream_t stream) {

@@ -68,11 +68,6 @@ struct AttnArgs {
   struct {
     uint64_t F[32];
   } phase;
-  // Balanced launch (one query tile per request, n_qtiles == 1): n_bal clusters share the
-  // requests' KV tiles laid end to end, tile_base[b] = tiles of requests before b (B <= 256);
-  // S is then the most pieces any request is cut into.  0: split launch, S splits per tile.
-  int n_bal;
-  int32_t tile_base[kInlineIndptr];
   int inline_table;  // 1: the table is `tab` below (chunks / indptr unused)
   InlineTable tab;
 };
@@ -171,7 +166,6 @@ cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
 size_t attn_smem_bytes(int Mv);
-int attn_max_active_clusters(int Mv);  // co-resident clusters of the attention kernel, 0 on error
 bool decode_supported(int H);
 int decode_max_active_clusters(int H, int C);  // 0 when C does not fit
 cudaError_t launch_mla_decode(const DecodeArgs& a, cudaStream_t stream);

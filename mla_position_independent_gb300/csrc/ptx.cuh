@@ -141,17 +141,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-// Per-warpgroup register budgets: every warp of a warpgroup executes the same instruction.
-// A block's warpgroups may only redistribute the registers it was launched with: an
-// increase waits until other warpgroups' decreases have released enough of them.
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 // Named barrier over `nthreads` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
   uint32_t r;
