@@ -310,6 +310,24 @@ def test_decode_split_kv(oracle_mod, H, ctxs):
     _check_attn(case, oracle_mod, prefill=False, select=sel, what=f"split-KV decode H={H} ctxs={ctxs}")
 
 
+@pytest.mark.parametrize("H", [64, 128])
+def test_decode_many_heads_ragged_batch(oracle_mod, H):
+    """96 requests of ragged contexts (24 to 250 KV tiles) with many heads: more query tiles
+    than fit on the GPU at once, so the tile kernel runs in waves; sampled on every request."""
+    rng = np.random.default_rng(40 + H)
+    ctxs = [int(c) for c in rng.integers(1500, 16000, 96)]
+    case = _ragged_decode_case(ctxs, H, seed=41 + H)
+    sel = np.array([[b, 0, h] for b in range(96) for h in (0, int(rng.integers(1, H - 1)), H - 1)])
+    _check_attn(case, oracle_mod, prefill=False, what=f"ragged decode H={H}", select=sel)
+
+
+def test_decode_single_tile_requests(oracle_mod):
+    """100 requests of at most one KV tile each, 128 heads; every output row is checked."""
+    ctxs = [33 + (13 * b) % 32 for b in range(100)]
+    case = _ragged_decode_case(ctxs, 128, seed=43)
+    _check_attn(case, oracle_mod, prefill=False, what="decode, one tile per request")
+
+
 @pytest.mark.parametrize("H", [16, 32])
 def test_decode_beyond_launch_hints(oracle_mod, H):
     """300 short requests: more decode splits than the launch arguments carry start hints for,
