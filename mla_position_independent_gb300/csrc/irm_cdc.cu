@@ -9,18 +9,19 @@
 //   else at the stream's end.
 //
 // Passes (two kernels):
-//   1. cdc_segment_kernel, one CTA per 4096-token segment of a stream: the CTA hashes the
+//   1. cdc_segment_kernel, four warps per 4096-token segment of a stream: they hash the
 //      segment and the max_len - 1 positions after it (a chunk starting in the segment ends
-//      there at the latest) into a candidate bitmask in shared memory (its own words also go
-//      to global memory), walks the chunks speculatively from the segment start (one ballot
-//      per chunk: next_end) and fingerprints those chunks while their tokens are hot.
+//      there at the latest) into a candidate bitmask in shared memory (the segment's own words
+//      also go to global memory); one of them walks the chunks speculatively from the segment
+//      start (one ballot per chunk: next_end), and all four fingerprint those chunks while
+//      their tokens are hot.
 //   2. cdc_resolve_kernel, one CTA per stream.  A walk entering a segment anywhere meets the
 //      segment's speculative chain within a chunk or two, after which both agree; the segment
 //      then exits where its speculative walk does.  So each warp takes one segment, enters it
 //      at the previous segment's speculative exit, re-walks until it meets the speculative
-//      chain, and counts its chunks; a prefix over the counts places every segment's chunks
-//      (the re-walked ones fingerprinted now, the speculative ones copied with their
-//      fingerprints).  A segment whose re-walk does not meet its chain (possible only with
+//      chain, and counts (and records and fingerprints) its chunks; a prefix over the counts
+//      places every segment's chunks (the recorded ones, then the speculative ones copied
+//      with their fingerprints).  A segment whose re-walk does not meet its chain (possible only with
 //      very long chunks) makes the rest of the stream follow the exact chain in order.
 // Token ids outside the Gear table are read as G = 0 and recorded in the status word.
 #include <cuda_runtime.h>
@@ -33,7 +34,7 @@ namespace irm {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kSegThreads = 128;      // threads per CTA of the segment pass (4 warps, a segment each)
+constexpr int kSegsPerCta = 2;        // segments per CTA of the segment pass
 constexpr int kResWarps = 16;         // warps per CTA of the resolve pass (segments at a time)
 
 // Gear word of token t from SplitMix64 (Steele, Lea, Flood 2014): the generator's (t+1)-th
@@ -207,8 +208,8 @@ __device__ __forceinline__ StreamTab stream_tab(const CdcArgs& a) {
                           : StreamTab{a.offsets, a.base, a.seg_base};
 }
 
-// Pass 1: two warps per segment (two segments per CTA; each pair syncs on its own named
-// barrier, never the whole block).
+// Pass 1: W warps per segment (two segments per CTA; each segment's warps sync on their own
+// named barrier, never the whole block).
 // Hashing: the window [p0, p_end) is cut into steps of 128 positions, lane l holding the 4
 // consecutive positions 4l .. 4l+3 of a step.  With g0..g3 their Gear words, the lane's block
 // contributes L = 8 g0 + 4 g1 + 2 g2 + g3 to the hash at its last position, and a 4-step
@@ -216,22 +217,25 @@ __device__ __forceinline__ StreamTab stream_tab(const CdcArgs& a) {
 // h(4l+3) = h_prev 2^(4l+4) + X_l (terms shifted by 64 or more vanish).  The lane then steps
 // h = 2 h + g through its own 4 positions from h(4l-1).  The step before the segment (whose
 // 128 positions include the 64 the first hash depends on) is hashed first, to warm the hash
-// up; each step's tokens are loaded one step ahead.  The two warps of a segment hash one half of
-// its steps each (the second warming up on the last step of the first half); the first walks.
-constexpr int kSegWarps = kSegThreads / 32;
-constexpr int kSegsPerCta = kSegWarps / 2;
-static_assert(kSegsPerCta == 2, "pair_sync");
-// Named barrier of a segment's two warps (ids fixed at compile time, so that the kernel uses
-// only the barriers it names).
-__device__ __forceinline__ void pair_sync(int pair) {
-  if (pair == 0) named_bar_sync(1, 64); else named_bar_sync(2, 64);
+// up; each step's tokens are loaded one step ahead.  The W warps of a segment hash a W-th of
+// its steps each (each but the first warming up on the step before its share); the first
+// walks.  W = 4 when the batch has few segments for the GPU (more warps to hide the 64-bit
+// arithmetic's latency), else 2 (less re-hashed warm-up).
+static_assert(kSegsPerCta == 2, "seg_sync");
+// Named barrier of a segment's warps (ids fixed at compile time, so that the kernel uses only
+// the barriers it names).
+template <int W>
+__device__ __forceinline__ void seg_sync(int seg) {
+  if (seg == 0) named_bar_sync(1, 32 * W); else named_bar_sync(2, 32 * W);
 }
-__global__ void __launch_bounds__(kSegThreads) cdc_segment_kernel(const __grid_constant__ CdcArgs a) {
+template <int W>
+__global__ void __launch_bounds__(32 * W * kSegsPerCta) cdc_segment_kernel(const __grid_constant__ CdcArgs a) {
+  constexpr int kSegWarpsPer = W;
   extern __shared__ uint32_t win_all[];  // per segment: candidate words of positions [p0, p_end)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pair = warp >> 1, half = warp & 1;
+  const int pair = warp / kSegWarpsPer, half = warp % kSegWarpsPer;  // segment in the CTA, its warp
   const int64_t g = (int64_t)blockIdx.x * kSegsPerCta + pair;
-  if (g >= a.n_segs) return;  // both warps of a pair leave together
+  if (g >= a.n_segs) return;  // a segment's warps leave together
   const int win_words = (kSeg + a.max_len - 1 + 31) / 32;
   uint32_t* win = win_all + pair * win_words;
   const StreamTab st = stream_tab(a);
@@ -257,8 +261,7 @@ __global__ void __launch_bounds__(kSegThreads) cdc_segment_kernel(const __grid_c
   // ---- candidate bitmask of the window
   {
     const int nsteps_all = (int)((p_end - p0 + 127) / 128);
-    const int mid = (nsteps_all + 1) / 2;
-    const int rbeg = half ? mid : 0, nsteps = half ? nsteps_all : mid;
+    const int rbeg = half * nsteps_all / kSegWarpsPer, nsteps = (half + 1) * nsteps_all / kSegWarpsPer;
     int bad = 0;
     uint64_t h_prev = 0;
     int r = (rbeg > 0 || p0 > 0) ? rbeg - 1 : 0;
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kSegThreads) cdc_segment_kernel(const __grid_c
     }
     if (__any_sync(kFull, bad) && lane == 0) set_status(a.status, kDevErrBounds);
   }
-  pair_sync(pair);  // the pair's window is complete
+  seg_sync<W>(pair);  // the segment's window is complete
   // ---- speculative walk from the segment start until a chunk ends at or past its end
   int32_t* ends = a.spec_ends + g * a.spec_cap;
   int* count_sh = reinterpret_cast<int*>(win_all + kSegsPerCta * win_words) + pair;
@@ -337,13 +340,13 @@ __global__ void __launch_bounds__(kSegThreads) cdc_segment_kernel(const __grid_c
       *count_sh = c;
     }
   }
-  pair_sync(pair);  // the walk's ends are visible to both warps
+  seg_sync<W>(pair);  // the walk's ends are visible to the segment's warps
   const int c = *count_sh;
   // ---- fingerprints of the speculative chunks, four lanes per chunk
   if (a.chunk_hash != nullptr) {
     const int q = lane & 3;
     const uint32_t gmask = 0xfu << (lane & ~3);
-    for (int i = (32 * half + lane) >> 2; i < c; i += 16) {
+    for (int i = (32 * half + lane) >> 2; i < c; i += 8 * kSegWarpsPer) {
       const int stt = i == 0 ? (int)p0 : ends[i - 1] + 1;
       const uint64_t h = chunk_xxh64_x4(tok + stt, ends[i] - stt + 1, a.seed, q, gmask, lane & ~3);
       if (q == 0) a.spec_hash[g * a.spec_cap + i] = h;
@@ -362,8 +365,17 @@ struct SegCtx {
   const uint32_t* gw;
   int64_t len, gb;
 };
+// The chunks a counting walk re-walked before it met the speculative chain (start, length,
+// fingerprint), kept in shared memory so that placing them needs no second walk.
+constexpr int kRec = 8;
+struct SegRec {
+  int32_t start[kRec], len[kRec];
+  uint64_t hash[kRec];
+  int n;  // re-walked chunks recorded, -1 when there were more than kRec
+  int p;  // the speculative chunk the walk met (-1: it started on the chain)
+};
 __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_t t, int64_t out, int lane,
-                            int64_t* exit, bool* met_out) {
+                            int64_t* exit, bool* met_out, SegRec* rec = nullptr) {
   const int64_t seg_start = k * kSeg, seg_end = min(x.len, seg_start + kSeg);
   if (t >= seg_end) {  // a chunk longer than a segment covers this one
     *exit = t;
@@ -391,6 +403,15 @@ __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_
           const uint64_t h = chunk_xxh64_x4(x.tok + t, (int)(e - t + 1), a.seed, lane, 0xfu, 0);
           if (lane == 0) a.chunk_hash[out + count] = h;
         }
+      } else if (rec != nullptr && count < kRec) {
+        uint64_t h = 0;
+        if (a.chunk_hash != nullptr && lane < 4)
+          h = chunk_xxh64_x4(x.tok + t, (int)(e - t + 1), a.seed, lane, 0xfu, 0);
+        if (lane == 0) {
+          rec->start[count] = (int32_t)t;
+          rec->len[count] = (int32_t)(e - t + 1);
+          rec->hash[count] = h;
+        }
       }
       ++count;
       t = (int64_t)e + 1;
@@ -412,6 +433,10 @@ __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_
       }
       if (met || !found) break;
     }
+  }
+  if (rec != nullptr && lane == 0) {
+    rec->n = count <= kRec ? count : -1;
+    rec->p = p;
   }
   if (!met) {
     *exit = t;
@@ -437,6 +462,31 @@ __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_
   return count + rest;
 }
 
+// Places a segment that met its speculative chain from its counting walk's record: the
+// re-walked chunks, then the speculative ones after the one the walk met.  Warp-collective.
+__device__ void emit_recorded(const CdcArgs& a, const SegCtx& x, int64_t k, const SegRec& r, int64_t out,
+                              int lane) {
+  if (lane < r.n) {
+    a.chunk_start[out + lane] = r.start[lane];
+    a.chunk_len[out + lane] = r.len[lane];
+    if (a.chunk_hash != nullptr) a.chunk_hash[out + lane] = r.hash[lane];
+  }
+  const int64_t seg_start = k * kSeg;
+  const int64_t gseg = x.gb + k;
+  const int32_t* ends = a.spec_ends + gseg * a.spec_cap;
+  const int nspec = a.spec_count[gseg];
+  for (int i0 = r.p + 1; i0 < nspec; i0 += 32) {
+    const int i = i0 + lane;
+    if (i < nspec) {
+      const int64_t stt = i == 0 ? seg_start : (int64_t)ends[i - 1] + 1;
+      const int64_t o = out + r.n + (i - (r.p + 1));
+      a.chunk_start[o] = (int32_t)stt;
+      a.chunk_len[o] = (int32_t)(ends[i] - stt + 1);
+      if (a.chunk_hash != nullptr) a.chunk_hash[o] = a.spec_hash[gseg * a.spec_cap + i];
+    }
+  }
+}
+
 // Pass 2: one CTA per stream, kResWarps segments at a time (see the header).
 __global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __grid_constant__ CdcArgs a) {
   __shared__ int cnt_sh[kResWarps];
@@ -444,6 +494,7 @@ __global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __gri
   __shared__ int64_t exit_sh[kResWarps];
   __shared__ int64_t pos_sh[kResWarps + 1];
   __shared__ int bad_sh;
+  __shared__ SegRec rec_sh[kResWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const StreamTab st = stream_tab(a);
   const int s = blockIdx.x;
@@ -458,7 +509,7 @@ __global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __gri
     const int64_t entry = k == 0 ? 0 : (k < nseg ? (int64_t)a.spec_exit[x.gb + k - 1] : 0);
     int64_t ex = 0;
     bool met = false;
-    const int cnt = k < nseg ? walk_segment(a, x, k, entry, -1, lane, &ex, &met) : 0;
+    const int cnt = k < nseg ? walk_segment(a, x, k, entry, -1, lane, &ex, &met, &rec_sh[warp]) : 0;
     if (lane == 0) {
       cnt_sh[warp] = cnt;
       met_sh[warp] = (k < nseg - 1) ? (met ? 1 : 0) : 1;  // the last segment's exit matters to nobody
@@ -485,9 +536,13 @@ __global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __gri
     __syncthreads();
     const int bad = bad_sh;
     if (k < nseg && warp <= bad) {
-      int64_t ex2;
-      bool met2;
-      walk_segment(a, x, k, entry, cb + pos_sh[warp], lane, &ex2, &met2);
+      if (met && rec_sh[warp].n >= 0) {
+        emit_recorded(a, x, k, rec_sh[warp], cb + pos_sh[warp], lane);
+      } else {
+        int64_t ex2;
+        bool met2;
+        walk_segment(a, x, k, entry, cb + pos_sh[warp], lane, &ex2, &met2);
+      }
     }
     done = pos_sh[kResWarps];
     if (bad < kResWarps) {
@@ -523,11 +578,17 @@ cudaError_t launch_cdc(const CdcArgs& a, int64_t max_stream_len, int64_t slots, 
     // each segment's window words (at most (4096 + 65535) / 32, 8.7 KB), then the walks' counts
     const size_t smem = (size_t)kSegsPerCta * ((kSeg + a.max_len - 1 + 31) / 32) * sizeof(uint32_t) +
                         kSegsPerCta * sizeof(int);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const unsigned grid = (unsigned)((n_segs + kSegsPerCta - 1) / kSegsPerCta);
+    // four warps per segment while two would leave fewer than 16 warps per SM
+    const bool wide = n_segs * 2 < (int64_t)16 * sms;
+    auto kern = wide ? cdc_segment_kernel<4> : cdc_segment_kernel<2>;
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(cdc_segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    cdc_segment_kernel<<<(unsigned)((n_segs + kSegsPerCta - 1) / kSegsPerCta), kSegThreads, smem, stream>>>(a);
+    kern<<<grid, 32 * (wide ? 4 : 2) * kSegsPerCta, smem, stream>>>(a);
   }
   cdc_resolve_kernel<<<(unsigned)a.S, kResWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
