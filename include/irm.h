@@ -34,11 +34,12 @@
  *     table as soon as the call returns (a captured graph replays the table as validated).
  *   - Otherwise the library copies the table into the table area of the caller's workspace
  *     on `stream` before the kernels that read it.
- *     Page-locked (pinned) host tables are read by a small copy kernel of the library straight
- *     from host memory, when `stream` reaches the call: keep them unchanged until `stream`
- *     has passed it.  Under CUDA stream capture the copy kernel becomes part of the graph and
- *     every replay reads the same host bytes again, so they must stay unchanged for as long
- *     as the graph is replayed (the launch geometry was planned from them).
+ *     Page-locked (pinned) host tables are read when `stream` reaches the call: by a small copy
+ *     kernel of the library straight from host memory (memory mapped for the device, as
+ *     cudaHostAlloc / cudaMallocHost give), else by cudaMemcpyAsync.  Keep them unchanged until
+ *     `stream` has passed the call.  Under CUDA stream capture the copy becomes part of the
+ *     graph and every replay reads the same host bytes again, so they must stay unchanged for
+ *     as long as the graph is replayed (the launch geometry was planned from them).
  *     Pageable host tables are packed by the library and handed to the CUDA runtime
  *     (cudaMemcpyAsync, host to device), which has read them when the call returns, so the
  *     caller may reuse them at once; such a copy cannot be captured into a CUDA graph

@@ -145,14 +145,20 @@ size_t table_bytes(int B, int64_t n_chunks) {
   return align_up(indptr_area(B) + (size_t)n_chunks * sizeof(irm_chunk), 256);
 }
 
-// Device-accessible address of page-locked host memory, or nullptr for pageable memory.
-const void* host_pinned(const void* p) {
+// Page-locked host memory: `locked`, and the address the device reads it through (nullptr
+// when the memory is locked but not mapped for the device).
+struct HostMem {
+  bool locked;
+  const void* dev;
+};
+HostMem host_mem(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
-    return nullptr;
+    return {false, nullptr};
   }
-  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  if (at.type != cudaMemoryTypeHost) return {false, nullptr};
+  return {true, at.devicePointer};
 }
 
 // A host array and where it goes inside the destination block.
@@ -161,21 +167,24 @@ struct HostPart {
   size_t off, bytes;
 };
 
-// Copies host arrays into a device block on `stream`.  Page-locked arrays are read by one small
-// kernel straight from host memory (cheaper inside a step than a copy-engine transfer, whose
-// latency dominates for tables of a few hundred KB); pageable ones are packed into a host staging
-// buffer and copied once, which the runtime has read when cudaMemcpyAsync returns (pageable
-// copies cannot be captured into a graph).
+// Copies host arrays into a device block on `stream`.  Page-locked arrays that the device can
+// address are read by one small kernel straight from host memory (cheaper inside a step than
+// copy-engine transfers, whose latency dominates for tables of a few hundred KB); other
+// page-locked arrays are copied by one cudaMemcpyAsync each; pageable ones are packed into a
+// host staging buffer and copied once, which the runtime has read when cudaMemcpyAsync returns
+// (pageable copies cannot be captured into a graph).
 irm_status stage_to_device(const HostPart* parts, int n, uint8_t* dst, cudaStream_t stream) {
   const void* dev_src[3] = {nullptr, nullptr, nullptr};
-  bool pinned = n <= 3;
-  for (int i = 0; i < n && pinned; ++i) {
-    dev_src[i] = host_pinned(parts[i].src);
-    pinned = dev_src[i] != nullptr && parts[i].bytes % 4 == 0 && parts[i].off % 4 == 0 &&
-             reinterpret_cast<uintptr_t>(dev_src[i]) % 4 == 0;
+  bool locked = true, mapped = n <= 3;
+  for (int i = 0; i < n && locked; ++i) {
+    const HostMem m = host_mem(parts[i].src);
+    locked = m.locked;
+    if (i < 3) dev_src[i] = m.dev;
+    mapped = mapped && m.dev != nullptr && parts[i].bytes % 4 == 0 && parts[i].off % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(m.dev) % 4 == 0;
   }
   cudaError_t e = cudaSuccess;
-  if (pinned) {
+  if (locked && mapped) {
     irm::HostCopyArgs c{};
     c.dst = dst;
     c.n = n;
@@ -185,6 +194,12 @@ irm_status stage_to_device(const HostPart* parts, int n, uint8_t* dst, cudaStrea
       c.bytes[i] = parts[i].bytes;
     }
     e = irm::launch_host_copy(c, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the chunk table to the workspace");
+    return IRM_OK;
+  }
+  if (locked) {
+    for (int i = 0; i < n && e == cudaSuccess; ++i)
+      e = cudaMemcpyAsync(dst + parts[i].off, parts[i].src, parts[i].bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "copying the chunk table to the workspace");
     return IRM_OK;
   }
