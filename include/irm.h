@@ -245,9 +245,12 @@ irm_status irm_mla_attn_decode_rope(const void* q_lat, const void* q_rope, int B
  *
  * Same arguments and results as irm_mla_attn_decode, minus the workspace.  The split-KV
  * scratch and the copied chunk table live in a fixed 32 MiB device array inside this library
- * (every GPU that loads the library holds it until the process exits).  A decode whose table
- * and scratch would exceed 32 MiB (IRM_ERR_WORKSPACE) is rejected before anything is copied
- * or launched; use irm_mla_attn_decode then.  The first call on each device looks up the
+ * (every GPU that loads the library holds it until the process exits).  The split of the
+ * decode is chosen within that scratch: where irm_mla_attn_decode would use a split whose
+ * scratch does not fit, this call uses the split it would otherwise take (same results up to
+ * rounding order).  A decode whose table and scratch would still exceed 32 MiB
+ * (IRM_ERR_WORKSPACE) is rejected before anything is copied or launched; use
+ * irm_mla_attn_decode then.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current and caches it per
  * device ordinal, which assumes the CUDA runtime's primary context of that device (a caller
  * that binds another context through the driver API must not use this entry point); make

@@ -191,8 +191,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto kr_slab = [&](int st) -> uint32_t { return L.kr + (uint32_t)(st >> 1) * kSlabKV; };  // smem offset
 
   // ---- work unit: request b, query tile, KV split --------------------------------------
-  const int b = blockIdx.y;
-  const int unit = blockIdx.x >> 1;
+  // Split launch: grid (2 n_qtiles S, B), cluster x / 2 = qtile S + split.  Long-first launch
+  // (one query tile per request, S = 2): grid (2 B, 2), split = y, so that every long split 0
+  // precedes every short split 1 in the grid and the short ones fill the cluster slots left.
+  const int b = a.long_first ? (int)(blockIdx.x >> 1) : (int)blockIdx.y;
+  const int unit = a.long_first ? (int)blockIdx.y : (int)(blockIdx.x >> 1);
   const int qtile = unit / a.S, split = unit % a.S;
   // the chunk table: in the parameter block (small tables) or in the workspace
   const irm_chunk* chunks = a.inline_table ? a.tab.chunks : a.chunks;
@@ -211,8 +214,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int rows_valid = nq_tile * a.H;
   const int pos_last = ctx - a.n_q + q0 + nq_tile - 1;
   const int kv_tiles = (table_ok && pos_last >= 0) ? (pos_last + kBN) / kBN : 0;
-  const int kb = (int)((int64_t)split * kv_tiles / a.S);
-  const int ke = (int)((int64_t)(split + 1) * kv_tiles / a.S);
+  // split boundaries at split * kv_tiles * num / den (the last one at kv_tiles): num / den = 1 / S,
+  // or for the long-first launch the cut (in 1/4096)
+  const int kb = (int)((int64_t)split * kv_tiles * a.split_num / a.split_den);
+  const int ke = split == a.S - 1 ? kv_tiles : (int)((int64_t)(split + 1) * kv_tiles * a.split_num / a.split_den);
   const int ntiles = ke - kb;
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBars + 8u * (uint32_t)i; };
@@ -840,26 +845,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 size_t attn_smem_bytes(int Mv) { return launch_smem(Mv); }
 
+namespace {
+// The kernel's dynamic shared memory limit belongs to the device: raised when a launch needs
+// more than what was set on this device before.
+cudaError_t raise_smem_limit(uint32_t smem) {
+  static std::mutex mu;
+  static uint32_t set_to[128];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= 128 || set_to[dev] < smem) {
+    e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) set_to[dev] = smem;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
+int attn_max_active_clusters(int Mv) {
+  const uint32_t smem = launch_smem(Mv);
+  if (raise_smem_limit(smem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_attn_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream) {
   if (make_layout(a.Mv, 0).stages < 2 || make_layout(a.Mv, 1).stages < 2)
     return cudaErrorInvalidConfiguration;
+  if (a.long_first && (a.S != 2 || a.n_qtiles != 1)) return cudaErrorInvalidConfiguration;
   const uint32_t smem = launch_smem(a.Mv);
-  {
-    // the kernel's dynamic shared memory limit belongs to the device: raised when a launch
-    // needs more than what was set on this device before
-    static std::mutex mu;
-    static uint32_t set_to[128];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev < 0 || dev >= 128 || set_to[dev] < smem) {
-      e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 128) set_to[dev] = smem;
-    }
-  }
-  dim3 grid(2 * a.n_qtiles * a.S, a.B);
+  cudaError_t e = raise_smem_limit(smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = a.long_first ? dim3(2 * a.B, 2) : dim3(2 * a.n_qtiles * a.S, a.B);
   mla_attn_kernel<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }

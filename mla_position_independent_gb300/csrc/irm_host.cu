@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstddef>
 #include <cstdio>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -242,7 +243,7 @@ constexpr int kBN = 64;
 // merge of the splits' partials.  In tile times (measured on the V3-shaped decode): a split's
 // pipeline fill and epilogue cost ~12 tiles, and the merge reads each split's fp32 partial,
 // ~3.6 tiles per split for 128 query rows (fewer rows, proportionally less).
-int choose_splits(int B, int64_t max_ctx, int H, int sms) {
+int choose_splits(int B, int64_t max_ctx, int H, int sms, double* cost_out = nullptr) {
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles = (max_ctx + kBN - 1) / kBN;
   const double split_cost = 12.0;
@@ -259,7 +260,43 @@ int choose_splits(int B, int64_t max_ctx, int H, int sms) {
       best = S;
     }
   }
+  if (cost_out != nullptr) *cost_out = best_cost;
   return best;
+}
+
+// Co-resident clusters of the attention kernel for Mv stored query rows, cached per device.
+int attn_clusters(int Mv) {
+  static std::mutex mu;
+  static int cache[64][17];
+  static bool have[64][17];
+  int dev = 0;
+  const int mi = std::min(16, std::max(0, Mv / 8));
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev][mi]) {
+    cache[dev][mi] = irm::attn_max_active_clusters(Mv);
+    have[dev][mi] = true;
+  }
+  return cache[dev][mi];
+}
+
+// Long-first split of U query tiles of `tiles` KV tiles each over P co-resident clusters, when
+// U < P: split 0 (the leading L tiles of every query tile) takes U clusters at once, the P - U
+// clusters left run the U short splits one after another (R = ceil(U / (P - U)) each).  L
+// balances the two, L + 12 = R (tiles - L + 12) (12: a split's fill and epilogue, in tile
+// times as in choose_splits), plus the merge of two partials.  Returns the cost (1e30 when it
+// does not apply) and the cut L / tiles in 1/4096.
+double choose_long_first(int U, int64_t tiles, int H, int P, int* cut_q12) {
+  *cut_q12 = 0;
+  if (P <= 0 || U >= P || tiles < 2) return 1e30;
+  const int64_t R = (U + (P - U) - 1) / (P - U);
+  const double L = std::min((double)tiles - 1.0, std::max(1.0, ((double)R * ((double)tiles + 12.0) - 12.0) / (1.0 + R)));
+  *cut_q12 = (int)std::lround(L / (double)tiles * 4096.0);
+  const double merge = 2.0 * 3.6 * std::min(H, kBM) / kBM;
+  return std::max(L + 12.0, (double)R * ((double)tiles - L + 12.0)) + merge;
 }
 
 // Split-KV scratch: fp32 partial O, per-rank partial LSE, finished-split counters.
@@ -278,6 +315,7 @@ struct AttnPlan {
   int qpt, n_qtiles, S;
   bool few_heads;  // decode with H in {16, 32}: the split-KV decode kernel
   int C, G;        // its cluster size and clusters per request
+  int long_first, cut_q12;  // attention kernel: long-first split (S == 2) and its cut
   size_t scratch_off;  // workspace offset of the split-KV scratch (after header and table)
   size_t ws_bytes;
 };
@@ -332,7 +370,10 @@ size_t decode_gpart_bytes(int B, int G, int H) { return ((size_t)B * G * H * IRM
 size_t decode_glse_bytes(int B, int G, int H) { return ((size_t)B * G * H * 4 + 255) / 256 * 256; }
 size_t decode_counter_bytes(int B, int C) { return ((size_t)B * C * 4 + 255) / 256 * 256; }
 
-irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p) {
+// ws_cap: the most scratch the caller can offer for a long-first split (the usual split is
+// planned instead when that one needs more).
+irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, AttnPlan* p,
+                     size_t ws_cap = SIZE_MAX) {
   if (H < 1 || H > IRM_MAX_HEADS) return fail(IRM_ERR_UNSUPPORTED, "H=%d outside [1, %d]", H, IRM_MAX_HEADS);
   if (n_q < 1) return fail(IRM_ERR_INVALID_ARG, "n_q must be >= 1");
   if (n_q > info.min_ctx)
@@ -351,15 +392,32 @@ irm_status plan_attn(const TableInfo& info, int B, int n_q, int H, bool decode, 
       p->ws_bytes += decode_gpart_bytes(B, p->G, H) + decode_glse_bytes(B, p->G, H) + decode_counter_bytes(B, p->C);
     return IRM_OK;
   }
-  p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms()) : 1;
+  double split_cost = 0.0;
+  p->S = decode ? choose_splits(B, info.max_ctx, H, num_sms(), &split_cost) : 1;
+  p->long_first = 0;
+  p->cut_q12 = 0;
   p->ws_bytes = p->scratch_off + (p->S > 1 ? partial_bytes(B, p->n_qtiles, p->S) : 0);
+  if (decode && p->n_qtiles == 1) {
+    const int Mv = std::min(kBM, (std::min(p->qpt, n_q) * H + 7) / 8 * 8);
+    int cut = 0;
+    const double lf_cost = choose_long_first(B * p->n_qtiles, (info.max_ctx + kBN - 1) / kBN, H,
+                                             attn_clusters(Mv), &cut);
+    const size_t lf_ws = p->scratch_off + partial_bytes(B, p->n_qtiles, 2);
+    if (lf_cost < split_cost - 1e-9 && lf_ws <= ws_cap) {
+      p->long_first = 1;
+      p->cut_q12 = cut;
+      p->S = 2;
+      p->ws_bytes = lf_ws;
+    }
+  }
   return IRM_OK;
 }
 
 irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H,
                     const irm_chunk* chunks_host, const int32_t* indptr_host, const void* kv_rows,
                     int64_t n_rows, float softmax_scale, void* out, float* lse, const irm_rope* rope,
-                    void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode) {
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream, bool decode,
+                    size_t ws_cap = SIZE_MAX) {
   TableInfo info;
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
@@ -367,7 +425,7 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   int interleaved = 0;
   if ((st = rope_select(rope, phaseF, &interleaved)) != IRM_OK) return st;
   AttnPlan pl{};
-  if ((st = plan_attn(info, B, n_q, H, decode, &pl)) != IRM_OK) return st;
+  if ((st = plan_attn(info, B, n_q, H, decode, &pl, ws_cap)) != IRM_OK) return st;
   if (!q_lat || !q_rope || !kv_rows || !out) return fail(IRM_ERR_INVALID_ARG, "null device pointer");
   if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_rows, 16) || !aligned(out, 16))
     return fail(IRM_ERR_INVALID_ARG, "q_lat, q_rope, kv_rows and out must be 16-byte aligned");
@@ -458,6 +516,9 @@ irm_status run_attn(const void* q_lat, const void* q_rope, int B, int n_q, int H
   a.qpt = pl.qpt;
   a.n_qtiles = pl.n_qtiles;
   a.S = pl.S;
+  a.long_first = pl.long_first;
+  a.split_num = pl.long_first ? pl.cut_q12 : 1;
+  a.split_den = pl.long_first ? 4096 : pl.S;
   // query rows a tile really holds (decode: H); Q, P and the score exchange store only these
   a.Mv = std::min(kBM, (std::min(pl.qpt, n_q) * H + 7) / 8 * 8);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -729,7 +790,7 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   irm_status st = validate(chunks_host, indptr_host, B, n_rows, &info);
   if (st != IRM_OK) return st;
   AttnPlan pl{};
-  if ((st = plan_attn(info, B, 1, H, true, &pl)) != IRM_OK) return st;
+  if ((st = plan_attn(info, B, 1, H, true, &pl, kNoAllocScratchBytes)) != IRM_OK) return st;
   if (pl.ws_bytes > kNoAllocScratchBytes)
     return fail(IRM_ERR_WORKSPACE,
                 "this decode needs %zu bytes of table and scratch, more than the %zu bytes the no-allocation "
@@ -752,7 +813,8 @@ irm_status irm_mla_attn_decode_noalloc(const void* q_lat, const void* q_rope, in
   }
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation scratch");
   return run_attn(q_lat, q_rope, B, 1, H, chunks_host, indptr_host, kv_rows,
-                  n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true);
+                  n_rows, softmax_scale, out, lse, nullptr, ws, kNoAllocScratchBytes, stream, true,
+                  kNoAllocScratchBytes);
 }
 
 irm_status irm_decode_noalloc_status(cudaStream_t stream) {

@@ -68,6 +68,12 @@ struct AttnArgs {
   struct {
     uint64_t F[32];
   } phase;
+  // Split boundaries: split s of a query tile starts at s * kv_tiles * split_num / split_den
+  // (1 / S for equal splits).  Long-first launch (one query tile per request, S == 2): the cut
+  // split_num / split_den is the long split's share, and the grid is (2 B, 2) so that every
+  // long split precedes every short one.
+  int long_first;
+  int split_num, split_den;
   int inline_table;  // 1: the table is `tab` below (chunks / indptr unused)
   InlineTable tab;
 };
@@ -166,6 +172,7 @@ cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attn(const AttnArgs& a, cudaStream_t stream);
 size_t attn_smem_bytes(int Mv);
+int attn_max_active_clusters(int Mv);  // co-resident clusters of the attention kernel, 0 on error
 bool decode_supported(int H);
 int decode_max_active_clusters(int H, int C);  // 0 when C does not fit
 cudaError_t launch_mla_decode(const DecodeArgs& a, cudaStream_t stream);

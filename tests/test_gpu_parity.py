@@ -321,6 +321,20 @@ def test_decode_many_heads_ragged_batch(oracle_mod, H):
     _check_attn(case, oracle_mod, prefill=False, what=f"ragged decode H={H}", select=sel)
 
 
+@pytest.mark.parametrize("H", [64, 128])
+def test_decode_long_first_split(oracle_mod, H):
+    """40 requests (fewer query tiles than cluster slots) of ragged contexts, some of a single KV
+    tile: each query tile's KV is cut into a long leading split, all scheduled first, and a short
+    trailing one run on the cluster slots left (empty for the one-tile requests); the two
+    partials are merged by whichever finishes last.  Sampled on every request."""
+    rng = np.random.default_rng(50 + H)
+    ctxs = [int(c) for c in rng.integers(4000, 9000, 40)]
+    ctxs[3], ctxs[17], ctxs[30] = 33, 64, 65
+    case = _ragged_decode_case(ctxs, H, seed=51 + H)
+    sel = np.array([[b, 0, h] for b in range(40) for h in (0, int(rng.integers(1, H - 1)), H - 1)])
+    _check_attn(case, oracle_mod, prefill=False, what=f"long-first decode H={H}", select=sel)
+
+
 def test_decode_single_tile_requests(oracle_mod):
     """100 requests of at most one KV tile each, 128 heads; every output row is checked."""
     ctxs = [33 + (13 * b) % 32 for b in range(100)]

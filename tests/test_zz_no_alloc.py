@@ -65,18 +65,15 @@ def test_noalloc_rejects_decode_larger_than_its_scratch():
         pytest.skip("no GPU")
     import mla_position_independent_gb300 as irm
     L = irm.lib()
-    # a batch of long 128-head requests whose split-KV scratch is more than the array holds
-    # (how far a decode is split depends on the device, so a few batch sizes are tried)
-    need = ctypes.c_size_t(0)
-    for B in (48, 64, 96, 128, 192):
-        reqs = [[(0, 32, 0, 0), (32, 32736, 0, 0)] for _ in range(B)]
-        chunks, indptr = synth.make_table(reqs)
-        assert L.irm_mla_attn_decode_workspace_size(chunks.ctypes.data, indptr.ctypes.data, B, 128,
-                                                    ctypes.byref(need)) == 0
-        if need.value > 32 << 20:
-            break
-    else:
-        pytest.skip("this device splits these decodes too little to exceed the scratch")
+    # one request whose chunk table alone (1.5M records of 24 bytes) is more than the array
+    # holds, whatever the split
+    n = 1_500_000
+    chunks = np.zeros(n, dtype=synth.CHUNK_DTYPE)
+    chunks["pool_offset"] = np.arange(n) % 1000
+    chunks["len"] = 1
+    chunks["p_tgt"] = np.arange(n)
+    indptr = np.array([0, n], dtype=np.int32)
+    B = 1
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: rejected first
     st = L.irm_mla_attn_decode_noalloc(
         dummy.data_ptr(), dummy.data_ptr(), B, 128, chunks.ctypes.data, indptr.ctypes.data,
