@@ -3,8 +3,9 @@ ABI.  It serves callers that cannot call cudaMalloc themselves -- a plugin insid
 application that owns the device memory pool, or code that must not allocate while a CUDA
 graph is being built -- so its split-KV scratch and copied chunk table live in a fixed array
 inside the library instead of a caller workspace.  It runs the same kernel with the same
-split as irm_mla_attn_decode, so on two calls in a row its output must equal the workspace
-decode's bit for bit (and both match the fp64 oracle within the parity tolerance).
+split as irm_mla_attn_decode whenever that split's scratch fits the array, so on two calls in
+a row its output must equal the workspace decode's bit for bit (and both match the fp64
+oracle within the parity tolerance); where it does not fit, it takes the split that does.
 
 This file is collected last on purpose, so that a run stopping at the first failure has
 already run every other test.  It must pass in a fresh process and after the other tests.
@@ -58,6 +59,33 @@ def test_noalloc_decode_matches_workspace_decode():
                                 case.indptr, synth.bits(case.kv_rows), SCALE, select=sel)
     got = out.float().cpu().numpy().astype(np.float64)[sel[:, 0], sel[:, 2]]
     assert rel_l2(got, O) <= TOL_REL_L2 and max_abs(got, O) <= TOL_MAX_ABS
+
+
+def test_noalloc_decode_within_its_scratch():
+    """The V3-shaped decode: the workspace decode's long-first split needs more scratch than the
+    array holds (two fp32 partials per request), so the no-allocation call takes the split
+    that fits, and still matches the fp64 oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import mla_position_independent_gb300 as irm
+    import oracle
+    oracle.build()
+    L = irm.lib()
+    case = synth.v3_decode(0, device="cuda")
+    table = irm.ChunkTable(case.chunks, case.indptr)
+    ql, qr = case.q_lat[:, 0].contiguous(), case.q_rope[:, 0].contiguous()
+    out = torch.full_like(case.q_lat[:, 0], float("nan"))
+    lse = torch.full(ql.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    assert _call_noalloc(L, case, table, ql, qr, out, lse) == 0, L.irm_last_error().decode()
+    torch.cuda.synchronize()
+    irm.decode_noalloc_status()
+    sel = np.array([[b, 0, h] for b in (0, 21, 63) for h in (0, 64, 127)])
+    O, Lo = oracle.mla_attention(synth.bits(case.q_lat), synth.bits(case.q_rope), case.chunks,
+                                 case.indptr, synth.bits(case.kv_rows), SCALE, select=sel)
+    got = out.float().cpu().numpy().astype(np.float64)[sel[:, 0], sel[:, 2]]
+    assert rel_l2(got, O) <= TOL_REL_L2 and max_abs(got, O) <= TOL_MAX_ABS
+    gl = lse.cpu().numpy().astype(np.float64)[sel[:, 0], sel[:, 2]]
+    assert np.max(np.abs(gl - Lo)) < 2e-2
 
 
 def test_noalloc_rejects_decode_larger_than_its_scratch():
