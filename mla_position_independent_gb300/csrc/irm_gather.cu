@@ -2,8 +2,9 @@
 // layout, cKV unchanged and k_r turned by R(delta) on the way ("Irminsul论文详解" §5: a
 // registry hit contributes (cKV, R(delta) k_r,base); §4: only the 64-d slice is touched).
 // Pure bandwidth: every row is read once (1152 B) and written once (1152 B) with 16-byte
-// vector accesses; one CTA walks one chunk at a time so the chunk's 32 (cos, sin) pairs
-// are computed once and the row addresses are contiguous on both sides.
+// vector accesses; a CTA walks its range of rows chunk by chunk, so each chunk's 32
+// (cos, sin) pairs are computed once per CTA and the row addresses are contiguous on both
+// sides.
 #include <cuda_runtime.h>
 
 #include "irm_common.cuh"
@@ -57,113 +58,149 @@ __global__ void __launch_bounds__(1024) row_start_kernel(const irm_chunk* __rest
 
 constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kMinRowsPerCta = 128;
+constexpr int kGatherCtasPerSm = 4;  // resident CTAs per SM (64 registers a thread at most)
 
-__global__ void __launch_bounds__(kGatherThreads) rotate_gather_kernel(const GatherArgs a) {
+// The CTAs share the batch's rows (requests laid end to end) in equal contiguous ranges, so
+// every CTA moves the same bytes whatever the chunk lengths (sharing whole chunks left the
+// CTAs that drew the last long chunks running alone at the end).  A CTA finds the chunk that
+// holds its first row, then walks the chunks in order, copying the part of each that lies
+// in its range; (cos, sin) are computed once per chunk it visits.
+__global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm) rotate_gather_kernel(const __grid_constant__ GatherArgs a) {
   __shared__ float cs_c[32], cs_s[32];
-  __shared__ int req_sh;
-  const int tid = threadIdx.x;
-  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
-    const irm_chunk ch = a.chunks[c];
-    const int32_t delta = ch.reused ? ch.p_tgt - ch.p_src : 0;
+  __shared__ int b_sh, c_sh;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t r_begin = (int64_t)blockIdx.x * a.total_rows / gridDim.x;
+  const int64_t r_end = (int64_t)(blockIdx.x + 1) * a.total_rows / gridDim.x;
+  if (r_begin >= r_end) return;
+  const int64_t* rowb = a.inline_rows ? a.rows : a.row_start;
+  if (tid < 32) {
+    // the request holding row r_begin: last b with rowb[b] <= r_begin (requests are non-empty)
+    int lo = 0, hi = a.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (rowb[mid] <= r_begin) lo = mid; else hi = mid;
+    }
+    // its chunk holding that row: last c with p_tgt <= r_begin - rowb[b], 32-fold per ballot
+    const int32_t t0 = (int32_t)(r_begin - rowb[lo]);
+    int cl = a.indptr[lo], ch = a.indptr[lo + 1];
+    while (ch - cl > 1) {
+      const int step = (ch - cl + 31) / 32;
+      const int c = cl + lane * step;
+      const bool le = c < ch && a.chunks[c].p_tgt <= t0;
+      const unsigned m = __ballot_sync(0xffffffffu, le);
+      const int k = m ? 31 - __clz((int)m) : 0;
+      cl = cl + k * step;
+      ch = min(ch, cl + step);
+    }
+    if (lane == 0) {
+      b_sh = lo;
+      c_sh = cl;
+    }
+  }
+  __syncthreads();
+  int b = b_sh;
+  int c = c_sh;
+  int64_t r = r_begin;
+  const int n_chunks = (int)a.n_chunks;
+  for (int guard = 0; r < r_end && c < n_chunks && b < a.B && guard < n_chunks; ++guard) {
+    const irm_chunk chk = a.chunks[c];
+    const int32_t delta = chk.reused ? chk.p_tgt - chk.p_src : 0;
+    const int64_t g0 = rowb[b] + chk.p_tgt;  // the chunk's first row in the batch
+    const int lo = (int)max((int64_t)0, r - g0);
+    const int hi = (int)min((int64_t)chk.len, r_end - g0);
     if (tid < 32) {
       float cc = 1.f, ss = 0.f;
       if (delta != 0) rope_cos_sin(delta, a.phase.F[tid], cc, ss);
       cs_c[tid] = cc;
       cs_s[tid] = ss;
     }
-    if (tid == 0) {  // owning request: last b with indptr[b] <= c
-      int lo = 0, hi = a.B;  // invariant indptr[lo] <= c < indptr[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (a.indptr[mid] <= c) lo = mid; else hi = mid;
-      }
-      req_sh = lo;
-    }
     __syncthreads();
-    const int b = req_sh;
-    const int len = ch.len;
     // The table in the workspace is the validated one; these checks only keep a table that
     // was overwritten meanwhile (calls overlapping on one workspace) inside every buffer.
-    bool src_ok = len > 0 && ch.p_tgt >= 0 && ch.pool_offset >= 0 && ch.pool_offset + len <= a.n_rows;
+    bool src_ok = chk.len > 0 && chk.p_tgt >= 0 && chk.pool_offset >= 0 && chk.pool_offset + chk.len <= a.n_rows &&
+                  g0 + chk.len <= a.total_rows;
     if (a.paged_out != nullptr)
-      src_ok = src_ok && (int64_t)ch.p_tgt + len <= (int64_t)a.max_pages * kPage;
-    int64_t r0 = 0;
-    if (a.out_src != nullptr && src_ok) {
-      r0 = a.row_start[b] + ch.p_tgt;
-      src_ok = r0 + len <= a.row_start[a.B];
-    }
+      src_ok = src_ok && (int64_t)chk.p_tgt + chk.len <= (int64_t)a.max_pages * kPage;
     if (!src_ok) {
       if (tid == 0) set_status(a.status, kDevErrBounds);
     }
-    if (a.out_src != nullptr && src_ok) {
-      for (int i = tid; i < len; i += kGatherThreads) {
-        a.out_src[r0 + i] = (int32_t)(ch.pool_offset + i);
-        a.out_delta[r0 + i] = delta;
-        a.out_pos_src[r0 + i] = ch.p_tgt + i - delta;
+    if (src_ok && hi > lo) {
+      const int len = hi - lo;
+      const int64_t pool0 = chk.pool_offset + lo;
+      const int32_t p0 = chk.p_tgt + lo;
+      if (a.out_src != nullptr) {
+        for (int i = tid; i < len; i += kGatherThreads) {
+          a.out_src[g0 + lo + i] = (int32_t)(pool0 + i);
+          a.out_delta[g0 + lo + i] = delta;
+          a.out_pos_src[g0 + lo + i] = p0 + i - delta;
+        }
       }
-    }
-    if (a.paged_out != nullptr && src_ok) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.kv) + ch.pool_offset * (kDRow / 8);
-      uint4* dst = reinterpret_cast<uint4*>(a.paged_out);
-      const int32_t* ptab = a.page_table + (int64_t)b * a.max_pages;
-      // cKV: 64 16-byte vectors per row; 4 rows per pass of 256 threads, kUnroll passes.
-      const int n_items = len * 64;
-      for (int i0 = 0; i0 < n_items; i0 += kGatherThreads * kUnroll) {
-        uint4 v[kUnroll];
-        int64_t d_off[kUnroll];
+      if (a.paged_out != nullptr) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.kv) + pool0 * (kDRow / 8);
+        uint4* dst = reinterpret_cast<uint4*>(a.paged_out);
+        const int32_t* ptab = a.page_table + (int64_t)b * a.max_pages;
+        // cKV: 64 16-byte vectors per row; 4 rows per pass of 256 threads, kUnroll passes.
+        const int n_items = len * 64;
+        for (int i0 = 0; i0 < n_items; i0 += kGatherThreads * kUnroll) {
+          uint4 v[kUnroll];
+          int64_t d_off[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int it = i0 + u * kGatherThreads + tid;
-          d_off[u] = -1;
-          if (it < n_items) {
-            const int row = it >> 6, vec = it & 63;
-            const int t = ch.p_tgt + row;
-            const int32_t page = ptab[t / kPage];
-            if (page >= 0 && page < a.n_pages) {
-              v[u] = __ldcs(src + (int64_t)row * (kDRow / 8) + vec);
-              d_off[u] = ((int64_t)page * kPage + (t % kPage)) * (kDRow / 8) + vec;
-            } else {
-              set_status(a.status, kDevErrBounds);
+          for (int u = 0; u < kUnroll; ++u) {
+            const int it = i0 + u * kGatherThreads + tid;
+            d_off[u] = -1;
+            if (it < n_items) {
+              const int row = it >> 6, vec = it & 63;
+              const int t = p0 + row;
+              const int32_t page = ptab[t / kPage];
+              if (page >= 0 && page < a.n_pages) {
+                v[u] = __ldcs(src + (int64_t)row * (kDRow / 8) + vec);
+                d_off[u] = ((int64_t)page * kPage + (t % kPage)) * (kDRow / 8) + vec;
+              } else {
+                set_status(a.status, kDevErrBounds);
+              }
             }
           }
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u)
+            if (d_off[u] >= 0) __stcs(dst + d_off[u], v[u]);
         }
+        // k_r: a thread takes 16-byte vectors 64+pv and 68+pv of a row (NeoX: pairs 8pv..8pv+7,
+        // first elements then partners; interleaved: the 4 pairs inside each vector).
+        const int n_kr = len * 4;
+        for (int it = tid; it < n_kr; it += kGatherThreads) {
+          const int row = it >> 2, pv = it & 3;
+          const int t = p0 + row;
+          const int32_t page = ptab[t / kPage];
+          if (page < 0 || page >= a.n_pages) continue;  // recorded by the cKV loop
+          const uint4* s = src + (int64_t)row * (kDRow / 8) + 64;
+          uint4 x = __ldcs(s + pv), y = __ldcs(s + 4 + pv);
+          if (delta != 0) {
+            float c8[8], s8[8];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (d_off[u] >= 0) __stcs(dst + d_off[u], v[u]);
-      }
-      // k_r: a thread takes 16-byte vectors 64+pv and 68+pv of a row (NeoX: pairs 8pv..8pv+7,
-      // first elements then partners; interleaved: the 4 pairs inside each vector).
-      const int n_kr = len * 4;
-      for (int it = tid; it < n_kr; it += kGatherThreads) {
-        const int row = it >> 2, pv = it & 3;
-        const int t = ch.p_tgt + row;
-        const int32_t page = ptab[t / kPage];
-        if (page < 0 || page >= a.n_pages) continue;  // recorded by the cKV loop
-        const uint4* s = src + (int64_t)row * (kDRow / 8) + 64;
-        uint4 x = __ldcs(s + pv), y = __ldcs(s + 4 + pv);
-        if (delta != 0) {
-          float c8[8], s8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = pair_index(a.interleaved, pv, pv + 4, e);
-            c8[e] = cs_c[j];
-            s8[e] = cs_s[j];
+            for (int e = 0; e < 8; ++e) {
+              const int j = pair_index(a.interleaved, pv, pv + 4, e);
+              c8[e] = cs_c[j];
+              s8[e] = cs_s[j];
+            }
+            rotate_pairs8_any(x, y, c8, s8, a.interleaved);
           }
-          rotate_pairs8_any(x, y, c8, s8, a.interleaved);
+          uint4* d = dst + ((int64_t)page * kPage + (t % kPage)) * (kDRow / 8) + 64;
+          __stcs(d + pv, x);
+          __stcs(d + 4 + pv, y);
         }
-        uint4* d = dst + ((int64_t)page * kPage + (t % kPage)) * (kDRow / 8) + 64;
-        __stcs(d + pv, x);
-        __stcs(d + 4 + pv, y);
       }
     }
-    __syncthreads();  // cs_c / req_sh reused by the next chunk
+    __syncthreads();  // cs_c / cs_s are reused by the next chunk
+    r = max(r, g0 + (chk.len > 0 ? chk.len : 1));
+    if (++c >= a.indptr[b + 1]) ++b;
   }
 }
 
 // Copies up to three host arrays into a device block: the sources are page-locked host memory
 // that the GPU reads directly (device-accessible addresses), in 4-byte words (every array is a
 // whole number of them).  One launch instead of one copy-engine transfer per array.
-__global__ void __launch_bounds__(256) host_copy_kernel(HostCopyArgs a) {
+__global__ void __launch_bounds__(256) host_copy_kernel(const __grid_constant__ HostCopyArgs a) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int p = 0; p < a.n; ++p) {
     const uint32_t* __restrict__ src = static_cast<const uint32_t*>(a.src[p]);
@@ -189,9 +226,11 @@ cudaError_t launch_row_start(const irm_chunk* chunks, const int32_t* indptr, int
 }
 
 cudaError_t launch_rotate_gather(const GatherArgs& a, int num_sms, cudaStream_t stream) {
-  if (a.n_chunks <= 0) return cudaSuccess;
-  const int64_t want = (int64_t)num_sms * 8;
-  const int grid = (int)(a.n_chunks < want ? a.n_chunks : want);
+  if (a.n_chunks <= 0 || a.total_rows <= 0) return cudaSuccess;
+  // one wave of resident CTAs, each with an equal share of the rows
+  const int64_t want = (int64_t)num_sms * kGatherCtasPerSm;
+  const int64_t by_rows = (a.total_rows + kMinRowsPerCta - 1) / kMinRowsPerCta;
+  const int grid = (int)(by_rows < want ? by_rows : want);
   rotate_gather_kernel<<<grid, kGatherThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -740,7 +740,19 @@ irm_status irm_assemble_kv_rope(const irm_chunk* chunks_host, const int32_t* ind
   g.out_pos_src = out_pos_src;
   std::memcpy(g.phase.F, phaseF, sizeof g.phase.F);
   g.interleaved = interleaved;
-  if (plan_out) {
+  // rows of the requests before each one: in the launch parameters for up to 256 requests,
+  // else computed on the device from the copied table
+  g.total_rows = 0;
+  for (int b = 0; b < B; ++b) g.total_rows += info.ctx[b];
+  g.inline_rows = B + 1 <= irm::kInlineIndptr ? 1 : 0;
+  if (g.inline_rows) {
+    int64_t t = 0;
+    for (int b = 0; b < B; ++b) {
+      g.rows[b] = t;
+      t += info.ctx[b];
+    }
+    g.rows[B] = t;
+  } else {
     int64_t* row_start =
         reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + IRM_WORKSPACE_HEADER + tab_bytes);
     g.row_start = row_start;

@@ -22,7 +22,10 @@ struct GatherArgs {
   int64_t n_pages;
   const int32_t* page_table;
   int max_pages;
-  const int64_t* row_start;  // [B+1], required when out_src != nullptr
+  const int64_t* row_start;  // device [B+1]: rows of the requests before b (unused with inline_rows)
+  int inline_rows;           // 1: row_start is `rows` below (B <= 256)
+  int64_t rows[257];
+  int64_t total_rows;        // rows of all requests: the CTAs share them in equal contiguous ranges
   int32_t* out_src;
   int32_t* out_delta;
   int32_t* out_pos_src;

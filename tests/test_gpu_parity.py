@@ -84,6 +84,36 @@ def test_assemble_multi_request(oracle_mod):
     _assemble_and_check(case, oracle_mod)
 
 
+def test_assemble_long_chunks_split_across_ctas(oracle_mod):
+    """Chunks far longer than a CTA's share of the rows: the CTAs split the batch's rows in
+    equal ranges, so many of them copy parts of one chunk (and a range can end inside one)."""
+    case = synth.custom_case([[(0, 32, 0, 0), (40, 30000, 100, 1), (30100, 7, 9000, 1)],
+                              [(31000, 5000, 0, 0), (36100, 3333, -777, 1)]],
+                             n_rows=40000, n_q=0, pages=True)
+    _assemble_and_check(case, oracle_mod)
+
+
+def test_assemble_many_requests(oracle_mod):
+    """300 requests (more than the launch parameters carry row offsets for, so the kernel
+    reads them from the device): ragged lengths, reused and fresh chunks, paged output and
+    the per-row plan."""
+    rng = np.random.default_rng(61)
+    n_rows = 9000
+    reqs = []
+    for b in range(300):
+        p, req = 0, [(int(rng.integers(0, n_rows - 32)), 32, 0, 0)]
+        p = 32
+        for _ in range(int(rng.integers(0, 4))):
+            n = int(rng.integers(1, 300))
+            reused = rng.random() < 0.7
+            d = int(rng.integers(-5000, 5001)) if reused else 0
+            req.append((int(rng.integers(0, n_rows - n)), n, p - d, int(reused)))
+            p += n
+        reqs.append(req)
+    case = synth.custom_case(reqs, n_rows=n_rows, n_q=0, pages=True)
+    _assemble_and_check(case, oracle_mod)
+
+
 def test_rotate_gather_64k_rows_full(oracle_mod):
     case = synth.rotate_gather_case(1 << 16, seed=0, device="cuda")
     r = _assemble_and_check(case, oracle_mod)
