@@ -210,17 +210,17 @@ __device__ __forceinline__ StreamTab stream_tab(const CdcArgs& a) {
 
 // Pass 1: W warps per segment (two segments per CTA; each segment's warps sync on their own
 // named barrier, never the whole block).
-// Hashing: the window [p0, p_end) is cut into steps of 128 positions, lane l holding the 4
-// consecutive positions 4l .. 4l+3 of a step.  With g0..g3 their Gear words, the lane's block
-// contributes L = 8 g0 + 4 g1 + 2 g2 + g3 to the hash at its last position, and a 4-step
-// shuffle scan X_l = sum_{j <= l} L_j 2^(4 (l - j)) gives the hash there:
-// h(4l+3) = h_prev 2^(4l+4) + X_l (terms shifted by 64 or more vanish).  The lane then steps
-// h = 2 h + g through its own 4 positions from h(4l-1).  The step before the segment (whose
-// 128 positions include the 64 the first hash depends on) is hashed first, to warm the hash
-// up; each step's tokens are loaded one step ahead.  The W warps of a segment hash a W-th of
-// its steps each (each but the first warming up on the step before its share); the first
-// walks.  W = 4 when the batch has few segments for the GPU (more warps to hide the 64-bit
-// arithmetic's latency), else 2 (less re-hashed warm-up).
+// Hashing: the window [p0, p_end) is cut into steps of 256 positions, lane l holding the 8
+// consecutive positions 8l .. 8l+7 of a step.  With g0..g7 their Gear words, the lane's block
+// contributes L = sum_e g_e 2^(7-e) to the hash at its last position (Horner), and a 3-step
+// shuffle scan X_l = sum_{j <= l} L_j 2^(8 (l - j)) gives the hash there:
+// h(8l+7) = h_prev 2^(8l+8) + X_l (terms shifted by 64 or more vanish).  The lane then steps
+// h = 2 h + g through its own 8 positions from h(8l-1).  A warp's first step needs the hash
+// at the position before it, h_prev = sum_{k<64} G[x_{q-1-k}] 2^k: lane l takes positions
+// q-64+2l and q-63+2l and a butterfly sums the 32 shifted pairs.  Each step's tokens are
+// loaded one step ahead (two 16-byte loads a lane when the stream is 16-byte aligned).  The
+// W warps of a segment hash a W-th of its steps each; the first walks.  W = 4 when the batch
+// has few segments for the GPU (more warps to hide the 64-bit arithmetic's latency), else 2.
 static_assert(kSegsPerCta == 2, "seg_sync");
 // Named barrier of a segment's warps (ids fixed at compile time, so that the kernel uses only
 // the barriers it names).
@@ -258,65 +258,87 @@ __global__ void __launch_bounds__(32 * W * kSegsPerCta) cdc_segment_kernel(const
   const uint64_t* gear = a.gear;
   const uint64_t gseed = a.gear_seed;
   const int vocab = a.vocab, bits = a.bits, mode = a.mode;
-  // ---- candidate bitmask of the window
+  // ---- candidate bitmask of the window (stream positions fit in 32 bits)
   {
-    const int nsteps_all = (int)((p_end - p0 + 127) / 128);
-    const int rbeg = half * nsteps_all / kSegWarpsPer, nsteps = (half + 1) * nsteps_all / kSegWarpsPer;
+    constexpr int kStep = 256;
+    const int len32 = (int)len, p032 = (int)p0;
+    const int nsteps_all = (int)((p_end - p0 + kStep - 1) / kStep);
+    const int rbeg = half * nsteps_all / kSegWarpsPer, rend = (half + 1) * nsteps_all / kSegWarpsPer;
+    const bool vec = (reinterpret_cast<uintptr_t>(tok) & 15u) == 0;
     int bad = 0;
-    uint64_t h_prev = 0;
-    int r = (rbeg > 0 || p0 > 0) ? rbeg - 1 : 0;
-    int32_t cur[4];
-    auto load_step = [&](int rr, int32_t (&t4)[4]) {
-      const int64_t p = p0 + 128 * (int64_t)rr + 4 * lane;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) t4[e] = p + e < len ? __ldg(tok + p + e) : -1;
+    auto word = [&](int32_t x) -> uint64_t {
+      if ((uint32_t)x >= (uint32_t)vocab) {
+        bad = 1;
+        return 0ull;
+      }
+      return gear != nullptr ? __ldg(gear + x) : splitmix_word(gseed, x);
     };
-    load_step(r, cur);
-    for (; r < nsteps; ++r) {
-      int32_t nxt[4];
-      if (r + 1 < nsteps) load_step(r + 1, nxt);
-      const int64_t p = p0 + 128 * (int64_t)r + 4 * lane;  // the lane's first position (>= 0)
-      uint64_t gv[4];
+    auto load_step = [&](int rr, int32_t (&t8)[8]) {
+      const int pb = p032 + kStep * rr + 8 * lane;
+      if (vec && pb + 8 <= len32) {
+        const int4 u = __ldg(reinterpret_cast<const int4*>(tok + pb));
+        const int4 v = __ldg(reinterpret_cast<const int4*>(tok + pb + 4));
+        t8[0] = u.x; t8[1] = u.y; t8[2] = u.z; t8[3] = u.w;
+        t8[4] = v.x; t8[5] = v.y; t8[6] = v.z; t8[7] = v.w;
+      } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int32_t x = cur[e];
-        if (p + e >= len) {
-          gv[e] = 0ull;
-        } else if (x < 0 || x >= vocab) {
-          bad = 1;
-          gv[e] = 0ull;
-        } else {
-          gv[e] = gear != nullptr ? __ldg(gear + x) : splitmix_word(gseed, x);
-        }
+        for (int e = 0; e < 8; ++e) t8[e] = pb + e < len32 ? __ldg(tok + pb + e) : 0;
       }
-      uint64_t xs = (gv[0] << 3) + (gv[1] << 2) + (gv[2] << 1) + gv[3];
+    };
+    uint64_t h_prev = 0;
+    const int q = p032 + kStep * rbeg;  // the warp's first position
+    if (rbeg < rend && q > 0) {
+      const int pa = q - 64 + 2 * lane;
+      const uint64_t ga = pa >= 0 ? word(__ldg(tok + pa)) : 0ull;
+      const uint64_t gb = pa + 1 >= 0 ? word(__ldg(tok + pa + 1)) : 0ull;
+      uint64_t t = ((ga << 1) + gb) << (62 - 2 * lane);  // positions q-1-(63-2l) and q-1-(62-2l)
 #pragma unroll
-      for (int d = 1; d < 16; d <<= 1) {  // shifts 4, 8, 16, 32 (the shift-64 step vanishes)
+      for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(kFull, t, o);
+      h_prev = t;
+    }
+    int32_t cur[8];
+    if (rbeg < rend) load_step(rbeg, cur);
+    for (int r = rbeg; r < rend; ++r) {
+      int32_t nxt[8];
+      if (r + 1 < rend) load_step(r + 1, nxt);
+      const int pb = p032 + kStep * r + 8 * lane;  // the lane's first position
+      uint64_t gv[8];
+      if (pb + 8 <= len32) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gv[e] = word(cur[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gv[e] = pb + e < len32 ? word(cur[e]) : 0ull;
+      }
+      uint64_t xs = gv[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) xs = (xs << 1) + gv[e];
+#pragma unroll
+      for (int d = 1; d < 8; d <<= 1) {  // shifts 8, 16, 32 (the shift-64 step vanishes)
         const uint64_t y = __shfl_up_sync(kFull, xs, d);
-        if (lane >= d) xs += y << (4 * d);
+        if (lane >= d) xs += y << (8 * d);
       }
-      const uint64_t h_last = (lane < 15 ? (h_prev << (4 * lane + 4)) : 0ull) + xs;
-      uint64_t h = __shfl_up_sync(kFull, h_last, 1);  // hash at position 4l - 1
+      const uint64_t h_last = (lane < 7 ? (h_prev << (8 * lane + 8)) : 0ull) + xs;
+      uint64_t h = __shfl_up_sync(kFull, h_last, 1);  // hash at position 8l - 1
       if (lane == 0) h = h_prev;
-      uint32_t nib = 0;
+      uint32_t byte = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         h = (h << 1) + gv[e];
-        if (p + e < len && cdc_candidate(h, bits, mode)) nib |= 1u << e;
+        if (pb + e < len32 && cdc_candidate(h, bits, mode)) byte |= 1u << e;
       }
-      // word j of the step collects the nibbles of lanes 8j .. 8j+7
-      uint32_t wv = nib << (4 * (lane & 7));
+      // word j of the step collects the bytes of lanes 4j .. 4j+3
+      uint32_t wv = byte << (8 * (lane & 3));
       wv |= __shfl_xor_sync(kFull, wv, 1);
       wv |= __shfl_xor_sync(kFull, wv, 2);
-      wv |= __shfl_xor_sync(kFull, wv, 4);
-      if (r >= rbeg && (lane & 7) == 0) {
-        const int w = 4 * r + (lane >> 3);
+      if ((lane & 3) == 0) {
+        const int w = 8 * r + (lane >> 2);
         if (w < nwin) win[w] = wv;
         if (w < seg_words) gw[w0 + w] = wv;  // the segment's own words, for the resolve pass
       }
       h_prev = __shfl_sync(kFull, h_last, 31);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
+      for (int e = 0; e < 8; ++e) cur[e] = nxt[e];
     }
     if (__any_sync(kFull, bad) && lane == 0) set_status(a.status, kDevErrBounds);
   }
@@ -354,6 +376,9 @@ __global__ void __launch_bounds__(32 * W * kSegsPerCta) cdc_segment_kernel(const
   }
 }
 
+// Brings the 128-byte line holding p into the SM's L1 (no fault, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
 // One segment of the chain, warp-collective: entering segment k of stream s at position t (the
 // first chunk start at or after the segment start), re-walk until a chunk ends where a
 // speculative one does, then take the rest of the speculative chunks.  Returns the chunks the
@@ -367,7 +392,7 @@ struct SegCtx {
 };
 // The chunks a counting walk re-walked before it met the speculative chain (start, length,
 // fingerprint), kept in shared memory so that placing them needs no second walk.
-constexpr int kRec = 8;
+constexpr int kRec = 8;  // at most 8: the recorded chunks are fingerprinted by 4-lane groups of one warp
 struct SegRec {
   int32_t start[kRec], len[kRec];
   uint64_t hash[kRec];
@@ -403,15 +428,9 @@ __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_
           const uint64_t h = chunk_xxh64_x4(x.tok + t, (int)(e - t + 1), a.seed, lane, 0xfu, 0);
           if (lane == 0) a.chunk_hash[out + count] = h;
         }
-      } else if (rec != nullptr && count < kRec) {
-        uint64_t h = 0;
-        if (a.chunk_hash != nullptr && lane < 4)
-          h = chunk_xxh64_x4(x.tok + t, (int)(e - t + 1), a.seed, lane, 0xfu, 0);
-        if (lane == 0) {
-          rec->start[count] = (int32_t)t;
-          rec->len[count] = (int32_t)(e - t + 1);
-          rec->hash[count] = h;
-        }
+      } else if (rec != nullptr && count < kRec && lane == 0) {
+        rec->start[count] = (int32_t)t;  // fingerprinted after the walk, all at once
+        rec->len[count] = (int32_t)(e - t + 1);
       }
       ++count;
       t = (int64_t)e + 1;
@@ -434,9 +453,25 @@ __device__ int walk_segment(const CdcArgs& a, const SegCtx& x, int64_t k, int64_
       if (met || !found) break;
     }
   }
-  if (rec != nullptr && lane == 0) {
-    rec->n = count <= kRec ? count : -1;
-    rec->p = p;
+  if (rec != nullptr) {
+    // fingerprints of the recorded chunks, four lanes per chunk (kRec <= 8), each chunk's
+    // tokens asked for at once first (a chunk of max_len tokens is several batches of loads)
+    __syncwarp();
+    const int j = lane >> 2, q = lane & 3;
+    if (j < min(count, kRec)) {
+      uint64_t h = 0;
+      if (a.chunk_hash != nullptr) {
+        const int32_t* ct = x.tok + rec->start[j];
+        const int n = rec->len[j];
+        for (int i = 32 * q; i < n; i += 128) prefetch_l1(ct + i);
+        h = chunk_xxh64_x4(ct, n, a.seed, q, 0xfu << (lane & ~3), lane & ~3);
+      }
+      if (q == 0) rec->hash[j] = h;
+    }
+    if (lane == 0) {
+      rec->n = count <= kRec ? count : -1;
+      rec->p = p;
+    }
   }
   if (!met) {
     *exit = t;
@@ -488,7 +523,7 @@ __device__ void emit_recorded(const CdcArgs& a, const SegCtx& x, int64_t k, cons
 }
 
 // Pass 2: one CTA per stream, kResWarps segments at a time (see the header).
-__global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __grid_constant__ CdcArgs a) {
+__global__ void __launch_bounds__(kResWarps * 32, 2) cdc_resolve_kernel(const __grid_constant__ CdcArgs a) {
   __shared__ int cnt_sh[kResWarps];
   __shared__ int met_sh[kResWarps];
   __shared__ int64_t exit_sh[kResWarps];
@@ -505,6 +540,13 @@ __global__ void __launch_bounds__(kResWarps * 32) cdc_resolve_kernel(const __gri
   int64_t done = 0;  // chunks written so far
   for (int64_t g0 = 0; g0 < nseg; g0 += kResWarps) {
     const int64_t k = g0 + warp;
+    if (k < nseg) {  // the segment's speculative chain and its fingerprints, asked for at once
+      const int64_t gseg = x.gb + k, cap = a.spec_cap;
+      if (32 * (int64_t)lane < cap) prefetch_l1(a.spec_ends + gseg * cap + 32 * (int64_t)lane);
+      if (a.chunk_hash != nullptr && 16 * (int64_t)lane < cap)
+        prefetch_l1(a.spec_hash + gseg * cap + 16 * (int64_t)lane);
+      if (lane == 0) prefetch_l1(a.spec_count + gseg);
+    }
     // the segment's entry, assuming the previous segment met its speculative chain
     const int64_t entry = k == 0 ? 0 : (k < nseg ? (int64_t)a.spec_exit[x.gb + k - 1] : 0);
     int64_t ex = 0;
