@@ -510,7 +510,24 @@ def assemble_host(wl: Workload, rounds: int = 3):
                 note="host, one thread, ctypes call per request included")
 
 
+# Content-defined chunking is integer arithmetic.  Its algorithmic work, in 32-bit integer
+# operations per token: the SplitMix64 Gear word (a 64 x 32-bit multiply-add 2, the seed add 2,
+# three 64-bit xor-shifts 4 each, two 64 x 64-bit multiplies 3 each: 22), the Gear step
+# h = 2 h + G (shift 2, add 2), the boundary test (2), and an eighth of an xxHash64 stripe
+# (four lanes of multiply 3, add 2, rotate 2, multiply 3 per 32 bytes: 5 per token): 33.
+CDC_INT_OPS_PER_TOKEN = 33
+# Its peak: every scheduler issuing one 32-bit integer instruction for 32 lanes each clock,
+# 152 SMs x 4 schedulers x 32 lanes x 2070 MHz (the maximum SM clock).
+ALU_PEAK_GOPS = 152 * 4 * 32 * 2.07
+ALU_PEAK_NOTE = "derived: 152 SMs x 4 schedulers x 32 lanes x 2070 MHz, one 32-bit integer op per lane per clock"
+
+
 def roofline(wl: Workload, ms: float, pk):
+    if wl.kind == "cdc":
+        ach = CDC_INT_OPS_PER_TOKEN * wl.n_tokens / (ms * 1e-3) / 1e9
+        return dict(bound="alu", achieved=round(ach, 1), peak=round(ALU_PEAK_GOPS, 1), unit="Gop/s",
+                    frac=round(ach / ALU_PEAK_GOPS, 4), peak_source=ALU_PEAK_NOTE,
+                    ops_per_token=CDC_INT_OPS_PER_TOKEN)
     if wl.kind == "prefill":
         ach = wl.flops / (ms * 1e-3) / 1e12
         return dict(bound="tensor", achieved=round(ach, 2), peak=pk["bf16"], unit="TFLOP/s",
@@ -736,11 +753,11 @@ def measure(name, steps, warmup, pk, device_index, rank, want_cpu, want_e2e=True
     val, unit = _value_unit(wl, ms)
     ent = dict(value=round(val, 4), unit=unit, ms_per_step=round(ms, 5), steps=steps,
                clocks=clocks, description=DESCR.get(name))
+    r = roofline(wl, ms, pk)
+    r["kernel"] = wl.kernel_name()
+    r["traffic"] = traffic_for(name)
+    ent["roofline"] = r
     if wl.kind != "cdc":
-        r = roofline(wl, ms, pk)
-        r["kernel"] = wl.kernel_name()
-        r["traffic"] = traffic_for(name)
-        ent["roofline"] = r
         ent["table_bytes"] = wl.table_bytes
     if wl.kind == "gather":
         ent["rows_per_s"] = round(wl.ctx_total / (ms * 1e-3), 1)
@@ -832,7 +849,7 @@ def main():
     val, unit = _value_unit(wl, ms)
     value = world * val
     rf = roofline(wl, ms, pk)
-    rf["peak_source"] = pk["src"]
+    rf.setdefault("peak_source", pk["src"])
     rf["kernel"] = wl.kernel_name()
     rf["traffic"] = traffic_for(args.workload)
     e2e_d = None
