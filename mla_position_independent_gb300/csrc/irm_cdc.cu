@@ -9,12 +9,12 @@
 //   else at the stream's end.
 //
 // Passes (two kernels):
-//   1. cdc_segment_kernel, four warps per 4096-token segment of a stream: they hash the
-//      segment and the max_len - 1 positions after it (a chunk starting in the segment ends
-//      there at the latest) into a candidate bitmask in shared memory (the segment's own words
-//      also go to global memory); one of them walks the chunks speculatively from the segment
-//      start (one ballot per chunk: next_end), and all four fingerprint those chunks while
-//      their tokens are hot.
+//   1. cdc_segment_kernel, W warps (2 or 4) per 4096-token segment of a stream: they hash
+//      the segment and the max_len - 1 positions after it (a chunk starting in the segment
+//      ends there at the latest) into a candidate bitmask in shared memory (the segment's own
+//      words also go to global memory); one of them walks the chunks speculatively from the
+//      segment start (one ballot per chunk: next_end), and all W fingerprint those chunks
+//      while their tokens are hot.
 //   2. cdc_resolve_kernel, one CTA per stream.  A walk entering a segment anywhere meets the
 //      segment's speculative chain within a chunk or two, after which both agree; the segment
 //      then exits where its speculative walk does.  So each warp takes one segment, enters it
