@@ -809,14 +809,15 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       if (q == 0) a.glse[((int64_t)b * G + g) * H + h] = lse2;
     }
   }
+  cluster_arrive();  // this CTA has finished reading its peers' shared memory (waited for at exit)
   if (threadIdx.x == 0) IRM_TL(TL_MERGED);
   if (G > 1) {
     // the last of the G clusters to finish slice crank merges it (threadfence reduction; the
     // counter resets itself so the workspace stays reusable)
     int* last_sh = reinterpret_cast<int*>(smem + kOffWfail);
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+      __threadfence();  // cumulative: the CTA's partial stores, ordered before it by the barrier
       int* cnt = a.counters + (int64_t)b * C + crank;
       const int done = atomicAdd(cnt, 1);
       *last_sh = done == G - 1;
@@ -861,8 +862,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
     }
   }
   if (threadIdx.x == 0) IRM_TL(TL_END);
-  cluster_arrive();  // peers are done reading this CTA's shared memory
-  cluster_wait();
+  cluster_wait();  // peers are done reading this CTA's shared memory
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols(H));
