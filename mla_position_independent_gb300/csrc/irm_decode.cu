@@ -53,12 +53,13 @@ namespace irm {
 
 // Timeline instrumentation, compiled only into the separately built timeline library
 // (build.build(timeline=True) defines IRM_TIMELINE): the CTAs of request 0 stamp %globaltimer
-// at the phases of a decode (kernel entry, set-up, each tile's scores and P.V issued, pipeline
-// end, cluster merge, end) into a device array that irm_timeline_read() copies out.  The
-// product library contains none of it.
+// at the phases of a decode (kernel entry, set-up and its steps, each tile's scores and P.V
+// issued, pipeline end, cluster merge, end) into a device array that irm_timeline_read()
+// copies out.  The product library contains none of it.
 #ifdef IRM_TIMELINE
 constexpr int kTlCtas = 64, kTlTiles = 64;
-enum : int { TL_ENTRY, TL_SETUP, TL_PIPE_END, TL_PARKED, TL_CLUSTER, TL_MERGED, TL_END, TL_N };
+enum : int { TL_ENTRY, TL_SETUP, TL_PIPE_END, TL_PARKED, TL_CLUSTER, TL_MERGED, TL_END,
+              TL_SPLIT, TL_TMEM, TL_MAP, TL_ISSUED, TL_N };  // the last four: set-up steps
 __device__ unsigned long long g_tl_cta[kTlCtas][TL_N];
 __device__ unsigned long long g_tl_tile[kTlCtas][kTlTiles][3];  // data landed, S issued, P.V issued
 #define IRM_TL(ev)                                                                        \
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   const int kb = (int)((int64_t)split * kv_tiles / (C * G));
   const int ke = (int)((int64_t)(split + 1) * kv_tiles / (C * G));
   const int ntiles = ke - kb;
+  if (threadIdx.x == 0) IRM_TL(TL_SPLIT);
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBars + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
   if (warp == kMmaWarp) {
     tmem_alloc(sb + kOffTmemPtr, tmem_cols(H));
     tmem_relinquish();
+    if (lane == 0) IRM_TL(TL_TMEM);
   }
 
   // ---- start-up work that needs no mbarrier: while the barriers and TMEM are being set up,
@@ -329,6 +332,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
       cw.build_map(kb * kBN, ctx, a.n_rows, map_src, map_delta, a.status, lane);
     }
     __syncwarp();
+    if (lane == 0) IRM_TL(TL_MAP);
     named_bar_arrive(2, kLoaderThreads + 32);  // tile 0's map is in slot 0
   } else if (is_loader) {
     named_bar_sync(2, kLoaderThreads + 32);
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(Roles<H>::kThreads, 1) mla_decode_kernel(const
           cp_async_16(ub + pair_offset(r, 1u, (uint32_t)chk), rowp[i] + (2 * pr + 1) * 64, nb[i]);
         }
       }
+      if (tp == 0) IRM_TL(TL_ISSUED);
     }
   }
   tc_fence_before();

@@ -10,7 +10,9 @@ stamps from the CTAs of request 0) and prints, as medians over the repetitions:
     step;
   - the kernel span (first CTA entry to last CTA end) and its phases: set-up, first tile's
     data landed, its scores issued, the steady-state period per tile, the pipeline end,
-    the in-cluster merge and the end (after the cross-cluster merge).
+    the in-cluster merge and the end (after the cross-cluster merge);
+  - the set-up's steps, each from its CTA's own entry: the split's chunk range known (launch
+    arguments read), TMEM allocated, tile 0's row map built, its copies issued.
 The stamps cost a few global stores per phase; the step times come from the same build.
 """
 from __future__ import annotations
@@ -24,8 +26,9 @@ import torch
 
 from . import binding, build, synth
 
-N_CTAS, N_TILES, N_EV = 64, 64, 7
-EV = ["entry", "setup", "pipe_end", "parked", "cluster_barrier", "cluster_merged", "end"]
+N_CTAS, N_TILES, N_EV = 64, 64, 11
+EV = ["entry", "setup", "pipe_end", "parked", "cluster_barrier", "cluster_merged", "end",
+      "split_known", "tmem_allocated", "tile0_map_built", "tile0_copies_issued"]
 
 
 def _graph(fn, stream):
@@ -107,7 +110,10 @@ def main():
         nt = int((t[0, :, 1] > 0).sum())
         s_issue = np.median(us(t[:, :nt, 1]), axis=0)  # per tile, median over CTAs
         period = float(np.median(np.diff(s_issue[1:]))) if nt > 2 else float("nan")
-        rows.append(dict(span=us(c[:, 6].max()), setup=np.median(us(c[:, 1])),
+        own = lambda j: float(np.median((c[:, j] - c[:, 0]) / 1e3))  # from each CTA's own entry
+        rows.append(dict(split_known=own(7), tmem=own(8), map=own(9), issued=own(10), setup_own=own(1),
+                         entry_skew=float(np.median(us(c[:, 0]))),
+                         span=us(c[:, 6].max()), setup=np.median(us(c[:, 1])),
                          first_landed=np.median(us(t[:, 0, 0])), first_scores=s_issue[0],
                          period=period, tiles=nt, pipe_end=np.median(us(c[:, 2])),
                          pipe_end_max=us(c[:, 2].max()), cluster=np.median(us(c[:, 4])),
@@ -124,6 +130,11 @@ def main():
                    ("merged", "in-cluster merge done"), ("end", "end (after cross-cluster merge)")):
         print(f"    {lab:<38}{med[k]:8.2f}")
     print(f"  steady state: {med['period']:.2f} us per 64-row tile over {int(med['tiles'])} tiles per CTA")
+    print(f"  set-up, from each CTA's own entry (median CTA entry {med['entry_skew']:.2f} after the first):")
+    for k, lab in (("split_known", "split's chunk range and tiles known"), ("tmem", "TMEM allocated"),
+                   ("map", "tile 0's row map built"), ("issued", "tile 0's copies issued"),
+                   ("setup_own", "block-wide set-up barrier passed")):
+        print(f"    {lab:<38}{med[k]:8.2f}")
 
 
 if __name__ == "__main__":
